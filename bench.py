@@ -1,0 +1,403 @@
+"""Benchmark: causal GQA prefill TFLOP/s (headline) plus paged-decode and
+merge GB/s, on the synthetic Qwen3-8B attention workloads, against the
+measured GB300 rooflines.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+A step is one fused causal prefill (rlk_attn_prefill) over the varlen batch
+{4096, 3000, 1024, 777} tokens, Hq=32, Hkv=8, D=128, KV block 128, with the
+inputs resident in HBM; L2 is flushed (a 512 MB write) before every timed
+step and each step is timed with CUDA events on the launch stream.  `value`
+is algorithmic TFLOP/s = 4*D*Hq*sum(visible (row, key) pairs) / time.  `e2e`
+is the same metric through the public API from pinned host buffers
+(host->device copy of q/k/v, the prefill, device->host copy of out_bf16 and
+lse) inside the timed region.  Under torchrun every rank runs the same batch
+on its own GPU (weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle (FP64 definition) on the host cores on
+a bounded sample of the same workload's rows, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from deterministic_context_attention_gb300 import synth  # noqa: E402
+
+METRIC = "causal prefill TFLOP/s + paged decode GB/s (% GB300 roofline), bit-invariant"
+WORKLOAD = ("qwen3-8b causal GQA prefill, varlen {4096,3000,1024,777} (8897 tokens), Hq=32 Hkv=8 D=128, "
+            "bf16 q/k/v N(0,1) + RoPE theta=1e6, KV block 128, logical CP=1, out fp32+bf16 + lse")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def prefill_workload():
+    cfg = dict(synth.CFG_PREFILL)
+    prob = synth.prefill_problem(**cfg)
+    flops = synth.prefill_flops(prob.cu_q, prob.cu_k, prob.hq, prob.d)
+    return prob, flops
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step device time (ms) of fn() with an L2 flush before each step."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_gpu(args):
+    import torch
+    import deterministic_context_attention_gb300 as rlk
+    from deterministic_context_attention_gb300 import build as rbuild
+    from deterministic_context_attention_gb300 import device as dv
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        rbuild.build()
+    if dist is not None:
+        dist.barrier()
+    rlk.load()
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    prob, flops = prefill_workload()
+    q, k, v = dv.bf16_to_device(prob.q), dv.bf16_to_device(prob.k), dv.bf16_to_device(prob.v)
+    rows = q.shape[0]
+    p = rlk.make_params(4, 32, 8, 128, 1, rlk.ZIGZAG, prob.scale)
+    out = torch.empty((rows, 32, 128), dtype=torch.float32, device="cuda")
+    outb = torch.empty((rows, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, 32), dtype=torch.float32, device="cuda")
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        rlk.rlk_attn_prefill(p, q, k, v, prob.cu_q, prob.cu_k, -1, out, outb, lse, stream=stream)
+
+    clocks = Clocks(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    times = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    rlk.rlk_attn_check_device_error(stream)
+    ms = float(np.mean(times))
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * flops / (ms * 1e-3) / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+
+    # ---- end to end through the public API from pinned host buffers
+    qh = torch.from_numpy(synth.bf16_bits(prob.q).view(np.int16)).pin_memory()
+    kh = torch.from_numpy(synth.bf16_bits(prob.k).view(np.int16)).pin_memory()
+    vh = torch.from_numpy(synth.bf16_bits(prob.v).view(np.int16)).pin_memory()
+    outb_h = torch.empty((rows, 32, 128), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((rows, 32), dtype=torch.float32).pin_memory()
+    qd = torch.empty_like(qh, device="cuda")
+    kd = torch.empty_like(kh, device="cuda")
+    vd = torch.empty_like(vh, device="cuda")
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        rlk.rlk_attn_prefill(p, qd.view(torch.bfloat16), kd.view(torch.bfloat16), vd.view(torch.bfloat16),
+                             prob.cu_q, prob.cu_k, -1, None, outb, lse, stream=stream)
+        outb_h.copy_(outb, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_times = time_steps(torch, e2e_step, args.steps, args.warmup, flush, stream)
+    e2e_ms = float(np.mean(e2e_times))
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = outb_h.numel() * 2 + lse_h.numel() * 4
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        extras = measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 4 * world, "seq_len": "varlen 4096/3000/1024/777",
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "flushed (512 MB write) before every timed step", "flops_per_step": flops},
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 dense burst",
+                         "kernel": "rlk_fwd_kernel<128, fused>",
+                         "physical_frac": round(1.5 * achieved / peak, 4)},
+            "clocks": clk,
+            "wall_s_timed_region": round(wall, 3),
+        }
+        line.update(extras)
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args):
+    """Paged decode GB/s and merge GB/s (each against the measured HBM
+    roofline), states-producer and chunked-replay rates."""
+    res = {}
+    # ---- states (CP=1 plan) + merge on the prefill workload
+    p = rlk.make_params(4, 32, 8, 128, 1, rlk.ZIGZAG, prob.scale)
+    slabs, npairs = rlk.rlk_attn_plan_states(p, prob.cu_q, prob.cu_k, -1, 0)
+    so = torch.empty((npairs, 128), dtype=torch.float32, device="cuda")
+    sl = torch.empty((npairs,), dtype=torch.float32, device="cuda")
+    ds = dv.slabs_to_device(slabs)
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, prob.cu_q, prob.cu_k), dtype=torch.uint8,
+                     device="cuda")
+    rows = q.shape[0]
+    out = torch.empty((rows, 32, 128), dtype=torch.float32, device="cuda")
+    outb = torch.empty((rows, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, 32), dtype=torch.float32, device="cuda")
+    t_states = time_steps(torch, lambda: rlk.rlk_attn_prefill_states(p, q, k, v, prob.cu_q, prob.cu_k, -1, 0, so,
+                                                                      sl, stream=stream),
+                          args.steps, args.warmup, flush, stream)
+    t_merge = time_steps(torch, lambda: rlk.rlk_attn_merge_states(p, prob.cu_q, prob.cu_k, ds, len(slabs), so, sl,
+                                                                   out, outb, lse, ws, stream=stream),
+                         args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    merge_bytes = npairs * (128 * 4 + 4) + rows * 32 * (128 * 4 + 128 * 2 + 4) + len(slabs) * 32
+    ms_m = float(np.mean(t_merge))
+    ms_s = float(np.mean(t_states))
+    gbs = merge_bytes / (ms_m * 1e-3) / 1e9
+    res["merge"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms_m, 4), "bytes": int(merge_bytes),
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
+                    "note": "canonical fold of the CP=1 state table of the prefill workload (index kernel + fold kernel)"}
+    states_bytes = npairs * (128 * 4 + 4)
+    flops = synth.prefill_flops(prob.cu_q, prob.cu_k, 32, 128)
+    res["states"] = {"tflops": round(flops / (ms_s * 1e-3) / 1e12, 2), "ms": round(ms_s, 4),
+                     "write_gbs": round(states_bytes / (ms_s * 1e-3) / 1e9, 1), "state_bytes": int(states_bytes)}
+    del so, sl
+    torch.cuda.empty_cache()
+
+    # ---- paged decode: 64 sequences, ctx ~ U[512, 32768], 16-token pages in a permuted pool
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    ctx = synth.rng(3, synth.T_LENS).integers(512, 32769, size=64).astype(np.int32)
+    pages_per = (ctx + 15) // 16
+    n_pages = int(pages_per.sum())
+    perm = synth.rng(3, synth.T_PAGES).permutation(n_pages).astype(np.int32)
+    max_pages = int(pages_per.max())
+    pt = np.full((64, max_pages), -1, np.int32)
+    off = 0
+    for s in range(64):
+        pt[s, :pages_per[s]] = perm[off:off + pages_per[s]]
+        off += pages_per[s]
+    kp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    vp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    qd = torch.randn((64, 32, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    ptd = dv.i32_to_device(pt)
+    pd = rlk.make_params(64, 32, 8, 128)
+    dout = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
+    doutb = torch.empty((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+    dlse = torch.empty((64, 32), dtype=torch.float32, device="cuda")
+    t_dec = time_steps(torch, lambda: rlk.rlk_attn_decode_paged(pd, qd, kp, vp, n_pages, 16, ptd, max_pages, ctx, dout,
+                                                                 doutb, dlse, stream=stream),
+                       args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    dec_bytes = int(ctx.astype(np.int64).sum()) * 8 * 128 * 2 * 2 + 64 * 32 * 128 * (2 + 4 + 2) + 64 * 32 * 4 \
+        + int(pages_per.sum()) * 4
+    ms_d = float(np.mean(t_dec))
+    gbs = dec_bytes / (ms_d * 1e-3) / 1e9
+    res["decode"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms_d, 4), "bytes": dec_bytes,
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
+                     "workload": "64 seqs, ctx ~ U[512,32768] (seeded), 16-token pages, permuted pool, Hq32/Hkv8/D128",
+                     "sum_ctx": int(ctx.sum())}
+    del kp, vp
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(seconds_target):
+    """The oracle (FP64 definition, OpenMP) on a bounded sample of the prefill
+    workload's rows, in TFLOP/s of the rows it computed."""
+    import oracle
+    prob, _ = prefill_workload()
+    oracle.build()
+    rows = np.arange(0, prob.q.shape[0], 1, dtype=np.int64)
+    # visible keys per row (bottom-right causal)
+    vis = np.empty(len(rows), np.int64)
+    for s in range(len(prob.cu_q) - 1):
+        a, b = prob.cu_q[s], prob.cu_q[s + 1]
+        vis[a:b] = np.arange(1, b - a + 1)
+    # calibrate on a small sample, then size the sample for ~seconds_target
+    rng = np.random.default_rng(0)
+    cal = np.sort(rng.choice(rows, 64, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_f64(prob.q, prob.k, prob.v, prob.cu_q, prob.cu_k, prob.scale, rows=cal)
+    dt = time.perf_counter() - t0
+    per_key = dt / max(1, vis[cal].sum())
+    target_keys = seconds_target / per_key
+    frac = min(1.0, target_keys / vis.sum())
+    n = max(64, int(frac * len(rows)))
+    sample = np.sort(rng.choice(rows, n, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_f64(prob.q, prob.k, prob.v, prob.cu_q, prob.cu_k, prob.scale, rows=sample)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * 128 * 32 * float(vis[sample].sum())
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{n} of {len(rows)} query rows (all 32 heads) of the prefill workload, uniformly drawn, seed 0"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    prob, _ = prefill_workload()
+    vis = np.empty(prob.q.shape[0], np.int64)
+    for s in range(len(prob.cu_q) - 1):
+        a, b = prob.cu_q[s], prob.cu_q[s + 1]
+        vis[a:b] = np.arange(1, b - a + 1)
+    rng = np.random.default_rng(1)
+    n = args.reference_rows
+    times, flops = [], []
+    for i in range(args.warmup + args.steps):
+        sample = np.sort(rng.choice(prob.q.shape[0], n, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention_f64(prob.q, prob.k, prob.v, prob.cu_q, prob.cu_k, prob.scale, rows=sample)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            flops.append(4.0 * 128 * 32 * float(vis[sample].sum()))
+    value = sum(flops) / sum(times) / 1e12
+    ms = 1e3 * float(np.mean(times))
+    sample_desc = f"{n} random query rows (all 32 heads) of the prefill workload per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample_desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample_desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-rows", type=int, default=48)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,591 @@
+// api.cu -- host side of the C ABI (include/rlk_attn.h): argument checks,
+// the global block plan and logical CP partition, TMA tensor maps, the static
+// longest-first work schedule, and kernel launches.  Nothing here allocates
+// device memory or synchronises, except rlk_attn_check_device_error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/rlk_attn.h"
+#include "rlk_internal.h"
+
+namespace rlk {
+cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int grid, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream);
+rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
+                        const float* out_f32, const void* dout, const float* lse,
+                        const int32_t* cu, int32_t cp_rank, float* dq, float* dk, float* dv,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu);
+}  // namespace rlk
+
+static_assert(sizeof(rlk::FwdParams) + 3 * sizeof(CUtensorMap) + 256 <= 32764,
+              "forward kernel parameters exceed the 32 KB launch limit");
+static_assert(sizeof(rlk::MergeParams) <= 4096, "merge parameters");
+static_assert(sizeof(rlk_attn_slab) == sizeof(rlk::Slab), "slab layout");
+
+// The device error word.  Host code reaches it through its device address,
+// looked up once per device.
+static __device__ rlk::ErrWord g_rlk_err;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+rlk_status fail(rlk_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+rlk_status ok() {
+  g_last_error.clear();
+  return RLK_OK;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  rlk::ErrWord* err = nullptr;
+};
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+rlk_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(RLK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(RLK_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_rlk_err);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    d.err = static_cast<rlk::ErrWord*>(addr);
+    d.ready = true;
+  }
+  *out = &d;
+  return RLK_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// BF16 tensor [d2][d1][128] as a 3-D map (innermost first), 128-byte swizzle,
+// box {64, box1, box2}.
+rlk_status make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint32_t box1, uint32_t box2) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {128, d1, d2};
+  cuuint64_t strides[2] = {256, 256 * d1};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return RLK_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rlk_status check_params(const rlk_attn_params* p) {
+  if (!p) return fail(RLK_ERR_INVALID_ARGUMENT, "params is NULL");
+  if (p->head_dim != rlk::kHeadDim) return fail(RLK_ERR_UNSUPPORTED, "head_dim %d: only 128 is supported", p->head_dim);
+  if (p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_q_heads % p->num_kv_heads)
+    return fail(RLK_ERR_INVALID_ARGUMENT, "heads %d / %d: Hkv must divide Hq", p->num_q_heads, p->num_kv_heads);
+  if (p->num_q_heads / p->num_kv_heads > 128)
+    return fail(RLK_ERR_UNSUPPORTED, "more than 128 query heads per KV head");
+  if (p->causal != 1) return fail(RLK_ERR_UNSUPPORTED, "only causal attention is supported");
+  if (p->kv_block_size != 64 && p->kv_block_size != 128)
+    return fail(RLK_ERR_UNSUPPORTED, "kv_block_size %d: must be 64 or 128", p->kv_block_size);
+  if (p->cp_size < 1 || p->cp_size > 8) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_size %d not in 1..8", p->cp_size);
+  if (p->cp_layout != 0 && p->cp_layout != 1) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_layout %d", p->cp_layout);
+  if (p->num_seqs < 1 || p->num_seqs > rlk::kMaxSeqs)
+    return fail(RLK_ERR_UNSUPPORTED, "num_seqs %d not in 1..%d", p->num_seqs, rlk::kMaxSeqs);
+  if (!(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "softmax_scale must be finite and > 0");
+  return RLK_OK;
+}
+
+rlk_status check_cu(const rlk_attn_params* p, const int32_t* cu_q, const int32_t* cu_k) {
+  if (!cu_q || !cu_k) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+  if (cu_q[0] != 0 || cu_k[0] != 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0");
+  for (int s = 0; s < p->num_seqs; ++s) {
+    const int64_t ql = static_cast<int64_t>(cu_q[s + 1]) - cu_q[s];
+    const int64_t kl = static_cast<int64_t>(cu_k[s + 1]) - cu_k[s];
+    if (ql < 0 || kl < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens not monotone at sequence %d", s);
+    if (ql > kl) return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: q_len %lld > kv_len %lld", s,
+                             static_cast<long long>(ql), static_cast<long long>(kl));
+  }
+  return RLK_OK;
+}
+
+float scale_log2(const rlk_attn_params* p) {
+  return static_cast<float>(static_cast<double>(p->softmax_scale) * 1.4426950408889634073599);
+}
+
+// Token chunks of a sequence of n tokens under the CP partition:
+// (rank, begin, end) with bounds floor(c * n / chunks).
+struct Chunk {
+  int rank, begin, end;
+};
+std::vector<Chunk> partition(int n, int cp, int layout) {
+  std::vector<Chunk> out;
+  if (layout == 0) {
+    for (int c = 0; c < cp; ++c)
+      out.push_back({c, static_cast<int>(static_cast<int64_t>(c) * n / cp),
+                     static_cast<int>(static_cast<int64_t>(c + 1) * n / cp)});
+  } else {
+    for (int c = 0; c < 2 * cp; ++c)
+      out.push_back({c < cp ? c : 2 * cp - 1 - c, static_cast<int>(static_cast<int64_t>(c) * n / (2 * cp)),
+                     static_cast<int>(static_cast<int64_t>(c + 1) * n / (2 * cp))});
+  }
+  return out;
+}
+int owner_rank(int pos, int n, int cp, int layout) {
+  for (const Chunk& c : partition(n, cp, layout))
+    if (pos >= c.begin && pos < c.end) return c.rank;
+  return -1;
+}
+
+struct SlabPlan {
+  std::vector<rlk_attn_slab> slabs;
+  int64_t n_pairs = 0;
+};
+
+void plan_slabs(const rlk_attn_params* p, const int32_t* cu_q, const int32_t* cu_k, int cp_rank, int64_t base,
+                SlabPlan* out) {
+  const int B = p->kv_block_size;
+  int64_t off = base;
+  for (int s = 0; s < p->num_seqs; ++s) {
+    const int ql = cu_q[s + 1] - cu_q[s];
+    const int kl = cu_k[s + 1] - cu_k[s];
+    if (ql == 0) continue;
+    const int nb = (kl + B - 1) / B;
+    const std::vector<Chunk> parts = partition(kl, p->cp_size, p->cp_layout);
+    for (int b = 0; b < nb; ++b) {
+      int prod = -1;
+      for (const Chunk& c : parts)
+        if (b * B >= c.begin && b * B < c.end) prod = c.rank;
+      if (cp_rank >= 0 && prod != cp_rank) continue;
+      rlk_attn_slab sl;
+      sl.seq = s;
+      sl.block = b;
+      sl.row_begin = std::max(0, b * B - (kl - ql));
+      sl.row_count = ql - sl.row_begin;
+      sl.offset = off;
+      sl.producer = prod;
+      sl.reserved = 0;
+      off += static_cast<int64_t>(sl.row_count) * p->num_q_heads;
+      out->slabs.push_back(sl);
+    }
+  }
+  out->n_pairs = off - base;
+}
+
+rlk_status launch_fwd_tiles(rlk::FwdParams* fp, const std::vector<rlk::FwdTile>& tiles, int items_per_tile,
+                            const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DeviceInfo* dev, cudaStream_t stream) {
+  for (size_t t0 = 0; t0 < tiles.size(); t0 += rlk::kMaxTilesPerLaunch) {
+    const size_t n = std::min(tiles.size() - t0, static_cast<size_t>(rlk::kMaxTilesPerLaunch));
+    std::copy(tiles.begin() + t0, tiles.begin() + t0 + n, fp->tiles);
+    fp->num_tiles = static_cast<int32_t>(n);
+    fp->num_items = static_cast<int32_t>(n) * items_per_tile;
+    const int grid = std::min(fp->num_items, dev->num_sms);
+    cudaError_t e = rlk::launch_fwd(*fp, tq, tk, tv, grid, stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  }
+  return RLK_OK;
+}
+
+void fill_seqs(rlk::FwdParams* fp, const rlk_attn_params* p, const int32_t* cu_q, const int32_t* cu_k) {
+  for (int s = 0; s <= p->num_seqs; ++s) {
+    fp->cu_q[s] = cu_q[s];
+    fp->cu_k[s] = cu_k[s];
+  }
+}
+
+void base_fwd(rlk::FwdParams* fp, const rlk_attn_params* p, const DeviceInfo* dev, int mode) {
+  std::memset(fp, 0, sizeof(*fp));
+  fp->err = dev->err;
+  fp->mode = mode;
+  fp->hq = p->num_q_heads;
+  fp->hkv = p->num_kv_heads;
+  fp->group = p->num_q_heads / p->num_kv_heads;
+  fp->block = p->kv_block_size;
+  fp->scale_log2 = scale_log2(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rlk_attn_last_error(void) { return g_last_error.c_str(); }
+
+const char* rlk_attn_core_id(void) {
+  return "rlk_attn.deterministic_core.v1/sm_103a;merge_order=global_block_index;"
+         "downcast_at=final_write;split_kv=fixed_global_blocks;accumulate=fp32;pv=bf16x2_split";
+}
+
+rlk_status rlk_attn_plan_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                const int32_t* cu_seqlens_k, int32_t cp_rank, int64_t pair_base,
+                                rlk_attn_slab* slabs, int64_t max_slabs, int64_t* n_slabs, int64_t* n_pairs) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
+  if (pair_base < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "pair_base < 0");
+  if (!n_slabs || !n_pairs) return fail(RLK_ERR_INVALID_ARGUMENT, "n_slabs / n_pairs is NULL");
+  SlabPlan plan;
+  plan_slabs(params, cu_seqlens_q, cu_seqlens_k, cp_rank, pair_base, &plan);
+  *n_slabs = static_cast<int64_t>(plan.slabs.size());
+  *n_pairs = plan.n_pairs;
+  if (slabs) {
+    if (max_slabs < *n_slabs) return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "max_slabs %lld < %lld",
+                                          static_cast<long long>(max_slabs), static_cast<long long>(*n_slabs));
+    std::copy(plan.slabs.begin(), plan.slabs.end(), slabs);
+  }
+  return ok();
+}
+
+rlk_status rlk_attn_block_manifest_hash(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                        const int32_t* cu_seqlens_k, uint64_t* hash) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (!hash) return fail(RLK_ERR_INVALID_ARGUMENT, "hash is NULL");
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&h](int64_t v) {
+    for (int i = 0; i < 8; ++i) {
+      h ^= static_cast<uint64_t>((v >> (8 * i)) & 0xFF);
+      h *= 1099511628211ull;
+    }
+  };
+  const int B = params->kv_block_size;
+  for (int s = 0; s < params->num_seqs; ++s) {
+    const int kl = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+    for (int b = 0; b * B < kl; ++b) {
+      mix(s);
+      mix(b);
+      mix(static_cast<int64_t>(b) * B);
+      mix(std::min(kl, (b + 1) * B) - 1);
+      mix(owner_rank(b * B, kl, params->cp_size, params->cp_layout));
+    }
+  }
+  *hash = h;
+  return ok();
+}
+
+rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
+                                   int64_t pair_base, float* state_o, float* state_lse, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
+  if (pair_base < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "pair_base < 0");
+  if (!q || !k || !v || !state_o || !state_lse) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_o))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  SlabPlan plan;
+  plan_slabs(params, cu_seqlens_q, cu_seqlens_k, cp_rank, pair_base, &plan);
+  if (plan.slabs.empty()) return ok();
+  const int tq = cu_seqlens_q[params->num_seqs], tk = cu_seqlens_k[params->num_seqs];
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(&mq, q, params->num_q_heads, tq, 1, rlk::kTileRows))) return st;
+  if ((st = make_map(&mk, k, params->num_kv_heads, tk, 1, params->kv_block_size))) return st;
+  if ((st = make_map(&mv, v, params->num_kv_heads, tk, 1, params->kv_block_size))) return st;
+  std::vector<rlk::FwdTile> tiles;
+  for (const rlk_attn_slab& sl : plan.slabs) {
+    for (int r = 0; r < sl.row_count; r += rlk::kTileRows) {
+      rlk::FwdTile t;
+      t.seq = sl.seq;
+      t.row_begin = sl.row_begin + r;
+      t.row_count = std::min(rlk::kTileRows, sl.row_count - r);
+      t.block = sl.block;
+      t.slab_offset = sl.offset;
+      t.slab_row_begin = sl.row_begin;
+      t.slab_row_count = sl.row_count;
+      tiles.push_back(t);
+    }
+  }
+  auto fp = std::make_unique<rlk::FwdParams>();
+  base_fwd(fp.get(), params, dev, rlk::kModeStates);
+  fill_seqs(fp.get(), params, cu_seqlens_q, cu_seqlens_k);
+  fp->state_o = state_o;
+  fp->state_lse = state_lse;
+  if ((st = launch_fwd_tiles(fp.get(), tiles, params->num_q_heads, mq, mk, mv, dev, stream))) return st;
+  return ok();
+}
+
+rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
+                            float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
+  if (!q || !k || !v) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
+  if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out_f32 && !aligned16(out_f32)) ||
+      (out_bf16 && !aligned16(out_bf16)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  const int B = params->kv_block_size;
+  std::vector<std::pair<int, rlk::FwdTile>> costed;
+  for (int s = 0; s < params->num_seqs; ++s) {
+    const int ql = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+    const int kl = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+    if (ql == 0) continue;
+    std::vector<Chunk> parts;
+    if (cp_rank < 0) parts.push_back({-1, 0, ql});
+    else
+      for (const Chunk& c : partition(ql, params->cp_size, params->cp_layout))
+        if (c.rank == cp_rank && c.end > c.begin) parts.push_back(c);
+    for (const Chunk& c : parts) {
+      for (int r = c.begin; r < c.end; r += rlk::kTileRows) {
+        rlk::FwdTile t;
+        std::memset(&t, 0, sizeof(t));
+        t.seq = s;
+        t.row_begin = r;
+        t.row_count = std::min(rlk::kTileRows, c.end - r);
+        t.block = -1;
+        const int pmax = kl - ql + r + t.row_count - 1;
+        costed.push_back({pmax / B + 1, t});
+      }
+    }
+  }
+  if (costed.empty()) return ok();
+  // longest first; ties by (sequence, row) so the schedule is a pure function of the inputs
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
+                     return a.first > b.first;
+                   });
+  std::vector<rlk::FwdTile> tiles;
+  for (auto& c : costed) tiles.push_back(c.second);
+  const int tq = cu_seqlens_q[params->num_seqs], tk = cu_seqlens_k[params->num_seqs];
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(&mq, q, params->num_q_heads, tq, 1, rlk::kTileRows))) return st;
+  if ((st = make_map(&mk, k, params->num_kv_heads, tk, 1, B))) return st;
+  if ((st = make_map(&mv, v, params->num_kv_heads, tk, 1, B))) return st;
+  auto fp = std::make_unique<rlk::FwdParams>();
+  base_fwd(fp.get(), params, dev, rlk::kModeFused);
+  fill_seqs(fp.get(), params, cu_seqlens_q, cu_seqlens_k);
+  fp->out_f32 = out_f32;
+  fp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  fp->lse = lse;
+  if ((st = launch_fwd_tiles(fp.get(), tiles, params->num_q_heads, mq, mk, mv, dev, stream))) return st;
+  return ok();
+}
+
+rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                 const void* v_pool, int32_t n_pages, int32_t page_size,
+                                 const int32_t* page_table, int32_t max_pages, const int32_t* seqlens,
+                                 float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out_f32 && !aligned16(out_f32)) ||
+      (out_bf16 && !aligned16(out_bf16)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const int B = params->kv_block_size;
+  if (page_size < 8 || page_size > B || B % page_size)
+    return fail(RLK_ERR_UNSUPPORTED, "page_size %d must be >= 8 and divide kv_block_size %d", page_size, B);
+  if (n_pages < 1 || max_pages < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "n_pages / max_pages < 1");
+  if (static_cast<int64_t>(n_pages + 1) * page_size >= (int64_t(1) << 31))
+    return fail(RLK_ERR_UNSUPPORTED, "page pool too large for 32-bit token coordinates");
+  for (int s = 0; s < params->num_seqs; ++s)
+    if (seqlens[s] < 1 || static_cast<int64_t>(seqlens[s]) > static_cast<int64_t>(max_pages) * page_size)
+      return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: context length %d not in 1..max_pages*page_size", s,
+                  seqlens[s]);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  const int group = params->num_q_heads / params->num_kv_heads;
+  std::vector<std::pair<int, rlk::FwdTile>> costed;
+  for (int s = 0; s < params->num_seqs; ++s)
+    for (int g = 0; g < params->num_kv_heads; ++g) {
+      rlk::FwdTile t;
+      std::memset(&t, 0, sizeof(t));
+      t.seq = s;
+      t.row_begin = g;
+      t.row_count = group;
+      t.block = -1;
+      costed.push_back({(seqlens[s] + B - 1) / B, t});
+    }
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
+                     return a.first > b.first;
+                   });
+  std::vector<rlk::FwdTile> tiles;
+  for (auto& c : costed) tiles.push_back(c.second);
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(&mq, q, params->num_q_heads, params->num_seqs, group, 1))) return st;
+  if ((st = make_map(&mk, k_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))
+    return st;
+  if ((st = make_map(&mv, v_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))
+    return st;
+  auto fp = std::make_unique<rlk::FwdParams>();
+  base_fwd(fp.get(), params, dev, rlk::kModeDecode);
+  for (int s = 0; s < params->num_seqs; ++s) fp->cu_k[s] = seqlens[s];
+  fp->out_f32 = out_f32;
+  fp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  fp->lse = lse;
+  fp->page_table = page_table;
+  fp->max_pages = max_pages;
+  fp->page_size = page_size;
+  fp->n_pages = n_pages;
+  if ((st = launch_fwd_tiles(fp.get(), tiles, 1, mq, mk, mv, dev, stream))) return st;
+  return ok();
+}
+
+size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k) {
+  if (check_params(params) != RLK_OK) return 0;
+  if (op == RLK_OP_MERGE) {
+    if (check_cu(params, cu_seqlens_q, cu_seqlens_k) != RLK_OK) return 0;
+    int max_blocks = 1;
+    for (int s = 0; s < params->num_seqs; ++s)
+      max_blocks = std::max(max_blocks, (cu_seqlens_k[s + 1] - cu_seqlens_k[s] + params->kv_block_size - 1) /
+                                            params->kv_block_size);
+    const size_t bytes = static_cast<size_t>(params->num_seqs) * max_blocks * sizeof(int32_t);
+    return (bytes + 255) / 256 * 256;
+  }
+  if (op == RLK_OP_BACKWARD) {
+    if (check_cu(params, cu_seqlens_q, cu_seqlens_q) != RLK_OK) return 0;
+    return rlk::backward_workspace_bytes(params, cu_seqlens_q);
+  }
+  return 0;
+}
+
+rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs, int64_t n_slabs,
+                                 const float* state_o, const float* state_lse, float* out_f32, void* out_bf16,
+                                 float* lse, void* workspace, size_t workspace_bytes, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (n_slabs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "bad state table");
+  if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if ((out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) || (state_o && !aligned16(state_o)) ||
+      (slabs && !aligned16(slabs)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const size_t need = rlk_attn_workspace_size(params, RLK_OP_MERGE, cu_seqlens_q, cu_seqlens_k);
+  if (!workspace || workspace_bytes < need)
+    return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  const int64_t total_rows = cu_seqlens_q[params->num_seqs];
+  if (total_rows == 0) return ok();
+  auto mp = std::make_unique<rlk::MergeParams>();
+  std::memset(mp.get(), 0, sizeof(*mp));
+  mp->err = dev->err;
+  mp->num_seqs = params->num_seqs;
+  mp->hq = params->num_q_heads;
+  mp->block = params->kv_block_size;
+  int max_blocks = 1;
+  for (int s = 0; s < params->num_seqs; ++s)
+    max_blocks = std::max(max_blocks, (cu_seqlens_k[s + 1] - cu_seqlens_k[s] + params->kv_block_size - 1) /
+                                          params->kv_block_size);
+  mp->max_blocks = max_blocks;
+  mp->total_rows = total_rows;
+  mp->n_slabs = n_slabs;
+  mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
+  mp->state_o = state_o;
+  mp->state_lse = state_lse;
+  mp->index = static_cast<int32_t*>(workspace);
+  mp->out_f32 = out_f32;
+  mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  mp->lse = lse;
+  for (int s = 0; s <= params->num_seqs; ++s) {
+    mp->cu_q[s] = cu_seqlens_q[s];
+    mp->cu_k[s] = cu_seqlens_k[s];
+  }
+  cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                             const float* out_f32, const void* dout, const float* lse, const int32_t* cu_seqlens,
+                             int32_t cp_rank, float* dq, float* dk, float* dv, void* workspace,
+                             size_t workspace_bytes, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens, cu_seqlens))) return st;
+  if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
+  if (!q || !k || !v || !out_f32 || !dout || !lse || !dq || !dk || !dv)
+    return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_f32) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const size_t need = rlk::backward_workspace_bytes(params, cu_seqlens);
+  if (!workspace || workspace_bytes < need)
+    return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  st = rlk::run_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,
+                         workspace_bytes, stream);
+  if (st) return st;
+  return ok();
+}
+
+rlk_status rlk_attn_check_device_error(rlk_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  rlk_status st = device_info(&dev);
+  if (st) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  rlk::ErrWord w{0, 0};
+  e = cudaMemcpy(&w, dev->err, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+  if (w.bits == 0) return ok();
+  const rlk::ErrWord zero{0, 0};
+  cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (w.bits & rlk::kErrDeviceTimeout) return fail(RLK_ERR_DEVICE_TIMEOUT, "device wait timed out (site 0x%x)", w.site);
+  if (w.bits & rlk::kErrDuplicateBlock) return fail(RLK_ERR_DUPLICATE_BLOCK, "duplicate global block in state table");
+  if (w.bits & rlk::kErrMissingBlock) return fail(RLK_ERR_MISSING_BLOCK, "missing global block in state table");
+  if (w.bits & rlk::kErrBadSlab) return fail(RLK_ERR_BAD_STATE_TABLE, "state table slab out of range");
+  if (w.bits & rlk::kErrBadPage) return fail(RLK_ERR_BAD_PAGE, "page id outside the pool");
+  return fail(RLK_ERR_CUDA, "device error bits 0x%x", w.bits);
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// numerics.cuh -- the one definition of every floating-point step that must
+// give the same bits in every kernel: the block state of one query row
+// against one global KV block, and the canonical fold of states.
+//
+// The state of a row against global block b is
+//   state_b = (o_b, lse_b, b)
+// ("WS2 Attention PR5 Drift Benchmark", Transformer Engine Reuse).  The fused
+// prefill, the state producer, the merge and the paged decode all call the
+// functions below, so a state produced by one kernel and merged by another
+// has exactly the bits the fused kernel folds on chip.  All of it is FP32
+// with one explicit rounding per operation (the library is compiled with
+// -fmad=false as well); the only downcast is the final BF16 write
+// ("[WS2][Attention] H100 validation and reproduction guide", Status: FP32
+// accumulation, fixed global_block_index merge, downcast at final write).
+#pragma once
+#include <cstdint>
+
+namespace rlk {
+
+constexpr float kLn2f = 0.693147182464599609375f;  // nearest float to ln 2
+
+// 2^x by the hardware's ex2 instruction (flush-to-zero; ex2(-inf) = +0).
+__device__ __forceinline__ float ex2_hw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Pack two floats into a bf16x2 word (round to nearest even): lo in bits
+// 0..15, hi in bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo_as_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_as_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Block softmax of one row, in the canonical order every kernel follows.
+//   x_c = S_c * scale_log2 for visible keys, -inf for the others
+//   m   = max_c x_c                              (log2 domain)
+//   p_c = 2^(x_c - m)
+//   l   = canonical row sum of p (below)
+//   lse_b = m ln2 + ln l  (natural log),  rcp = 1/l (IEEE-rounded)
+// A row with no visible key has no state: p = 0, lse_b = -inf.
+//
+// Canonical row sum: key c goes to partial c mod 32, the keys of a partial
+// added in ascending order; the 32 partials are then combined by the fixed
+// tree a[t] <- a[t] + a[t + off] for off = 16, 8, 4, 2, 1 -- the association a
+// 32-lane xor butterfly produces, so a warp-per-row kernel reproduces it.
+__device__ __forceinline__ float scaled_score(float s, int c, int n_visible, float scale_log2) {
+  return (c < n_visible) ? __fmul_rn(s, scale_log2) : -INFINITY;
+}
+__device__ __forceinline__ float prob(float x, float m) { return ex2_hw(__fsub_rn(x, m)); }
+// add probability p of key c (keys visited in ascending order) to partials a
+__device__ __forceinline__ void partial_add(float (&a)[32], int c, float p) {
+  if (c < 32) a[c & 31] = p;
+  else a[c & 31] = __fadd_rn(a[c & 31], p);
+}
+__device__ __forceinline__ float partial_tree(float (&a)[32]) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+    for (int t = 0; t < off; ++t) a[t] = __fadd_rn(a[t], a[t + off]);
+  }
+  return a[0];
+}
+__device__ __forceinline__ void block_stats(float m, float l, float& lse_b, float& rcp) {
+  lse_b = __fmaf_rn(m, kLn2f, logf(l));
+  rcp = __frcp_rn(l);
+}
+
+// Split p into BF16 hi + lo (p_hi = bf16(p), p_lo = bf16(p - p_hi)) packed
+// two keys per word, key 2k in the low half.
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(p0, p1);
+  const float r0 = __fsub_rn(p0, bf16_lo_as_f32(hi));
+  const float r1 = __fsub_rn(p1, bf16_hi_as_f32(hi));
+  lo = pack_bf16x2(r0, r1);
+}
+
+// Block output element: o = PV * (1/l).
+__device__ __forceinline__ float state_elem(float pv, float rcp) { return __fmul_rn(pv, rcp); }
+
+// Canonical fold of running (O, L) with state (o_b, lse_b):
+//   M = max(L, lse_b), mn = min(L, lse_b)
+//   L' = M + log1p(exp(mn - M))
+//   alpha = exp(L - L'), beta = exp(lse_b - L')
+//   O  = fma(o_b, beta, O * alpha)
+__device__ __forceinline__ void fold_coeffs(float L, float lb, float& Lp, float& alpha,
+                                            float& beta) {
+  const float M = fmaxf(L, lb);
+  const float mn = fminf(L, lb);
+  Lp = __fadd_rn(M, log1pf(expf(__fsub_rn(mn, M))));
+  alpha = expf(__fsub_rn(L, Lp));
+  beta = expf(__fsub_rn(lb, Lp));
+}
+__device__ __forceinline__ float fold_elem(float O, float o, float alpha, float beta) {
+  return __fmaf_rn(o, beta, __fmul_rn(O, alpha));
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(0.0f), "f"(x));
+  return static_cast<uint16_t>(w & 0xFFFFu);
+}
+
+}  // namespace rlk

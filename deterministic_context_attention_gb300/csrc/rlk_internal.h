@@ -1,0 +1,89 @@
+// rlk_internal.h -- launch parameter blocks and limits shared by the host
+// side of the C ABI and the kernels.  Not part of the public interface.
+#pragma once
+#include <cstdint>
+
+namespace rlk {
+
+constexpr int kHeadDim = 128;           // D, the only head size the kernels take
+constexpr int kMaxSeqs = 128;           // sequences per call (they ride in kernel params)
+constexpr int kMaxTilesPerLaunch = 880; // work tiles per launch (kernel param space)
+constexpr int kTileRows = 128;          // MMA M: query rows per tile
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded mbarrier waits: 1 s
+
+// device error word bits
+constexpr unsigned kErrDeviceTimeout = 1u;
+constexpr unsigned kErrBadPage = 2u;
+constexpr unsigned kErrDuplicateBlock = 4u;
+constexpr unsigned kErrMissingBlock = 8u;
+constexpr unsigned kErrBadSlab = 16u;
+
+struct ErrWord {
+  unsigned int bits;
+  unsigned int site;
+};
+
+enum FwdMode : int { kModeFused = 0, kModeStates = 1, kModeDecode = 2 };
+
+// One unit of forward work: up to 128 query rows of one sequence (all query
+// heads are looped inside the grid), or, for decode, one (sequence, KV head)
+// whose query heads form the rows.
+struct alignas(16) FwdTile {
+  int32_t seq;
+  int32_t row_begin;       // first query row, relative to the sequence's first query row
+  int32_t row_count;       // rows of the tile that are written (<= 128)
+  int32_t block;           // states mode: the global block; otherwise -1
+  int64_t slab_offset;     // states mode: first (row, head) pair of the slab
+  int32_t slab_row_begin;  // states mode: first row the slab covers
+  int32_t slab_row_count;  // states mode: rows the slab covers
+};
+
+struct FwdParams {
+  ErrWord* err;
+  int32_t mode;
+  int32_t hq, hkv, group;  // query heads, KV heads, hq / hkv
+  int32_t block;           // KV block size (64 or 128)
+  float scale_log2;        // softmax_scale * log2(e), rounded once on the host
+  int32_t num_tiles;
+  int32_t num_items;
+  // fused / decode outputs
+  float* out_f32;
+  uint16_t* out_bf16;
+  float* lse;
+  // states outputs
+  float* state_o;
+  float* state_lse;
+  // decode
+  const int32_t* page_table;
+  int32_t max_pages, page_size, n_pages, pad0;
+  // sequences: fused/states use cu_q / cu_k (packed offsets); decode uses
+  // cu_k[s] as the context length of sequence s.
+  int32_t cu_q[kMaxSeqs + 1];
+  int32_t cu_k[kMaxSeqs + 1];
+  FwdTile tiles[kMaxTilesPerLaunch];
+};
+
+// Merge (canonical fold of a partial-state table).
+struct Slab {  // mirrors rlk_attn_slab
+  int32_t seq, block, row_begin, row_count;
+  int64_t offset;
+  int32_t producer, reserved;
+};
+
+struct MergeParams {
+  ErrWord* err;
+  int32_t num_seqs, hq, block, max_blocks;
+  int64_t total_rows;      // query rows over all sequences
+  int64_t n_slabs;
+  const Slab* slabs;       // device, arrival order
+  const float* state_o;
+  const float* state_lse;
+  int32_t* index;          // [num_seqs * max_blocks] slab id per (seq, block)
+  float* out_f32;
+  uint16_t* out_bf16;
+  float* lse;
+  int32_t cu_q[kMaxSeqs + 1];
+  int32_t cu_k[kMaxSeqs + 1];
+};
+
+}  // namespace rlk

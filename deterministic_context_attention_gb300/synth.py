@@ -128,27 +128,46 @@ def permute_batch(p: Prefill, order) -> Prefill:
 
 @dataclass
 class PagedDecode:
-    q: np.ndarray            # [n, hq, d]
-    k_pool: np.ndarray       # [n_pages, page_size, hkv, d]
-    v_pool: np.ndarray
-    page_table: np.ndarray   # [n, max_pages] int32
+    q: np.ndarray            # [n, hq, d] float32 (BF16-exact)
+    k_bits: np.ndarray       # [n_pages, page_size, hkv, d] uint16 BF16 words
+    v_bits: np.ndarray
+    page_table: np.ndarray   # [n, max_pages] int32 (-1 past a sequence's last page)
     seqlens: np.ndarray      # [n] int32
     page_size: int
     hq: int
     hkv: int
     d: int
     scale: float
-    k_seq: list = field(default_factory=list)   # contiguous per-sequence K [ctx, hkv, d]
-    v_seq: list = field(default_factory=list)
+    seed: int
+
+    def seq_kv(self, s):
+        """Contiguous K, V of sequence s ([ctx, hkv, d] float32), regenerated
+        from the seed (the pool holds the same values)."""
+        return decode_seq_kv(self.seed, s, int(self.seqlens[s]), self.hkv, self.d)
+
+    @property
+    def k_pool(self):
+        return bits_to_f32(self.k_bits)
+
+    @property
+    def v_pool(self):
+        return bits_to_f32(self.v_bits)
+
+
+def decode_seq_kv(seed, s, ctx, hkv, d):
+    k = normal_bf16(seed * 1000 + s + 1, T_K, (ctx, hkv, d))
+    v = normal_bf16(seed * 1000 + s + 1, T_V, (ctx, hkv, d))
+    return k, v
 
 
 def paged_decode_problem(n=64, ctx_lo=512, ctx_hi=32768, hq=32, hkv=8, d=128, page_size=16,
                          seed=3, ctx=None, spare_pages=0, garbage_tail=True) -> PagedDecode:
     """Context lengths ~ U[ctx_lo, ctx_hi] (integers, from the seed) unless
     ``ctx`` is given; every sequence's KV lives in pages of ``page_size``
-    tokens scattered over a pool by a seeded random permutation (numpy's
-    Generator.permutation).  Unused tail slots of a sequence's last page hold
-    NaN when ``garbage_tail`` so that a kernel reading them would show it."""
+    tokens scattered over the pool by a seeded random permutation.  Unused
+    tail slots of a sequence's last page (and spare pages) hold NaN when
+    ``garbage_tail``, so a kernel that let them into its arithmetic would show
+    it."""
     if ctx is None:
         ctx = rng(seed, T_LENS).integers(ctx_lo, ctx_hi + 1, size=n)
     ctx = np.asarray(ctx, np.int64)
@@ -158,29 +177,25 @@ def paged_decode_problem(n=64, ctx_lo=512, ctx_hi=32768, hq=32, hkv=8, d=128, pa
     max_pages = int(pages_per.max())
     perm = rng(seed, T_PAGES).permutation(n_pages).astype(np.int32)
     q = normal_bf16(seed, T_Q, (n, hq, d))
-    k_pool = np.zeros((n_pages, page_size, hkv, d), np.float32)
-    v_pool = np.zeros((n_pages, page_size, hkv, d), np.float32)
+    fill = 0x7FC0 if garbage_tail else 0
+    k_bits = np.full((n_pages, page_size, hkv, d), fill, np.uint16)
+    v_bits = np.full((n_pages, page_size, hkv, d), fill, np.uint16)
     page_table = np.full((n, max_pages), -1, np.int32)
-    k_seq, v_seq = [], []
     nxt = 0
     for s in range(n):
-        ks = normal_bf16(seed * 1000 + s, T_K, (int(ctx[s]), hkv, d))
-        vs = normal_bf16(seed * 1000 + s, T_V, (int(ctx[s]), hkv, d))
-        k_seq.append(ks)
-        v_seq.append(vs)
-        for pg in range(int(pages_per[s])):
-            phys = int(perm[nxt])
-            nxt += 1
-            page_table[s, pg] = phys
-            t0 = pg * page_size
-            t1 = min(t0 + page_size, int(ctx[s]))
-            k_pool[phys, :t1 - t0] = ks[t0:t1]
-            v_pool[phys, :t1 - t0] = vs[t0:t1]
-            if garbage_tail and t1 - t0 < page_size:
-                k_pool[phys, t1 - t0:] = np.nan
-                v_pool[phys, t1 - t0:] = np.nan
-    return PagedDecode(q, k_pool, v_pool, page_table, ctx.astype(np.int32), page_size, hq, hkv,
-                       d, 1.0 / np.sqrt(d), k_seq, v_seq)
+        c, npg = int(ctx[s]), int(pages_per[s])
+        ks, vs = decode_seq_kv(seed, s, c, hkv, d)
+        pad_k = np.full((npg * page_size, hkv, d), fill, np.uint16)
+        pad_v = np.full((npg * page_size, hkv, d), fill, np.uint16)
+        pad_k[:c] = bf16_bits(ks)
+        pad_v[:c] = bf16_bits(vs)
+        phys = perm[nxt:nxt + npg]
+        nxt += npg
+        page_table[s, :npg] = phys
+        k_bits[phys] = pad_k.reshape(npg, page_size, hkv, d)
+        v_bits[phys] = pad_v.reshape(npg, page_size, hkv, d)
+    return PagedDecode(q, k_bits, v_bits, page_table, ctx.astype(np.int32), page_size, hq, hkv,
+                       d, 1.0 / np.sqrt(d), seed)
 
 
 # The five synthetic workloads (sizes, shapes and value distributions of the

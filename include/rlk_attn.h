@@ -1,0 +1,244 @@
+/*
+ * rlk_attn.h -- C ABI of librlk_attn.so: batch-invariant, split-order-
+ * invariant causal GQA attention for sm_103a (GB300).
+ *
+ * What the library computes.  For every query row and every global KV block
+ * b of its sequence, a partial state
+ *     state_b = (o_b, lse_b, global_block_index = b)
+ * with FP32 accumulation; the states of a row are merged in ascending
+ * global_block_index order, whatever logical context-parallel (CP) rank or
+ * arrival order produced them, and the result is downcast to BF16 only at the
+ * final write.  Source pages:
+ *   [P1] "WS2 Attention PR5 Drift Benchmark" (design doc): Scope (Qwen3-8B
+ *        heads Hq=32, Hkv=8, D=128; CP sweep; full and chunked prefill; BF16
+ *        path vs FP32), Transformer Engine Reuse (state tuple; sort by
+ *        global_block_index, then online-softmax correction), Report Contract
+ *        (merge order global_block_index, downcast_at final_write, block
+ *        metadata hash).
+ *   [P3] "[WS2][Attention] H100 validation and reproduction guide for #235
+ *        PR1-PR8": Status (FP32 accumulation, Split-KV disabled, fixed merge
+ *        order, full-KV arithmetic retained), PR stack (decode KV-cache replay,
+ *        paged-KV adapter, dQ/dK/dV backward), Acceptance (Out/LSE/dQ/dK/dV
+ *        max abs 0.0 across 2/4/8 ranks; fallback=false).
+ *
+ * Conventions (every entry point):
+ *   - Tensors are packed varlen ("THD"), row-major, contiguous:
+ *       q [Tq, Hq, 128] BF16, k/v [Tk, Hkv, 128] BF16,
+ *       out [Tq, Hq, 128] FP32 and/or BF16, lse [Tq, Hq] FP32.
+ *     Query head h reads KV head h / (Hq / Hkv).  softmax scale is given.
+ *   - Device pointers are CUDA device memory of the current device, 16-byte
+ *     aligned.  Arrays documented as HOST are read on the host during the
+ *     call and not retained.
+ *   - The caller owns every buffer (outputs, state table, workspace).  The
+ *     library never allocates, frees or synchronises in these calls; work is
+ *     enqueued on `stream` (NULL = legacy default stream).
+ *   - Arguments are validated before anything is launched.  On failure the
+ *     call returns a status, launches nothing and sets rlk_attn_last_error().
+ *     There is no fallback: an unsupported shape returns RLK_ERR_UNSUPPORTED.
+ *   - Faults detected on the device (a wait that timed out, a bad page id, a
+ *     duplicate or missing block in a state table) set the device error word;
+ *     read it with rlk_attn_check_device_error().
+ *   - Causal masking is bottom-right aligned: query row i of a sequence with
+ *     q_len queries and kv_len keys sits at key position kv_len - q_len + i
+ *     (q_len <= kv_len), so chunked-prefill replay passes the chunk's queries
+ *     and the KV cache up to the chunk's end.
+ */
+#ifndef RLK_ATTN_H
+#define RLK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* rlk_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  RLK_OK = 0,
+  RLK_ERR_INVALID_ARGUMENT = 1,
+  RLK_ERR_UNSUPPORTED = 2,
+  RLK_ERR_WORKSPACE_TOO_SMALL = 3,
+  RLK_ERR_DUPLICATE_BLOCK = 4,
+  RLK_ERR_MISSING_BLOCK = 5,
+  RLK_ERR_DEVICE_TIMEOUT = 6,
+  RLK_ERR_CUDA = 7,
+  RLK_ERR_BAD_PAGE = 8,
+  RLK_ERR_BAD_STATE_TABLE = 9
+} rlk_status;
+
+/* Problem description shared by the entry points. */
+typedef struct {
+  int32_t num_seqs;      /* sequences in the batch, 1..128 */
+  int32_t num_q_heads;   /* Hq */
+  int32_t num_kv_heads;  /* Hkv, divides Hq */
+  int32_t head_dim;      /* must be 128 */
+  float softmax_scale;   /* e.g. 1/sqrt(128) */
+  int32_t causal;        /* must be 1 */
+  int32_t kv_block_size; /* global KV block size B: 64 or 128 */
+  int32_t cp_size;       /* logical context-parallel ranks, 1..8 */
+  int32_t cp_layout;     /* 0 = contiguous chunks, 1 = zigzag (2*cp chunks, rank r owns r and 2cp-1-r) */
+} rlk_attn_params;
+
+/*
+ * One slab of the partial-state table: the states of global block `block`
+ * of sequence `seq` for the query rows [row_begin, row_begin + row_count)
+ * (relative to the sequence's first query row) -- exactly the rows whose
+ * causal window reaches the block.  Storage, for query head h and row i:
+ *     pair  = offset + h * row_count + (i - row_begin)
+ *     o_b   = state_o[pair * 128 .. pair * 128 + 127]   (FP32)
+ *     lse_b = state_lse[pair]                            (FP32, natural log)
+ * `producer` is the logical CP rank that produced the slab (provenance).
+ * [P1] Transformer Engine Reuse: state_i = (out_i, lse_i, global_block_index_i).
+ */
+typedef struct {
+  int32_t seq;
+  int32_t block;
+  int32_t row_begin;
+  int32_t row_count;
+  int64_t offset;
+  int32_t producer;
+  int32_t reserved;
+} rlk_attn_slab;
+
+/*
+ * Block plan (host only, no device work).  Lists the slabs that logical rank
+ * `cp_rank` produces (cp_rank = -1: every rank's), in ascending (seq, block)
+ * order, with storage offsets starting at `pair_base`.  Global block b of a
+ * sequence holds keys [b*B, (b+1)*B) counted from the sequence's first key;
+ * its producer is the rank that owns key b*B under the cp_layout partition of
+ * the sequence's kv_len keys ([P3] Status: full-KV deterministic arithmetic
+ * retained, so a state always covers a whole global block).
+ *   cu_seqlens_q, cu_seqlens_k: HOST [num_seqs + 1], prefix sums, q_len <= kv_len.
+ *   slabs: HOST output of max_slabs entries, or NULL to only count.
+ *   *n_slabs, *n_pairs: slabs listed and (row, head) pairs they hold.
+ * Returns RLK_ERR_INVALID_ARGUMENT for bad lengths / ranks, and
+ * RLK_ERR_WORKSPACE_TOO_SMALL when max_slabs is too small (counts still set).
+ */
+rlk_status rlk_attn_plan_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                const int32_t* cu_seqlens_k, int32_t cp_rank, int64_t pair_base,
+                                rlk_attn_slab* slabs, int64_t max_slabs, int64_t* n_slabs,
+                                int64_t* n_pairs);
+
+/*
+ * Block-manifest hash (host only): FNV-1a 64 over (seq, block, first key,
+ * last key, producer) of every global block, in ascending (seq, block)
+ * order.  Two runs agree on it iff they use the same block decomposition and
+ * producer assignment ([P1] Report Contract: block metadata hash).
+ */
+rlk_status rlk_attn_block_manifest_hash(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                        const int32_t* cu_seqlens_k, uint64_t* hash);
+
+/*
+ * Partial states of logical rank `cp_rank` (-1: all ranks): writes, for every
+ * slab rlk_attn_plan_states(params, cu_seqlens_q, cu_seqlens_k, cp_rank,
+ * pair_base, ...) lists, o_b and lse_b into state_o / state_lse at the
+ * slab's offsets.  q, k, v: device BF16 as in the conventions;
+ * cu_seqlens_q/_k: HOST.  state_o: device FP32 [>= (pair_base + n_pairs) * 128],
+ * state_lse: device FP32 [>= pair_base + n_pairs].
+ */
+rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q, const void* k,
+                                   const void* v, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t cp_rank, int64_t pair_base,
+                                   float* state_o, float* state_lse, rlk_stream_t stream);
+
+/*
+ * Canonical merge of a state table whose slabs arrive in ANY order: sorts by
+ * global_block_index per (sequence, block), then folds each (row, head) left
+ * to right with the canonical FP32 fold, writing out_f32 (device FP32
+ * [Tq,Hq,128], nullable), out_bf16 (device BF16, nullable; not both NULL)
+ * and lse (device FP32 [Tq,Hq]).  slabs: DEVICE array of n_slabs entries
+ * (e.g. several ranks' plans concatenated in any order), offsets into
+ * state_o / state_lse.  workspace: device, >= rlk_attn_workspace_size(...,
+ * RLK_OP_MERGE, ...) bytes.  Every block of every row must be present exactly
+ * once: a duplicate sets RLK_ERR_DUPLICATE_BLOCK, a missing one
+ * RLK_ERR_MISSING_BLOCK (and NaN rows) on the device error word.
+ * [P1] Transformer Engine Reuse; the drift-class table (merge_order_probe:
+ * reversed arrival equals the sorted merge).
+ */
+rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
+                                 int64_t n_slabs, const float* state_o, const float* state_lse,
+                                 float* out_f32, void* out_bf16, float* lse, void* workspace,
+                                 size_t workspace_bytes, rlk_stream_t stream);
+
+/*
+ * Fused causal prefill (full or chunked replay): for each query row, the
+ * block states of blocks 0..last are computed and folded on chip in
+ * ascending order -- bit-identical to rlk_attn_prefill_states followed by
+ * rlk_attn_merge_states.  cp_rank >= 0 computes only the query rows that
+ * logical rank owns under the cp_layout partition of each sequence's q_len
+ * rows (other rows are left untouched); -1 computes every row.  Outputs as
+ * in rlk_attn_merge_states.  cu_seqlens_q/_k: HOST.
+ * [P1] Scope: full prefill and chunked-prefill replay; [P3] Acceptance.
+ */
+rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const void* k,
+                            const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t cp_rank, float* out_f32, void* out_bf16, float* lse,
+                            rlk_stream_t stream);
+
+/*
+ * Paged-KV decode: one query token per sequence, at the last position of its
+ * context, against keys stored in pages of page_size tokens:
+ *   q: device BF16 [num_seqs, Hq, 128]
+ *   k_pool, v_pool: device BF16 [n_pages, page_size, Hkv, 128]
+ *   page_table: device int32 [num_seqs, max_pages]; key t of sequence s is
+ *     slot t % page_size of page page_table[s * max_pages + t / page_size]
+ *   seqlens: HOST int32 [num_seqs], context lengths, 1 .. max_pages*page_size
+ *   out_f32 / out_bf16 / lse: device, [num_seqs, Hq, 128] / [num_seqs, Hq].
+ * page_size must divide kv_block_size and be >= 8: page_size-token pages
+ * are addressing only; the arithmetic blocks are the same kv_block_size
+ * global blocks as prefill, so the result equals the last row of the
+ * equivalent full prefill bit for bit.  A page id outside [0, n_pages) is
+ * read as zeros and sets RLK_ERR_BAD_PAGE on the device error word.
+ * [P3] PR stack: decode KV-cache replay, paged-KV adapter; Acceptance.
+ */
+rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                 const void* v_pool, int32_t n_pages, int32_t page_size,
+                                 const int32_t* page_table, int32_t max_pages,
+                                 const int32_t* seqlens, float* out_f32, void* out_bf16, float* lse,
+                                 rlk_stream_t stream);
+
+/*
+ * Deterministic backward of causal prefill (q_len == kv_len per sequence):
+ *   q, k, v, dout: device BF16; out_f32: device FP32 forward output;
+ *   lse: device FP32 forward lse; cu_seqlens: HOST [num_seqs + 1];
+ *   dq [Tq,Hq,128], dk, dv [Tk,Hkv,128]: device FP32 outputs.
+ * Delta_i = sum_d dout_id * out_id; P = exp(S - lse); dS = P (dP - Delta).
+ * dK/dV of a KV block accumulate over query blocks in ascending order, and
+ * within a query block over the Hq/Hkv query heads of the group in ascending
+ * order; dQ accumulates over KV blocks in ascending order; no atomics.
+ * cp_rank >= 0 computes the dK/dV rows of the KV blocks that rank produces
+ * and the dQ rows it owns (other rows untouched); -1 computes all.
+ * workspace: device, >= rlk_attn_workspace_size(..., RLK_OP_BACKWARD, ...).
+ * [P1] Scope: optional backward dq, dk, dv; [P3] Acceptance: dQ/dK/dV max
+ * abs 0.0 across ranks.
+ */
+rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const void* k,
+                             const void* v, const float* out_f32, const void* dout,
+                             const float* lse, const int32_t* cu_seqlens, int32_t cp_rank,
+                             float* dq, float* dk, float* dv, void* workspace,
+                             size_t workspace_bytes, rlk_stream_t stream);
+
+enum { RLK_OP_MERGE = 1, RLK_OP_BACKWARD = 2 };
+
+/* Workspace bytes an entry point needs (HOST cu_seqlens; 0 on bad input). */
+size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op,
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k);
+
+/* Synchronises `stream`, reads and clears the device error word of the
+ * current device; returns RLK_OK or the status of the first fault class. */
+rlk_status rlk_attn_check_device_error(rlk_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* rlk_attn_last_error(void);
+
+/* Provenance of the arithmetic core and merge order. */
+const char* rlk_attn_core_id(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_ATTN_H */

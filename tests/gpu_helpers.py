@@ -1,0 +1,120 @@
+"""Shared helpers of the GPU tests: run the library's entry points on device
+tensors and compare against the oracle with the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+TOL_OUT = 2e-5      # |out_f32 - oracle| (absolute)
+TOL_LSE = 1e-5      # |lse - oracle| (absolute)
+TOL_BF16_ULP = 1    # BF16 out vs the oracle rounded to BF16
+TOL_GRAD_REL_L2 = 1e-4
+
+
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+def lib():
+    from deterministic_context_attention_gb300 import build as rbuild
+    import deterministic_context_attention_gb300 as rlk
+    rbuild.build()
+    rlk.load()
+    return rlk
+
+
+def device_inputs(prob):
+    from deterministic_context_attention_gb300 import device as dv
+    return dv.bf16_to_device(prob.q), dv.bf16_to_device(prob.k), dv.bf16_to_device(prob.v)
+
+
+def params_of(prob, cp=1, layout=1):
+    import deterministic_context_attention_gb300 as rlk
+    return rlk.make_params(len(prob.cu_q) - 1, prob.hq, prob.hkv, prob.block, cp, layout, prob.scale)
+
+
+def empty_outputs(torch, rows, hq):
+    out = torch.full((rows, hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    outb = torch.full((rows, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((rows, hq), float("nan"), dtype=torch.float32, device="cuda")
+    return out, outb, lse
+
+
+def to_np(out, outb, lse):
+    return out.cpu().numpy(), outb.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def run_fused(prob, cp=1, layout=1, ranks=None, qkv=None):
+    """Fused prefill; with ``ranks`` each listed logical rank writes its rows."""
+    torch = torch_cuda()
+    rlk = lib()
+    q, k, v = qkv if qkv is not None else device_inputs(prob)
+    out, outb, lse = empty_outputs(torch, q.shape[0], prob.hq)
+    p = params_of(prob, cp, layout)
+    for r in (ranks if ranks is not None else [-1]):
+        rlk.rlk_attn_prefill(p, q, k, v, prob.cu_q, prob.cu_k, r, out, outb, lse)
+    rlk.rlk_attn_check_device_error()
+    return to_np(out, outb, lse)
+
+
+def run_states_merge(prob, cp=1, layout=1, rank_order=None, shuffle_seed=None, qkv=None):
+    """Each logical rank produces its states (launched in ``rank_order``), the
+    slab lists are concatenated in that arrival order (optionally shuffled),
+    and the merge sorts and folds them."""
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    q, k, v = qkv if qkv is not None else device_inputs(prob)
+    p = params_of(prob, cp, layout)
+    order = list(range(cp)) if rank_order is None else list(rank_order)
+    plans, base = [], 0
+    for r in order:
+        slabs, npairs = rlk.rlk_attn_plan_states(p, prob.cu_q, prob.cu_k, r, base)
+        plans.append((r, slabs, base))
+        base += npairs
+    state_o = torch.full((max(base, 1), 128), float("nan"), dtype=torch.float32, device="cuda")
+    state_lse = torch.full((max(base, 1),), float("nan"), dtype=torch.float32, device="cuda")
+    for r, slabs, b0 in plans:
+        rlk.rlk_attn_prefill_states(p, q, k, v, prob.cu_q, prob.cu_k, r, b0, state_o, state_lse)
+    slabs = np.concatenate([s for _, s, _ in plans])
+    if shuffle_seed is not None:
+        slabs = slabs[np.random.default_rng(shuffle_seed).permutation(len(slabs))]
+    dslabs = dv.slabs_to_device(slabs)
+    ws_bytes = rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, prob.cu_q, prob.cu_k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out, outb, lse = empty_outputs(torch, q.shape[0], prob.hq)
+    rlk.rlk_attn_merge_states(p, prob.cu_q, prob.cu_k, dslabs, len(slabs), state_o, state_lse, out, outb, lse,
+                              ws)
+    rlk.rlk_attn_check_device_error()
+    return to_np(out, outb, lse)
+
+
+def bf16_ordered(x):
+    """Monotone integer image of BF16 values (for ulp distances)."""
+    from deterministic_context_attention_gb300.synth import bf16_round
+    b = (bf16_round(np.asarray(x, np.float32)).view(np.uint32) >> 16).astype(np.int64)
+    return np.where(b & 0x8000, 0x8000 - b, b + 0x8000)
+
+
+def assert_forward_parity(out, outb, lse, ref_out, ref_lse, what=""):
+    assert np.isfinite(out).all(), what
+    e_out = float(np.abs(out - ref_out).max())
+    e_lse = float(np.abs(lse - ref_lse).max())
+    ref_b = ref_out.astype(np.float32)
+    ulp = int(np.abs(bf16_ordered(outb) - bf16_ordered(ref_b)).max())
+    assert e_out <= TOL_OUT, f"{what}: max |out - oracle| = {e_out:.3g}"
+    assert e_lse <= TOL_LSE, f"{what}: max |lse - oracle| = {e_lse:.3g}"
+    assert ulp <= TOL_BF16_ULP, f"{what}: BF16 out {ulp} ulp from the oracle"
+    return e_out, e_lse, ulp
+
+
+def assert_bitwise(a, b, what=""):
+    for x, y, name in zip(a, b, ("out_f32", "out_bf16", "lse")):
+        xb = np.ascontiguousarray(x).view(np.uint32)
+        yb = np.ascontiguousarray(y).view(np.uint32)
+        if not np.array_equal(xb, yb):
+            n = int(np.sum(xb != yb))
+            raise AssertionError(f"{what}: {name} differs in {n} elements")

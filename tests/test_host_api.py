@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI (no GPU): the library loads and exports every
+entry point include/rlk_attn.h declares, argument validation fails closed
+before any launch, and the block plan / CP partition / manifest hash behave
+as the pages fix them."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import deterministic_context_attention_gb300 as rlk
+from deterministic_context_attention_gb300 import build as rbuild
+from deterministic_context_attention_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlk_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rbuild.build()
+    return rlk.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(rlk_attn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert "global_block_index" in rlk.rlk_attn_core_id()
+
+
+def test_slab_struct_layout_matches_header():
+    assert rlk.SLAB_DTYPE.itemsize == 32
+    assert ctypes.sizeof(rlk.rlk_attn_params) == 36
+
+
+@pytest.mark.parametrize("layout", [rlk.CONTIGUOUS, rlk.ZIGZAG])
+@pytest.mark.parametrize("cp", [1, 2, 4, 8])
+def test_plan_covers_every_block_once(lib, cp, layout):
+    lens = [4096, 3000, 1024, 777]
+    cu = synth.cu_seqlens(lens)
+    p = rlk.make_params(4, cp_size=cp, cp_layout=layout)
+    all_slabs, all_pairs = rlk.rlk_attn_plan_states(p, cu, cu, -1, 0)
+    assert len(all_slabs) == 32 + 24 + 8 + 7
+    seen = {}
+    base = 0
+    for r in range(cp):
+        slabs, npairs = rlk.rlk_attn_plan_states(p, cu, cu, r, base)
+        for s in slabs:
+            key = (int(s["seq"]), int(s["block"]))
+            assert key not in seen
+            seen[key] = r
+            assert s["producer"] == r
+        if len(slabs):
+            assert slabs["offset"][0] == base
+        base += npairs
+    assert base == all_pairs
+    assert sorted(seen) == sorted((int(s["seq"]), int(s["block"])) for s in all_slabs)
+    # rows of each slab: those whose causal window reaches the block
+    for s in all_slabs:
+        assert s["row_begin"] == s["block"] * 128
+        assert s["row_count"] == lens[s["seq"]] - s["row_begin"]
+    # (row, block) pairs of the 4-sequence workload, times 32 heads
+    pairs = sum(sum(L - b * 128 for b in range((L + 127) // 128)) for L in lens)
+    assert all_pairs == pairs * 32
+
+
+def test_plan_chunked_rows_are_bottom_right(lib):
+    # 100 new queries over a cache of 1000 keys: every query sees blocks 0..7
+    cu_q = np.array([0, 100], np.int32)
+    cu_k = np.array([0, 1000], np.int32)
+    p = rlk.make_params(1, num_q_heads=16, num_kv_heads=4)
+    slabs, npairs = rlk.rlk_attn_plan_states(p, cu_q, cu_k)
+    assert len(slabs) == 8
+    # block 7 holds keys 896..999; query row i sits at 900 + i
+    assert slabs[-1]["row_begin"] == 0 and slabs[-1]["row_count"] == 100
+    assert npairs == 8 * 100 * 16
+
+
+def test_manifest_hash_depends_on_blocks_and_producers(lib):
+    cu = synth.cu_seqlens([4096, 3000, 1024, 777])
+    h1 = rlk.rlk_attn_block_manifest_hash(rlk.make_params(4, cp_size=2), cu, cu)
+    assert h1 == rlk.rlk_attn_block_manifest_hash(rlk.make_params(4, cp_size=2), cu, cu)
+    assert h1 != rlk.rlk_attn_block_manifest_hash(rlk.make_params(4, cp_size=4), cu, cu)
+    assert h1 != rlk.rlk_attn_block_manifest_hash(rlk.make_params(4, cp_size=2, kv_block_size=64), cu, cu)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, 2), ("causal", 0, 2), ("kv_block_size", 32, 2), ("cp_size", 9, 1),
+    ("num_kv_heads", 3, 1), ("num_seqs", 0, 2), ("softmax_scale", float("nan"), 1),
+])
+def test_bad_params_fail_closed(lib, field, value, status):
+    cu = synth.cu_seqlens([16])
+    p = rlk.make_params(1)
+    setattr(p, field, value)
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_prefill(p, 16, 16, 16, cu, cu, -1, 16, None, 16, stream=0)
+    assert e.value.status == status
+    assert rlk.rlk_attn_last_error()
+
+
+def test_bad_lengths_and_pointers_fail_closed(lib):
+    p = rlk.make_params(1)
+    with pytest.raises(rlk.RlkError) as e:  # q_len > kv_len
+        rlk.rlk_attn_prefill(p, 16, 16, 16, [0, 20], [0, 10], -1, 16, None, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(rlk.RlkError) as e:  # misaligned q
+        rlk.rlk_attn_prefill(p, 18, 16, 16, [0, 10], [0, 10], -1, 16, None, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(rlk.RlkError) as e:  # no output
+        rlk.rlk_attn_prefill(p, 16, 16, 16, [0, 10], [0, 10], -1, None, None, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(rlk.RlkError) as e:  # cp_rank out of range
+        rlk.rlk_attn_prefill(p, 16, 16, 16, [0, 10], [0, 10], 1, 16, None, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(rlk.RlkError) as e:  # page size that does not divide the block
+        rlk.rlk_attn_decode_paged(p, 16, 16, 16, 4, 12, 16, 4, [10], 16, None, 16, stream=0)
+    assert e.value.status == 2
+    with pytest.raises(rlk.RlkError) as e:  # context longer than its page table row
+        rlk.rlk_attn_decode_paged(p, 16, 16, 16, 4, 16, 16, 4, [65], 16, None, 16, stream=0)
+    assert e.value.status == 1
+
+
+def test_workspace_sizes(lib):
+    cu = synth.cu_seqlens([4096, 3000, 1024, 777])
+    p = rlk.make_params(4)
+    assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, cu, cu) >= 4 * 32 * 4
+    assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_BACKWARD, cu) >= int(cu[-1]) * 32 * 4
+    assert rlk.rlk_attn_workspace_size(p, 99, cu, cu) == 0
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_merge_states(p, cu, cu, 16, 1, 16, 16, 16, None, 16, 16, 8, stream=0)
+    assert e.value.status == 3

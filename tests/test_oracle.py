@@ -286,8 +286,8 @@ def test_paged_decode_equals_last_prefill_row():
         q = np.zeros((ctx, dec.hq, dec.d), np.float32)
         q[-1] = dec.q[s]
         cu = np.array([0, ctx], np.int32)
-        o, l = oracle.attention_f64(q, dec.k_seq[s], dec.v_seq[s], cu, cu, dec.scale,
-                                    rows=np.array([ctx - 1]))
+        ks, vs = dec.seq_kv(s)
+        o, l = oracle.attention_f64(q, ks, vs, cu, cu, dec.scale, rows=np.array([ctx - 1]))
         np.testing.assert_allclose(out[s], o[0], atol=1e-14, rtol=0)
         np.testing.assert_allclose(lse[s], l[0], atol=1e-14, rtol=0)
 
