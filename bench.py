@@ -109,7 +109,10 @@ class Clocks:
 
 
 def time_steps(torch, fn, steps, warmup, flush, stream):
-    """Per-step device time (ms) of fn() with an L2 flush before each step."""
+    """Per-step device time (ms) of fn() with an L2 flush before each step.
+    A short device-side sleep after the flush keeps the stream busy while the
+    host prepares the launch, so host-side launch cost stays outside the
+    events."""
     for _ in range(warmup):
         flush.zero_()
         fn()
@@ -118,6 +121,7 @@ def time_steps(torch, fn, steps, warmup, flush, stream):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
         flush.zero_()
+        torch.cuda._sleep(400000)
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -383,7 +387,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-extras", action="store_true")

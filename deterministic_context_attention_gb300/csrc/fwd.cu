@@ -18,16 +18,20 @@
 // Status and Acceptance: fixed merge order, full-KV arithmetic retained, max
 // abs 0.0 across ranks).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r)
 //   warps 4-7  softmax: thread r owns TMEM lane r, writes P_hi/P_lo to TMEM
 //              over its scores (per 16-key MMA step: 8 columns hi, 8 lo)
 //   warp  8    TMA producer (Q tile, K/V blocks or pages)
 //   warp  9    TMEM allocator and MMA issuer (also zeroes V rows past the
 //              valid length of a partial block)
+//   warps 10-11 idle (the block is sized in whole warpgroups, the unit in
+//              which registers are granted)
 // TMEM (512 columns): S/P double buffer [0,256), PV [256,384), O [384,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <cstdio>
 
 #include "numerics.cuh"
 #include "ptx.cuh"
@@ -112,7 +116,7 @@ __device__ __forceinline__ int visible_keys(int pos, int kv_len, int b, int B) {
 }
 
 template <int B, int MODE>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(384, 1)
     rlk_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = FwdLayout<B>;
@@ -313,7 +317,7 @@ __global__ void __maxnreg__(200)
       kv_it += it.nb;
       s_it += it.nb;
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax
     const int r = tid - 128;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -381,7 +385,7 @@ __global__ void __maxnreg__(200)
       }
       if (fail) break;
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ correction / epilogue
     const int r = tid;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -507,8 +511,15 @@ static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const
   auto kern = rlk_fwd_kernel<B, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 320, L::kAlloc, stream>>>(p, tq, tk, tv);
-  return cudaGetLastError();
+  kern<<<grid, 384, L::kAlloc, stream>>>(p, tq, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kern) == cudaSuccess)
+      fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers, max %d threads/block, %zu B dynamic smem\n", B, MODE,
+              a.numRegs, a.maxThreadsPerBlock, static_cast<size_t>(L::kAlloc));
+  }
+  return e;
 }
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -96,7 +96,7 @@ def bf16_ordered(x):
     """Monotone integer image of BF16 values (for ulp distances)."""
     from deterministic_context_attention_gb300.synth import bf16_round
     b = (bf16_round(np.asarray(x, np.float32)).view(np.uint32) >> 16).astype(np.int64)
-    return np.where(b & 0x8000, 0x8000 - b, b + 0x8000)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
 def assert_forward_parity(out, outb, lse, ref_out, ref_lse, what=""):
