@@ -313,7 +313,42 @@ def measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args):
                      "sum_ctx": int(ctx.sum())}
     del kp, vp
     torch.cuda.empty_cache()
+    res["backward"] = measure_backward(torch, rlk, dv, peaks, flush, stream, args)
     return res
+
+
+def backward_workload(torch, rlk, dv):
+    cfg = dict(synth.CFG_BACKWARD)
+    prob = synth.prefill_problem(**cfg)
+    q, k, v = dv.bf16_to_device(prob.q), dv.bf16_to_device(prob.k), dv.bf16_to_device(prob.v)
+    T = q.shape[0]
+    p = rlk.make_params(2, 32, 8, 128, 1, rlk.ZIGZAG, prob.scale)
+    out = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((T, 32), dtype=torch.float32, device="cuda")
+    rlk.rlk_attn_prefill(p, q, k, v, prob.cu_q, prob.cu_k, -1, out, None, lse)
+    do = dv.bf16_to_device(synth.normal_bf16(cfg["seed"], synth.T_DOUT, prob.q.shape))
+    dq = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+    dk = torch.empty((T, 8, 128), dtype=torch.float32, device="cuda")
+    dvv = torch.empty((T, 8, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_BACKWARD, prob.cu_q), dtype=torch.uint8,
+                     device="cuda")
+    flops = 2.5 * synth.prefill_flops(prob.cu_q, prob.cu_k, 32, 128)
+    return prob, p, (q, k, v, out, do, lse, dq, dk, dvv, ws), flops
+
+
+def measure_backward(torch, rlk, dv, peaks, flush, stream, args):
+    """dQ/dK/dV of causal prefill, 2 x 4096 tokens, 32/8/128: algorithmic
+    TFLOP/s = 2.5 x forward flops (five matmul-equivalents)."""
+    prob, p, (q, k, v, out, do, lse, dq, dk, dvv, ws), flops = backward_workload(torch, rlk, dv)
+    t = time_steps(torch, lambda: rlk.rlk_attn_backward(p, q, k, v, out, do, lse, prob.cu_q, -1, dq, dk, dvv, ws,
+                                                         stream=stream),
+                   args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    ms = float(np.mean(t))
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": flops,
+            "frac": round(tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
+            "workload": "2 x 4096 causal, Hq32/Hkv8/D128, dout ~ N(0,1) bf16; preprocess + dK/dV + dQ kernels"}
 
 
 def cpu_baseline(seconds_target):
@@ -384,6 +419,71 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Run one entry point a few times without timing, for ncu captures:
+    --profile prefill|states|merge|decode|backward."""
+    import torch
+    import deterministic_context_attention_gb300 as rlk
+    from deterministic_context_attention_gb300 import build as rbuild
+    from deterministic_context_attention_gb300 import device as dv
+    rbuild.build()
+    rlk.load()
+    stream = torch.cuda.current_stream()
+    n = args.profile_iters
+    if args.profile == "backward":
+        prob, p, (q, k, v, out, do, lse, dq, dk, dvv, ws), _ = backward_workload(torch, rlk, dv)
+        for _ in range(n):
+            rlk.rlk_attn_backward(p, q, k, v, out, do, lse, prob.cu_q, -1, dq, dk, dvv, ws, stream=stream)
+    elif args.profile == "decode":
+        g = torch.Generator(device="cuda")
+        g.manual_seed(3)
+        ctx = synth.rng(3, synth.T_LENS).integers(512, 32769, size=64).astype(np.int32)
+        pages_per = (ctx + 15) // 16
+        n_pages = int(pages_per.sum())
+        perm = synth.rng(3, synth.T_PAGES).permutation(n_pages).astype(np.int32)
+        pt = np.full((64, int(pages_per.max())), -1, np.int32)
+        off = 0
+        for s_ in range(64):
+            pt[s_, :pages_per[s_]] = perm[off:off + pages_per[s_]]
+            off += pages_per[s_]
+        kp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+        vp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+        qd = torch.randn((64, 32, 128), generator=g, device="cuda").to(torch.bfloat16)
+        ptd = dv.i32_to_device(pt)
+        pd = rlk.make_params(64, 32, 8, 128)
+        o = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
+        ob = torch.empty((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+        l = torch.empty((64, 32), dtype=torch.float32, device="cuda")
+        for _ in range(n):
+            rlk.rlk_attn_decode_paged(pd, qd, kp, vp, n_pages, 16, ptd, pt.shape[1], ctx, o, ob, l, stream=stream)
+    else:
+        prob, _ = prefill_workload()
+        q, k, v = dv.bf16_to_device(prob.q), dv.bf16_to_device(prob.k), dv.bf16_to_device(prob.v)
+        rows = q.shape[0]
+        p = rlk.make_params(4, 32, 8, 128, 1, rlk.ZIGZAG, prob.scale)
+        out = torch.empty((rows, 32, 128), dtype=torch.float32, device="cuda")
+        outb = torch.empty((rows, 32, 128), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((rows, 32), dtype=torch.float32, device="cuda")
+        if args.profile == "prefill":
+            for _ in range(n):
+                rlk.rlk_attn_prefill(p, q, k, v, prob.cu_q, prob.cu_k, -1, out, outb, lse, stream=stream)
+        else:
+            slabs, npairs = rlk.rlk_attn_plan_states(p, prob.cu_q, prob.cu_k, -1, 0)
+            so = torch.empty((npairs, 128), dtype=torch.float32, device="cuda")
+            sl = torch.empty((npairs,), dtype=torch.float32, device="cuda")
+            ds = dv.slabs_to_device(slabs)
+            ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, prob.cu_q, prob.cu_k),
+                             dtype=torch.uint8, device="cuda")
+            for _ in range(n):
+                rlk.rlk_attn_prefill_states(p, q, k, v, prob.cu_q, prob.cu_k, -1, 0, so, sl, stream=stream)
+                if args.profile == "merge":
+                    rlk.rlk_attn_merge_states(p, prob.cu_q, prob.cu_k, ds, len(slabs), so, sl, out, outb, lse, ws,
+                                              stream=stream)
+    torch.cuda.synchronize()
+    rlk.rlk_attn_check_device_error(stream)
+    print("profile run ok:", args.profile, n)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,7 +494,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-rows", type=int, default=48)
+    ap.add_argument("--profile", default=None, choices=["prefill", "states", "merge", "decode", "backward"])
+    ap.add_argument("--profile-iters", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

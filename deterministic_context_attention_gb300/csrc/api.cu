@@ -254,6 +254,16 @@ void base_fwd(rlk::FwdParams* fp, const rlk_attn_params* p, const DeviceInfo* de
 
 }  // namespace
 
+namespace rlk {
+// Device address of the error word on the current device (nullptr if the
+// device is unusable).
+ErrWord* device_error_word() {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != RLK_OK) return nullptr;
+  return d->err;
+}
+}  // namespace rlk
+
 extern "C" {
 
 const char* rlk_attn_last_error(void) { return g_last_error.c_str(); }

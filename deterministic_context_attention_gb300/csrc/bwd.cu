@@ -1,19 +1,643 @@
-// bwd.cu -- deterministic backward (placeholder until the kernels land).
+// bwd.cu -- deterministic backward of causal GQA attention for sm_103a.
+//
+// Three kernels, one stream, no atomics on any result:
+//   preprocess  Delta_i = sum_d dout_id * out_id (fixed order), written with
+//               lse transposed to [Hq][T] for coalesced per-block reads;
+//   dK/dV       one CTA per (sequence, KV head g, KV block j).  For query
+//               blocks i = j .. last in ascending order, and within each for
+//               the query heads of group g in ascending order, it recomputes
+//               S^T = K_j Q_i^T and dP^T = V_j dO_i^T on the tensor core, forms
+//               P^T = exp(S^T - lse) and dS^T = P^T (dP^T - Delta), and
+//               accumulates dV += P^T dO and dK += dS^T Q in TMEM (FP32), with
+//               P^T and dS^T each split into BF16 hi + lo parts;
+//   dQ          one CTA per (sequence, query head, query block i): for KV
+//               blocks j = 0 .. i ascending, S = Q_i K_j^T, dP = dO_i V_j^T,
+//               dS as above, dQ += dS K_j in TMEM.
+// The reduction order of every dK/dV/dQ element is therefore fixed by the
+// block decomposition alone, so the result is bitwise identical across
+// logical CP ranks and repeated runs ("[WS2][Attention] H100 validation and
+// reproduction guide", Acceptance: dQ/dK/dV max abs 0.0 at 2/4/8 ranks;
+// "WS2 Attention PR5 Drift Benchmark", Scope: optional backward dq, dk, dv).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <vector>
+
 #include "../../include/rlk_attn.h"
+#include "numerics.cuh"
+#include "ptx.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
 
-size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu) {
-  const size_t rows = static_cast<size_t>(cu[prm->num_seqs]);
-  return (rows * prm->num_q_heads * sizeof(float) + 255) / 256 * 256;
+ErrWord* device_error_word();  // api.cu
+
+constexpr float kLog2e = 1.44269504088896340736f;
+
+struct alignas(16) BwdItem {
+  int32_t seq;
+  int32_t head;   // dK/dV: KV head g; dQ: query head h
+  int32_t block;  // dK/dV: KV block j; dQ: first row of the query tile
+  int32_t rows;   // dQ: rows of the tile written; dK/dV: unused
+};
+
+constexpr int kMaxBwdItems = 1800;
+
+struct BwdParams {
+  ErrWord* err;
+  int32_t hq, hkv, group, num_items;
+  int64_t t_pad;        // row stride of the transposed lse / Delta
+  float scale, scale_log2;
+  const float* lse_t;   // [hq][t_pad]
+  const float* delta_t; // [hq][t_pad]
+  float* dq;
+  float* dk;
+  float* dv;
+  int32_t cu[kMaxSeqs + 1];
+  BwdItem items[kMaxBwdItems];
+};
+
+// ------------------------------------------------------------------ preprocess
+struct PrepParams {
+  int32_t hq;
+  int64_t rows, t_pad;
+  const float* out;
+  const uint16_t* dout;
+  const float* lse;
+  float* lse_t;
+  float* delta_t;
+};
+
+// One warp per (row, head): lane l takes elements 4l..4l+3 (fma in order),
+// then a fixed xor butterfly.
+__global__ void __launch_bounds__(256) rlk_bwd_prep_kernel(const __grid_constant__ PrepParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); w < p.rows * p.hq; w += warps) {
+    const int64_t row = w / p.hq;
+    const int h = static_cast<int>(w - row * p.hq);
+    const float4 o = *reinterpret_cast<const float4*>(p.out + w * kHeadDim + 4 * lane);
+    const uint2 d = *reinterpret_cast<const uint2*>(p.dout + w * kHeadDim + 4 * lane);
+    float acc = __fmul_rn(bf16_lo_as_f32(d.x), o.x);
+    acc = __fmaf_rn(bf16_hi_as_f32(d.x), o.y, acc);
+    acc = __fmaf_rn(bf16_lo_as_f32(d.y), o.z, acc);
+    acc = __fmaf_rn(bf16_hi_as_f32(d.y), o.w, acc);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if (lane == 0) {
+      p.delta_t[static_cast<int64_t>(h) * p.t_pad + row] = acc;
+      p.lse_t[static_cast<int64_t>(h) * p.t_pad + row] = p.lse[w];
+    }
+  }
 }
 
-rlk_status run_backward(const rlk_attn_params*, const void*, const void*, const void*, const float*, const void*,
-                        const float*, const int32_t*, int32_t, float*, float*, float*, void*, size_t, cudaStream_t) {
-  return RLK_ERR_UNSUPPORTED;
+// ------------------------------------------------------------------ shared layout
+struct BwdLayout {
+  static constexpr int kTile = 128 * kHeadDim * 2;  // one 128 x 128 BF16 tile (two 64-column halves)
+  static constexpr int kHalf = 128 * 128;
+  static constexpr int kResOff = 0;                 // resident pair (K_j,V_j) or (Q_i,dO_i)
+  static constexpr int kStreamOff = 2 * kTile;      // 2 stages x streamed pair
+  static constexpr int kStages = 2;
+  static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;  // [2][2][128] floats (lse, Delta)
+  static constexpr int kBarOff = kVecOff + 2 * 2 * 128 * 4;
+  // barriers
+  static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 7,
+                       kAccFull = 8, kAccEmpty = 9, kNumBars = 10;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kTotal = kMiscOff + 16;
+  static constexpr int kAlloc = kTotal + 1024;
+};
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int k) {  // K-major operand, K-step k (16 elements)
+  return sdesc_sw128(tile + (k >> 2) * BwdLayout::kHalf + (k & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int k) {  // MN-major operand, K-step k (16 rows)
+  return sdesc_sw128(tile + k * 16 * 128, BwdLayout::kHalf, 1024);
+}
+
+// Per-element backward arithmetic shared by both kernels:
+//   p  = 2^(s * scale_log2 - lse * log2 e)    (0 where masked)
+//   ds = p * (dp - Delta)                      (0 where masked)
+__device__ __forceinline__ void p_and_ds(float s, float dp, float lse2, float delta, bool ok, float scale_log2,
+                                         float& p, float& ds) {
+  const float x = __fsub_rn(__fmul_rn(s, scale_log2), lse2);
+  p = ok ? ex2_hw(x) : 0.0f;
+  ds = ok ? __fmul_rn(p, __fsub_rn(dp, delta)) : 0.0f;
+}
+
+// KIND 0: dK/dV (rows = keys of block j, columns = query rows);
+// KIND 1: dQ    (rows = query rows,       columns = keys of block j).
+template <int KIND>
+__global__ void __launch_bounds__(384, 1)
+    rlk_bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_do) {
+  using L = BwdLayout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float* vecs = reinterpret_cast<float*>(smem + L::kVecOff);  // [buf][lse2, delta][128]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&bars[L::kResFull], 1);
+    mbar_init(&bars[L::kResEmpty], 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&bars[L::kStFull + s], 1);
+      mbar_init(&bars[L::kStEmpty + s], 1);
+    }
+    mbar_init(&bars[L::kSFull], 1);
+    mbar_init(&bars[L::kPFull], 128);
+    mbar_init(&bars[L::kAccFull], 1);
+    mbar_init(&bars[L::kAccEmpty], 128);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_s = tmem, tm_dp = tmem + 128, tm_acc0 = tmem + 256, tm_acc1 = tmem + 384;
+  const uint32_t res_addr = smem_u32(smem + L::kResOff);
+  uint8_t* st_base = smem + L::kStreamOff;
+
+  // steps of an item: dK/dV: (query block i from j to the last) x (heads of the
+  // group); dQ: KV blocks 0 .. last of the tile.
+  auto item_steps = [&](const BwdItem& it, int& len, int& nsteps) {
+    len = p.cu[it.seq + 1] - p.cu[it.seq];
+    if (KIND == 0) {
+      const int nq = (len + 127) / 128;
+      nsteps = (nq - it.block) * p.group;
+    } else {
+      nsteps = (it.block + it.rows - 1) / 128 + 1;
+    }
+  };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    uint32_t res_it = 0, st_it = 0;
+    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      const BwdItem it = p.items[item];
+      int len, nsteps;
+      item_steps(it, len, nsteps);
+      const int tok0 = p.cu[it.seq];
+      bool ok = mbar_wait(&bars[L::kResEmpty], (res_it & 1) ^ 1, abort, p.err, 0x601);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[L::kResFull], 2 * L::kTile);
+        uint8_t* a = smem + L::kResOff;
+        if (KIND == 0) {
+          const int r = tok0 + it.block * 128;
+          tma_load_3d(a, &tm_k, &bars[L::kResFull], 0, it.head, r);
+          tma_load_3d(a + L::kHalf, &tm_k, &bars[L::kResFull], 64, it.head, r);
+          tma_load_3d(a + L::kTile, &tm_v, &bars[L::kResFull], 0, it.head, r);
+          tma_load_3d(a + L::kTile + L::kHalf, &tm_v, &bars[L::kResFull], 64, it.head, r);
+        } else {
+          const int r = tok0 + it.block;
+          tma_load_3d(a, &tm_q, &bars[L::kResFull], 0, it.head, r);
+          tma_load_3d(a + L::kHalf, &tm_q, &bars[L::kResFull], 64, it.head, r);
+          tma_load_3d(a + L::kTile, &tm_do, &bars[L::kResFull], 0, it.head, r);
+          tma_load_3d(a + L::kTile + L::kHalf, &tm_do, &bars[L::kResFull], 64, it.head, r);
+        }
+      }
+      ++res_it;
+      for (int t = 0; t < nsteps; ++t) {
+        const uint32_t stage = st_it % L::kStages;
+        ok = mbar_wait(&bars[L::kStEmpty + stage], ((st_it / L::kStages) & 1) ^ 1, abort, p.err, 0x602);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) {
+          uint8_t* d = st_base + stage * 2 * L::kTile;
+          mbar_arrive_expect_tx(&bars[L::kStFull + stage], 2 * L::kTile);
+          if (KIND == 0) {
+            const int i = it.block + t / p.group;
+            const int h = it.head * p.group + t % p.group;
+            const int r = tok0 + i * 128;
+            tma_load_3d(d, &tm_q, &bars[L::kStFull + stage], 0, h, r);
+            tma_load_3d(d + L::kHalf, &tm_q, &bars[L::kStFull + stage], 64, h, r);
+            tma_load_3d(d + L::kTile, &tm_do, &bars[L::kStFull + stage], 0, h, r);
+            tma_load_3d(d + L::kTile + L::kHalf, &tm_do, &bars[L::kStFull + stage], 64, h, r);
+          } else {
+            const int g = it.head / p.group;
+            const int r = tok0 + t * 128;
+            tma_load_3d(d, &tm_k, &bars[L::kStFull + stage], 0, g, r);
+            tma_load_3d(d + L::kHalf, &tm_k, &bars[L::kStFull + stage], 64, g, r);
+            tma_load_3d(d + L::kTile, &tm_v, &bars[L::kStFull + stage], 0, g, r);
+            tma_load_3d(d + L::kTile + L::kHalf, &tm_v, &bars[L::kStFull + stage], 64, g, r);
+          }
+        }
+        ++st_it;
+      }
+      if (*abort) break;
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdK = idesc_bf16(128, 128, false, false);  // both operands K-major
+    constexpr uint32_t kIdMN = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
+    uint32_t res_it = 0, st_it = 0, s_it = 0, acc_it = 0;
+    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      const BwdItem it = p.items[item];
+      int len, nsteps;
+      item_steps(it, len, nsteps);
+      bool ok = mbar_wait(&bars[L::kResFull], res_it & 1, abort, p.err, 0x611);
+      ok = ok && mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ++res_it;
+      bool fail = false;
+      for (int t = 0; t < nsteps; ++t) {
+        const uint32_t stage = st_it % L::kStages;
+        bool w = mbar_wait(&bars[L::kStFull + stage], (st_it / L::kStages) & 1, abort, p.err, 0x613);
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+        tc_fence_after();
+        const uint32_t st_addr = smem_u32(st_base + stage * 2 * L::kTile);
+        // resident A = (K_j, V_j) [dK/dV] or (Q_i, dO_i) [dQ]; streamed B = the other pair
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK, k > 0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK, k > 0);
+          umma_commit(&bars[L::kSFull]);
+        }
+        __syncwarp();
+        w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+        ++s_it;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t first = (t == 0) ? 0u : 1u;
+          if (KIND == 0) {
+            // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: N = D, K = query rows)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              umma_ts(tm_acc0, tm_s + 16 * k, mndesc(st_addr + L::kTile, k), kIdMN, (k > 0) ? 1u : first);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) umma_ts(tm_acc0, tm_s + 16 * k + 8, mndesc(st_addr + L::kTile, k), kIdMN, 1u);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              umma_ts(tm_acc1, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (k > 0) ? 1u : first);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
+          } else {
+            // dQ += dS K_j  (B = K_j MN-major: N = D, K = keys)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (k > 0) ? 1u : first);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
+          }
+          umma_commit(&bars[L::kStEmpty + stage]);
+          if (t + 1 == nsteps) {
+            umma_commit(&bars[L::kAccFull]);
+            umma_commit(&bars[L::kResEmpty]);
+          }
+        }
+        __syncwarp();
+        ++st_it;
+      }
+      if (fail) break;
+      ++acc_it;
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P / dS
+    const int r = tid - 128;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t s_it = 0;
+    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      const BwdItem it = p.items[item];
+      int len, nsteps;
+      item_steps(it, len, nsteps);
+      const int tok0 = p.cu[it.seq];
+      // dQ: this thread's row statistics are fixed for the item
+      float row_lse2 = 0.f, row_delta = 0.f;
+      int row_pos = 0;
+      bool row_ok = false;
+      if (KIND == 1) {
+        row_pos = it.block + r;
+        row_ok = r < it.rows && row_pos < len;
+        if (row_ok) {
+          const int64_t idx = static_cast<int64_t>(it.head) * p.t_pad + tok0 + row_pos;
+          row_lse2 = __fmul_rn(p.lse_t[idx], kLog2e);
+          row_delta = p.delta_t[idx];
+        }
+      }
+      const int key_pos = (KIND == 0) ? it.block * 128 + r : 0;
+      bool fail = false;
+      for (int t = 0; t < nsteps; ++t) {
+        float* vb = vecs + (s_it & 1) * 256;
+        int col0;  // position of column 0 of this step
+        if (KIND == 0) {
+          const int i = it.block + t / p.group;
+          const int h = it.head * p.group + t % p.group;
+          col0 = i * 128;
+          // column statistics of the step's query block, shared through smem
+          const int qp = col0 + r;
+          const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
+          vb[r] = qp < len ? __fmul_rn(p.lse_t[idx], kLog2e) : 0.f;
+          vb[128 + r] = qp < len ? p.delta_t[idx] : 0.f;
+          named_bar_sync(1, 128);
+        } else {
+          col0 = t * 128;
+        }
+        bool w = mbar_wait(&bars[L::kSFull], s_it & 1, abort, p.err, 0x621);
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tm_s + lane_off + 32 * c, sr);
+          tmem_ld32(tm_dp + lane_off + 32 * c, dr);
+          tmem_ld_wait(sr);
+          tmem_ld_wait(dr);
+          uint32_t pw[32], dw[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], dsv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int col = 32 * c + e + u;
+              bool ok;
+              float lse2, delta;
+              if (KIND == 0) {
+                const int qp = col0 + col;
+                ok = key_pos < len && qp < len && qp >= key_pos;
+                lse2 = vb[col];
+                delta = vb[128 + col];
+              } else {
+                const int kp = col0 + col;
+                ok = row_ok && kp <= row_pos;
+                lse2 = row_lse2;
+                delta = row_delta;
+              }
+              p_and_ds(__uint_as_float(sr[e + u]), __uint_as_float(dr[e + u]), lse2, delta, ok, p.scale_log2,
+                       pv[u], dsv[u]);
+            }
+            const int slot = (e >> 4) * 16 + ((e & 15) >> 1);
+            uint32_t hi, lo;
+            split_pair(pv[0], pv[1], hi, lo);
+            pw[slot] = hi;
+            pw[slot + 8] = lo;
+            split_pair(dsv[0], dsv[1], hi, lo);
+            dw[slot] = hi;
+            dw[slot + 8] = lo;
+          }
+          tmem_st32(tm_s + lane_off + 32 * c, pw);
+          tmem_st32(tm_dp + lane_off + 32 * c, dw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[L::kPFull]);
+        ++s_it;
+      }
+      if (fail) break;
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ epilogue
+    const int r = tid;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t acc_it = 0;
+    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      const BwdItem it = p.items[item];
+      int len, nsteps;
+      item_steps(it, len, nsteps);
+      const int tok0 = p.cu[it.seq];
+      bool w = mbar_wait(&bars[L::kAccFull], acc_it & 1, abort, p.err, 0x631);
+      if (!__all_sync(0xffffffffu, w)) break;
+      tc_fence_after();
+      const int nacc = (KIND == 0) ? 2 : 1;
+      for (int a = 0; a < nacc; ++a) {
+        float* dst_base;
+        bool ok;
+        float mul;
+        if (KIND == 0) {
+          const int kp = it.block * 128 + r;
+          ok = kp < len;
+          const int64_t row = static_cast<int64_t>(tok0 + kp) * p.hkv + it.head;
+          dst_base = (a == 0 ? p.dv : p.dk) + row * kHeadDim;
+          mul = (a == 0) ? 1.0f : p.scale;
+        } else {
+          const int qp = it.block + r;
+          ok = r < it.rows && qp < len;
+          const int64_t row = static_cast<int64_t>(tok0 + qp) * p.hq + it.head;
+          dst_base = p.dq + row * kHeadDim;
+          mul = p.scale;
+        }
+        const uint32_t src = (a == 0 ? tm_acc0 : tm_acc1) + lane_off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          tmem_ld32(src + 32 * c, x);
+          tmem_ld_wait(x);
+          if (ok) {
+            float4* dst = reinterpret_cast<float4*>(dst_base + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              // dV is the raw sum; dK and dQ take the softmax scale here
+              float v0 = __uint_as_float(x[e]), v1 = __uint_as_float(x[e + 1]);
+              float v2 = __uint_as_float(x[e + 2]), v3 = __uint_as_float(x[e + 3]);
+              if (mul != 1.0f) {
+                v0 = __fmul_rn(v0, mul);
+                v1 = __fmul_rn(v1, mul);
+                v2 = __fmul_rn(v2, mul);
+                v3 = __fmul_rn(v3, mul);
+              }
+              dst[e / 4] = make_float4(v0, v1, v2, v3);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[L::kAccEmpty]);
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    if (*abort) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_map_bwd(CUtensorMap* m, const void* base, uint64_t heads, uint64_t rows) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  cuuint64_t dims[3] = {128, heads, rows};
+  cuuint64_t strides[2] = {256, 256 * heads};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::vector<int> cp_chunks_owner(int n, int cp, int layout, int rank, std::vector<std::pair<int, int>>* ranges) {
+  std::vector<int> owner;
+  const int chunks = layout == 0 ? cp : 2 * cp;
+  for (int c = 0; c < chunks; ++c) {
+    const int b = static_cast<int>(static_cast<int64_t>(c) * n / chunks);
+    const int e = static_cast<int>(static_cast<int64_t>(c + 1) * n / chunks);
+    const int r = layout == 0 ? c : (c < cp ? c : 2 * cp - 1 - c);
+    if (ranges && r == rank && e > b) ranges->push_back({b, e});
+    owner.push_back(r);
+  }
+  return owner;
+}
+
+int owner_of(int pos, int n, int cp, int layout) {
+  const int chunks = layout == 0 ? cp : 2 * cp;
+  for (int c = 0; c < chunks; ++c) {
+    const int b = static_cast<int>(static_cast<int64_t>(c) * n / chunks);
+    const int e = static_cast<int>(static_cast<int64_t>(c + 1) * n / chunks);
+    if (pos >= b && pos < e) return layout == 0 ? c : (c < cp ? c : 2 * cp - 1 - c);
+  }
+  return -1;
+}
+
+template <int KIND>
+cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& items, const CUtensorMap& mq,
+                       const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int num_sms,
+                       cudaStream_t stream) {
+  auto kern = rlk_bwd_kernel<KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kAlloc);
+  if (e != cudaSuccess) return e;
+  for (size_t i0 = 0; i0 < items.size(); i0 += kMaxBwdItems) {
+    const size_t n = std::min(items.size() - i0, static_cast<size_t>(kMaxBwdItems));
+    std::copy(items.begin() + i0, items.begin() + i0 + n, bp->items);
+    bp->num_items = static_cast<int32_t>(n);
+    const int grid = std::min(static_cast<int>(n), num_sms);
+    kern<<<grid, 384, BwdLayout::kAlloc, stream>>>(*bp, mq, mk, mv, mdo);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+static_assert(sizeof(BwdParams) + 4 * sizeof(CUtensorMap) + 256 <= 32764, "backward parameters");
+
+size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu) {
+  const size_t t_pad = static_cast<size_t>(cu[prm->num_seqs]) + 128;
+  return (2 * t_pad * prm->num_q_heads * sizeof(float) + 255) / 256 * 256;
+}
+
+rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
+                        const float* out_f32, const void* dout, const float* lse, const int32_t* cu,
+                        int32_t cp_rank, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  (void)workspace_bytes;
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RLK_ERR_CUDA;
+  const int T = cu[prm->num_seqs];
+  if (T == 0) return RLK_OK;
+  if (prm->kv_block_size != 128) return RLK_ERR_UNSUPPORTED;
+  const int64_t t_pad = static_cast<int64_t>(T) + 128;
+  float* lse_t = static_cast<float*>(workspace);
+  float* delta_t = lse_t + t_pad * prm->num_q_heads;
+
+  // preprocess
+  PrepParams pp;
+  pp.hq = prm->num_q_heads;
+  pp.rows = T;
+  pp.t_pad = t_pad;
+  pp.out = out_f32;
+  pp.dout = static_cast<const uint16_t*>(dout);
+  pp.lse = lse;
+  pp.lse_t = lse_t;
+  pp.delta_t = delta_t;
+  {
+    int64_t blocks = (static_cast<int64_t>(T) * prm->num_q_heads + 7) / 8;
+    blocks = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms) * 8);
+    rlk_bwd_prep_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+  }
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map_bwd(&mq, q, prm->num_q_heads, T) || !make_map_bwd(&mk, k, prm->num_kv_heads, T) ||
+      !make_map_bwd(&mv, v, prm->num_kv_heads, T) || !make_map_bwd(&mdo, dout, prm->num_q_heads, T))
+    return RLK_ERR_CUDA;
+
+  auto bp = std::make_unique<BwdParams>();
+  std::memset(bp.get(), 0, sizeof(BwdParams));
+  bp->err = device_error_word();
+  if (!bp->err) return RLK_ERR_CUDA;
+  bp->hq = prm->num_q_heads;
+  bp->hkv = prm->num_kv_heads;
+  bp->group = prm->num_q_heads / prm->num_kv_heads;
+  bp->t_pad = t_pad;
+  bp->scale = prm->softmax_scale;
+  bp->scale_log2 = static_cast<float>(static_cast<double>(prm->softmax_scale) * 1.4426950408889634073599);
+  bp->lse_t = lse_t;
+  bp->delta_t = delta_t;
+  bp->dq = dq;
+  bp->dk = dk;
+  bp->dv = dv;
+  for (int s = 0; s <= prm->num_seqs; ++s) bp->cu[s] = cu[s];
+
+  // dK/dV items: (seq, KV head, KV block), most query blocks first
+  std::vector<std::pair<int, BwdItem>> kv;
+  std::vector<std::pair<int, BwdItem>> qi;
+  for (int s = 0; s < prm->num_seqs; ++s) {
+    const int len = cu[s + 1] - cu[s];
+    const int nb = (len + 127) / 128;
+    for (int j = 0; j < nb; ++j) {
+      if (cp_rank >= 0 && owner_of(j * 128, len, prm->cp_size, prm->cp_layout) != cp_rank) continue;
+      for (int g = 0; g < prm->num_kv_heads; ++g) kv.push_back({nb - j, BwdItem{s, g, j, 128}});
+    }
+    std::vector<std::pair<int, int>> ranges;
+    if (cp_rank < 0) ranges.push_back({0, len});
+    else cp_chunks_owner(len, prm->cp_size, prm->cp_layout, cp_rank, &ranges);
+    for (auto& rg : ranges)
+      for (int r0 = rg.first; r0 < rg.second; r0 += 128) {
+        const int rows = std::min(128, rg.second - r0);
+        const int cost = (r0 + rows - 1) / 128 + 1;
+        for (int h = 0; h < prm->num_q_heads; ++h) qi.push_back({cost, BwdItem{s, h, r0, rows}});
+      }
+  }
+  auto by_cost = [](const std::pair<int, BwdItem>& a, const std::pair<int, BwdItem>& b) { return a.first > b.first; };
+  std::stable_sort(kv.begin(), kv.end(), by_cost);
+  std::stable_sort(qi.begin(), qi.end(), by_cost);
+  std::vector<BwdItem> items;
+  for (auto& x : kv) items.push_back(x.second);
+  if (!items.empty() && launch_bwd<0>(bp.get(), items, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
+    return RLK_ERR_CUDA;
+  items.clear();
+  for (auto& x : qi) items.push_back(x.second);
+  if (!items.empty() && launch_bwd<1>(bp.get(), items, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
+    return RLK_ERR_CUDA;
+  return RLK_OK;
 }
 
 }  // namespace rlk

@@ -99,16 +99,33 @@ def bf16_ordered(x):
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def bf16_ulp(x):
+    """Spacing of BF16 numbers at |x| (the ulp of bf16_rn(x))."""
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
 def assert_forward_parity(out, outb, lse, ref_out, ref_lse, what=""):
+    """FP32 out within TOL_OUT, lse within TOL_LSE, and BF16 out within one
+    BF16 ulp of the oracle rounded to BF16.  The BF16 output is the FP32
+    output rounded once, so where an element is so close to zero that the
+    FP32 tolerance exceeds a BF16 ulp, the BF16 gate reads as the FP32 gate
+    plus half an ulp of that final rounding."""
     assert np.isfinite(out).all(), what
     e_out = float(np.abs(out - ref_out).max())
     e_lse = float(np.abs(lse - ref_lse).max())
     ref_b = ref_out.astype(np.float32)
-    ulp = int(np.abs(bf16_ordered(outb) - bf16_ordered(ref_b)).max())
+    ulp = np.abs(bf16_ordered(outb) - bf16_ordered(ref_b))
+    near_zero_ok = np.abs(outb.astype(np.float64) - ref_out) <= TOL_OUT + 0.5 * bf16_ulp(outb)
+    bad = (ulp > TOL_BF16_ULP) & ~near_zero_ok
     assert e_out <= TOL_OUT, f"{what}: max |out - oracle| = {e_out:.3g}"
     assert e_lse <= TOL_LSE, f"{what}: max |lse - oracle| = {e_lse:.3g}"
-    assert ulp <= TOL_BF16_ULP, f"{what}: BF16 out {ulp} ulp from the oracle"
-    return e_out, e_lse, ulp
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: BF16 out {int(ulp[tuple(i)])} ulp from the oracle at {tuple(i)}: "
+                             f"gpu {outb[tuple(i)]!r} oracle {ref_out[tuple(i)]!r}")
+    return e_out, e_lse, int(ulp[~near_zero_ok].max()) if (~near_zero_ok).any() else 0
 
 
 def assert_bitwise(a, b, what=""):

@@ -1,0 +1,107 @@
+"""GPU parity and bit invariance of the deterministic backward.
+
+dQ/dK/dV against the FP64 oracle within 1e-4 relative L2; bitwise identical
+across logical CP ranks {1, 2, 4} and repeated runs ("[WS2][Attention] H100
+validation and reproduction guide", Acceptance: dQ/dK/dV max abs 0.0 at
+2/4/8 ranks; "WS2 Attention PR5 Drift Benchmark", Scope: optional backward
+dq, dk, dv)."""
+import numpy as np
+import pytest
+
+import oracle
+from deterministic_context_attention_gb300 import synth
+from tests.gpu_helpers import TOL_GRAD_REL_L2, device_inputs, lib, params_of, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def forward_and_backward(prob, dout, cp=1, layout=1, ranks=None, qkv=None):
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    q, k, v = qkv if qkv is not None else device_inputs(prob)
+    T = q.shape[0]
+    p = params_of(prob, cp, layout)
+    out = torch.empty((T, prob.hq, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((T, prob.hq), dtype=torch.float32, device="cuda")
+    rlk.rlk_attn_prefill(p, q, k, v, prob.cu_q, prob.cu_k, -1, out, None, lse)
+    do = dv.bf16_to_device(dout)
+    dq = torch.full((T, prob.hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    dk = torch.full((T, prob.hkv, 128), float("nan"), dtype=torch.float32, device="cuda")
+    dvv = torch.full((T, prob.hkv, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_BACKWARD, prob.cu_q), dtype=torch.uint8,
+                     device="cuda")
+    for r in (ranks if ranks is not None else [-1]):
+        rlk.rlk_attn_backward(p, q, k, v, out, do, lse, prob.cu_q, r, dq, dk, dvv, ws)
+    rlk.rlk_attn_check_device_error()
+    return dq.cpu().numpy(), dk.cpu().numpy(), dvv.cpu().numpy()
+
+
+def rel_l2(x, ref):
+    return float(np.linalg.norm((x - ref).ravel()) / np.linalg.norm(ref.ravel()))
+
+
+def assert_bitwise3(a, b, what):
+    for x, y, name in zip(a, b, ("dq", "dk", "dv")):
+        if not np.array_equal(x.view(np.uint32), y.view(np.uint32)):
+            raise AssertionError(f"{what}: {name} differs in {int(np.sum(x.view(np.uint32) != y.view(np.uint32)))}")
+
+
+@pytest.fixture(scope="module")
+def small():
+    prob = synth.prefill_problem(lens=[300, 129, 1], hq=32, hkv=8, block=128, seed=14)
+    dout = synth.normal_bf16(14, synth.T_DOUT, prob.q.shape)
+    return prob, dout
+
+
+def test_backward_parity_small(small):
+    prob, dout = small
+    dq, dk, dv = forward_and_backward(prob, dout)
+    rq, rk, rv = oracle.backward_f64(prob.q, prob.k, prob.v, dout, prob.cu_q, prob.scale)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        assert np.isfinite(got).all(), name
+        e = rel_l2(got, ref)
+        assert e <= TOL_GRAD_REL_L2, f"{name}: relative L2 {e:.3g}"
+
+
+@pytest.mark.parametrize("cp", [2, 4])
+def test_backward_cp_and_repeat_bitwise(small, cp):
+    prob, dout = small
+    qkv = device_inputs(prob)
+    base = forward_and_backward(prob, dout, qkv=qkv)
+    assert_bitwise3(forward_and_backward(prob, dout, qkv=qkv), base, "repeat")
+    ranks = list(np.random.default_rng(cp).permutation(cp))
+    assert_bitwise3(forward_and_backward(prob, dout, cp=cp, layout=1, ranks=ranks, qkv=qkv), base, f"CP={cp}")
+
+
+@pytest.fixture(scope="module")
+def full():
+    prob = synth.prefill_problem(**synth.CFG_BACKWARD)
+    dout = synth.normal_bf16(synth.CFG_BACKWARD["seed"], synth.T_DOUT, prob.q.shape)
+    qkv = device_inputs(prob)
+    return prob, dout, qkv, forward_and_backward(prob, dout, qkv=qkv)
+
+
+def test_backward_fullsize_parity(full):
+    prob, dout, _, (dq, dk, dv) = full
+    s, g = 1, 5
+    rq, rk, rv = oracle.backward_f64(prob.q, prob.k, prob.v, dout, prob.cu_q, prob.scale, only_seq=s, only_group=g)
+    a, b = prob.cu_q[s], prob.cu_q[s + 1]
+    heads = slice(g * 4, g * 4 + 4)
+    for got, ref, name in ((dq[a:b, heads], rq[a:b, heads], "dq"), (dk[a:b, g], rk[a:b, g], "dk"),
+                           (dv[a:b, g], rv[a:b, g], "dv")):
+        e = rel_l2(got, ref)
+        assert e <= TOL_GRAD_REL_L2, f"{name}: relative L2 {e:.3g}"
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+@pytest.mark.parametrize("cp", [2, 4])
+def test_backward_fullsize_cp_bitwise(full, cp):
+    prob, dout, qkv, base = full
+    ranks = list(np.random.default_rng(20 + cp).permutation(cp))
+    assert_bitwise3(forward_and_backward(prob, dout, cp=cp, layout=1, ranks=ranks, qkv=qkv), base, f"CP={cp}")
+
+
+def test_backward_fullsize_repeat_bitwise(full):
+    prob, dout, qkv, base = full
+    assert_bitwise3(forward_and_backward(prob, dout, qkv=qkv), base, "repeat")
