@@ -102,8 +102,9 @@ struct BwdLayout {
   static constexpr int kResOff = 0;                 // resident pair (K_j,V_j) or (Q_i,dO_i)
   static constexpr int kStreamOff = 2 * kTile;      // 2 stages x streamed pair
   static constexpr int kStages = 2;
-  static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;  // [2][2][128] floats (lse, Delta)
-  static constexpr int kBarOff = kVecOff + 2 * 2 * 128 * 4;
+  // per-warp copies of a step's column statistics: [buf 2][warp 4][lse2, Delta][128] floats
+  static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;
+  static constexpr int kBarOff = kVecOff + 2 * 4 * 2 * 128 * 4;
   // barriers
   static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 7,
                        kAccFull = 8, kAccEmpty = 9, kNumBars = 10;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  float* vecs = reinterpret_cast<float*>(smem + L::kVecOff);  // [buf][lse2, delta][128]
+  float* vecs = reinterpret_cast<float*>(smem + L::kVecOff);  // [buf][warp][lse2, delta][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -333,18 +334,23 @@ __global__ void __launch_bounds__(384, 1)
       const int key_pos = (KIND == 0) ? it.block * 128 + r : 0;
       bool fail = false;
       for (int t = 0; t < nsteps; ++t) {
-        float* vb = vecs + (s_it & 1) * 256;
+        float* vb = vecs + ((s_it & 1) * 4 + (warp & 3)) * 256;
         int col0;  // position of column 0 of this step
         if (KIND == 0) {
           const int i = it.block + t / p.group;
           const int h = it.head * p.group + t % p.group;
           col0 = i * 128;
-          // column statistics of the step's query block, shared through smem
-          const int qp = col0 + r;
-          const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
-          vb[r] = qp < len ? __fmul_rn(p.lse_t[idx], kLog2e) : 0.f;
-          vb[128 + r] = qp < len ? p.delta_t[idx] : 0.f;
-          named_bar_sync(1, 128);
+          // column statistics of the step's query block: each warp stages its
+          // own copy (warp-local sync only)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = lane + 32 * u;
+            const int qp = col0 + col;
+            const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
+            vb[col] = qp < len ? __fmul_rn(p.lse_t[idx], kLog2e) : 0.f;
+            vb[128 + col] = qp < len ? p.delta_t[idx] : 0.f;
+          }
+          __syncwarp();
         } else {
           col0 = t * 128;
         }
