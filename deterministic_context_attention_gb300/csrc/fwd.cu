@@ -19,15 +19,18 @@
 // abs 0.0 across ranks).
 //
 // Warp roles (384 threads, three warpgroups):
-//   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r)
-//   warps 4-7  softmax: thread r owns TMEM lane r, writes P_hi/P_lo to TMEM
-//              over its scores (per 16-key MMA step: 8 columns hi, 8 lo)
-//   warp  8    TMA producer (Q tile, K/V blocks or pages)
+//   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r) and
+//              keeps the running O of its row in registers (240 per thread)
+//   warps 4-7  softmax: thread r owns TMEM lane r; reads S, writes P_hi/P_lo
+//              over it (per 16-key MMA step: 8 columns hi, then 8 lo)
+//   warp  8    TMA producer (Q tile; K and V blocks or pages, separate rings)
 //   warp  9    TMEM allocator and MMA issuer (also zeroes V rows past the
 //              valid length of a partial block)
-//   warps 10-11 idle (the block is sized in whole warpgroups, the unit in
-//              which registers are granted)
-// TMEM (512 columns): S/P double buffer [0,256), PV [256,384), O [384,512).
+//   warps 10-11 idle (registers are granted per warpgroup; warps 8-11 give
+//              theirs to warps 0-3)
+// TMEM (512 columns): S/P double buffer [0,256), PV double buffer [256,512).
+// Per block the tensor core runs S_{b+1} then PV_b, so the softmax of block
+// b+1 overlaps PV_b and the correction of block b overlaps both.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,24 +42,31 @@
 
 namespace rlk {
 
+// register split per warpgroup (launch: 168 per thread for 384 threads)
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsCorrection = 240;
+constexpr int kRegsProducer = 96;
+static_assert(kRegsCorrection + kRegsLaunch + kRegsProducer <= 3 * kRegsLaunch, "register split");
+
 template <int B>
 struct FwdLayout {
-  static constexpr int kStages = (B == 128) ? 2 : 4;
+  static constexpr int kSK = (B == 128) ? 3 : 4;         // K ring
+  static constexpr int kSV = (B == 128) ? 2 : 4;         // V ring
+  static constexpr int kStatsRing = 8;
   static constexpr int kQBytes = kTileRows * kHeadDim * 2;  // 32 KB, two 64-column halves
   static constexpr int kQHalf = kTileRows * 128;            // bytes of one half
   static constexpr int kKVHalf = B * 128;                   // bytes of one 64-column half
   static constexpr int kKVBytes = 2 * kKVHalf;              // K (or V) of one block
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQBytes;                    // stage s: K then V
-  static constexpr int kBarOff = kKVOff + kStages * 2 * kKVBytes;
-  // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 1, kKVFull = 2, kKVEmpty = 2 + kStages,
-                       kSFull = 2 + 2 * kStages, kPFull = kSFull + 2, kPVFull = kPFull + 2,
-                       kPVEmpty = kPVFull + 1, kStatsFull = kPVEmpty + 1,
-                       kNumBars = kStatsFull + 4;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + kSK * kKVBytes;
+  static constexpr int kBarOff = kVOff + kSV * kKVBytes;
+  static constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kSK, kVFull = kKEmpty + kSK,
+                       kVEmpty = kVFull + kSV, kSFull = kVEmpty + kSV, kPFull = kSFull + 2, kPVFull = kPFull + 2,
+                       kPVEmpty = kPVFull + 2, kStatsFull = kPVEmpty + 2, kNumBars = kStatsFull + kStatsRing;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;
-  static constexpr int kTotal = kStatsOff + 4 * kTileRows * 8;
+  static constexpr int kTotal = kStatsOff + kStatsRing * kTileRows * 8;
   static constexpr int kAlloc = kTotal + 1024;
 };
 
@@ -115,18 +125,53 @@ __device__ __forceinline__ int visible_keys(int pos, int kv_len, int b, int B) {
   return max(0, min(B, last - b * B + 1));
 }
 
+__device__ __forceinline__ void setmaxnreg_inc240() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 240;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec96() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+}
+
+// Probabilities of 32 keys (chunk c of the block) for one row: writes the
+// packed hi/lo words in MMA-step order and adds the keys to the canonical
+// partial sums.
+template <bool FIRST>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, int nvis, float scale_log2,
+                                              float neg_mc, bool has, float (&part)[32], uint32_t (&w)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const int key = 32 * c + e;
+    float p0 = prob(__uint_as_float(raw[e]), scale_log2, neg_mc);
+    float p1 = prob(__uint_as_float(raw[e + 1]), scale_log2, neg_mc);
+    p0 = (has && key < nvis) ? p0 : 0.0f;
+    p1 = (has && key + 1 < nvis) ? p1 : 0.0f;
+    if (FIRST) {
+      part[e] = p0;
+      part[e + 1] = p1;
+    } else {
+      part[e] = __fadd_rn(part[e], p0);
+      part[e + 1] = __fadd_rn(part[e + 1], p1);
+    }
+    uint32_t hi, lo;
+    split_pair(p0, p1, hi, lo);
+    const int slot = (e >> 4) * 16 + ((e & 15) >> 1);  // K-step e/16, word within it
+    w[slot] = hi;
+    w[slot + 8] = lo;
+  }
+}
+
 template <int B, int MODE>
 __global__ void __launch_bounds__(384, 1)
     rlk_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = FwdLayout<B>;
-  constexpr int S = L::kStages;
+  constexpr int SK = L::kSK, SV = L::kSV, SR = L::kStatsRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);  // [4][128]
+  float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);  // [ring][128]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -135,17 +180,21 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0) {
     mbar_init(&bars[L::kQFull], 1);
     mbar_init(&bars[L::kQEmpty], 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&bars[L::kKVFull + s], 1);
-      mbar_init(&bars[L::kKVEmpty + s], 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&bars[L::kKFull + s], 1);
+      mbar_init(&bars[L::kKEmpty + s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&bars[L::kVFull + s], 1);
+      mbar_init(&bars[L::kVEmpty + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[L::kSFull + s], 1);
       mbar_init(&bars[L::kPFull + s], 128);
+      mbar_init(&bars[L::kPVFull + s], 1);
+      mbar_init(&bars[L::kPVEmpty + s], 128);
     }
-    mbar_init(&bars[L::kPVFull], 1);
-    mbar_init(&bars[L::kPVEmpty], 128);
-    for (int s = 0; s < 4; ++s) mbar_init(&bars[L::kStatsFull + s], 128);
+    for (int s = 0; s < SR; ++s) mbar_init(&bars[L::kStatsFull + s], 128);
     *abort = 0;
     fence_mbar_init();
   }
@@ -158,166 +207,180 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem;          // S/P buffers: + 128 * buf
-  const uint32_t tm_pv = tmem + 256;
-  const uint32_t tm_o = tmem + 384;
+  const uint32_t tm_pv = tmem + 256;   // PV buffers: + 128 * buf
 
   const uint32_t q_addr = smem_u32(smem + L::kQOff);
-  uint8_t* kv_base = smem + L::kKVOff;
+  uint8_t* k_base = smem + L::kKOff;
+  uint8_t* v_base = smem + L::kVOff;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
-    uint32_t kv_it = 0, q_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-      const ItemInfo it = item_info<MODE>(p, item);
-      bool ok = mbar_wait(&bars[L::kQEmpty], (q_it & 1) ^ 1, abort, p.err, 0x101);
-      if (!__all_sync(0xffffffffu, ok)) break;
+  if (warp >= 8) {
+    setmaxnreg_dec96();
+    if (warp == 8) {
+      // ---------------------------------------------------------- producer
       if (lane == 0) {
-        if (MODE == kModeDecode) {
-          mbar_arrive_expect_tx(&bars[L::kQFull], p.group * kHeadDim * 2);
-          tma_load_3d(smem + L::kQOff, &tm_q, &bars[L::kQFull], 0, it.head * p.group, it.seq);
-          tma_load_3d(smem + L::kQOff + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head * p.group, it.seq);
-        } else {
-          mbar_arrive_expect_tx(&bars[L::kQFull], L::kQBytes);
-          const int row0 = it.q_tok0 + it.row_begin;
-          tma_load_3d(smem + L::kQOff, &tm_q, &bars[L::kQFull], 0, it.head, row0);
-          tma_load_3d(smem + L::kQOff + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head, row0);
-        }
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
       }
-      ++q_it;
-      const int g = (MODE == kModeDecode) ? it.head : it.head / p.group;
-      for (int j = 0; j < it.nb; ++j) {
-        const int b = it.blk0 + j;
-        const uint32_t stage = kv_it % S;
-        ok = mbar_wait(&bars[L::kKVEmpty + stage], ((kv_it / S) & 1) ^ 1, abort, p.err, 0x102);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        uint8_t* kd = kv_base + stage * 2 * L::kKVBytes;
-        uint8_t* vd = kd + L::kKVBytes;
+      uint32_t k_it = 0, v_it = 0, q_it = 0;
+      // load K (IS_V false) or V of block b into its ring slot; false on abort
+      auto load_kv = [&](const ItemInfo& it, int g, int b, bool is_v) -> bool {
+        const uint32_t idx = is_v ? v_it : k_it;
+        const int S = is_v ? SV : SK;
+        const uint32_t stage = idx % S;
+        uint64_t* empty = &bars[(is_v ? L::kVEmpty : L::kKEmpty) + stage];
+        uint64_t* full = &bars[(is_v ? L::kVFull : L::kKFull) + stage];
+        bool ok = mbar_wait(empty, ((idx / S) & 1) ^ 1, abort, p.err, is_v ? 0x103 : 0x102);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        uint8_t* dst = (is_v ? v_base : k_base) + stage * L::kKVBytes;
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         if (MODE != kModeDecode) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[L::kKVFull + stage], 2 * L::kKVBytes);
+            mbar_arrive_expect_tx(full, L::kKVBytes);
             const int r = it.k_tok0 + b * B;
-            tma_load_3d(kd, &tm_k, &bars[L::kKVFull + stage], 0, g, r);
-            tma_load_3d(kd + L::kKVHalf, &tm_k, &bars[L::kKVFull + stage], 64, g, r);
-            tma_load_3d(vd, &tm_v, &bars[L::kKVFull + stage], 0, g, r);
-            tma_load_3d(vd + L::kKVHalf, &tm_v, &bars[L::kKVFull + stage], 64, g, r);
+            tma_load_3d(dst, map, full, 0, g, r);
+            tma_load_3d(dst + L::kKVHalf, map, full, 64, g, r);
           }
         } else {
           const int ps = p.page_size;
           const int n_tok = min(B, it.kv_len - b * B);
           const int n_pg = (n_tok + ps - 1) / ps;
-          if (lane == 0) mbar_arrive_expect_tx(&bars[L::kKVFull + stage], n_pg * ps * 512);
+          if (lane == 0) mbar_arrive_expect_tx(full, n_pg * ps * 256);
           __syncwarp();
           if (lane < n_pg) {
             int32_t pe = p.page_table[static_cast<int64_t>(it.seq) * p.max_pages + b * (B / ps) + lane];
             if (pe < 0 || pe >= p.n_pages) {
-              report_error(p.err, kErrBadPage, 0x103);
+              report_error(p.err, kErrBadPage, 0x104);
               pe = p.n_pages;  // out of range: the copy reads the zero fill
             }
             const int r = pe * ps;
             const int off = lane * ps * 128;
-            tma_load_3d(kd + off, &tm_k, &bars[L::kKVFull + stage], 0, g, r);
-            tma_load_3d(kd + L::kKVHalf + off, &tm_k, &bars[L::kKVFull + stage], 64, g, r);
-            tma_load_3d(vd + off, &tm_v, &bars[L::kKVFull + stage], 0, g, r);
-            tma_load_3d(vd + L::kKVHalf + off, &tm_v, &bars[L::kKVFull + stage], 64, g, r);
+            tma_load_3d(dst + off, map, full, 0, g, r);
+            tma_load_3d(dst + L::kKVHalf + off, map, full, 64, g, r);
           }
         }
-        ++kv_it;
-      }
-      if (*abort) break;
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdescS = idesc_bf16(128, B, false, false);
-    constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, false, true);
-    uint32_t kv_it = 0, s_it = 0, pv_it = 0, q_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-      const ItemInfo it = item_info<MODE>(p, item);
-      bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x201);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ++q_it;
-      const uint32_t kvb = kv_it, sb0 = s_it;
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t kvi = kvb + j;
-        const uint32_t stage = kvi % S;
-        bool w = mbar_wait(&bars[L::kKVFull + stage], (kvi / S) & 1, abort, p.err, 0x202);
-        if (!__all_sync(0xffffffffu, w)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t k_addr = smem_u32(kv_base + stage * 2 * L::kKVBytes);
-          const uint32_t d = tm_s + ((sb0 + j) & 1) * 128;
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t half = k >> 2, sub = (k & 3) * 32;
-            const uint64_t ad = sdesc_sw128(q_addr + half * L::kQHalf + sub, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k_addr + half * L::kKVHalf + sub, 16, 1024);
-            umma_ss(d, ad, bd, kIdescS, k > 0 ? 1u : 0u);
-          }
-          umma_commit(&bars[L::kSFull + ((sb0 + j) & 1)]);
-        }
-        __syncwarp();
+        if (is_v) ++v_it; else ++k_it;
         return true;
       };
-      if (!issue_s(0)) break;
-      bool fail = false;
-      for (int j = 0; j < it.nb; ++j) {
-        if (j + 1 < it.nb) {
-          if (!issue_s(j + 1)) { fail = true; break; }
-        } else {
-          if (lane == 0) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
-          __syncwarp();
-        }
-        const uint32_t sidx = sb0 + j;
-        const uint32_t buf = sidx & 1;
-        bool w = mbar_wait(&bars[L::kPFull + buf], (sidx >> 1) & 1, abort, p.err, 0x203);
-        w = w && mbar_wait(&bars[L::kPVEmpty], (pv_it & 1) ^ 1, abort, p.err, 0x204);
-        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-        const uint32_t stage = (kvb + j) % S;
-        uint8_t* vd = kv_base + stage * 2 * L::kKVBytes + L::kKVBytes;
-        // V rows past the valid keys of a partial block may hold stale or
-        // non-finite data; P is exactly 0 there, so zero them (0 * NaN = NaN).
-        const int b = it.blk0 + j;
-        const int valid = min(B, it.kv_len - b * B);
-        if (valid < B) {
-          const int nrow = B - valid;
-          for (int i = lane; i < nrow * 16; i += 32) {
-            const int row = valid + (i >> 4);
-            const int part = i & 15;  // 16 B pieces: 8 per half-row, 2 halves
-            uint4* dst = reinterpret_cast<uint4*>(vd + (part >> 3) * L::kKVHalf + row * 128 + (part & 7) * 16);
-            *dst = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        tc_fence_after();
+      for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+        const ItemInfo it = item_info<MODE>(p, item);
+        bool ok = mbar_wait(&bars[L::kQEmpty], (q_it & 1) ^ 1, abort, p.err, 0x101);
+        if (!__all_sync(0xffffffffu, ok)) break;
         if (lane == 0) {
-          const uint32_t v_addr = smem_u32(vd);
-          const uint32_t a0 = tm_s + buf * 128;
-#pragma unroll
-          for (int k = 0; k < B / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
-            umma_ts(tm_pv, a0 + 16 * k, bd, kIdescPV, k > 0 ? 1u : 0u);
+          if (MODE == kModeDecode) {
+            mbar_arrive_expect_tx(&bars[L::kQFull], p.group * kHeadDim * 2);
+            tma_load_3d(smem + L::kQOff, &tm_q, &bars[L::kQFull], 0, it.head * p.group, it.seq);
+            tma_load_3d(smem + L::kQOff + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head * p.group, it.seq);
+          } else {
+            mbar_arrive_expect_tx(&bars[L::kQFull], L::kQBytes);
+            const int row0 = it.q_tok0 + it.row_begin;
+            tma_load_3d(smem + L::kQOff, &tm_q, &bars[L::kQFull], 0, it.head, row0);
+            tma_load_3d(smem + L::kQOff + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head, row0);
           }
-#pragma unroll
-          for (int k = 0; k < B / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
-            umma_ts(tm_pv, a0 + 16 * k + 8, bd, kIdescPV, 1u);
-          }
-          umma_commit(&bars[L::kPVFull]);
-          umma_commit(&bars[L::kKVEmpty + stage]);
         }
-        __syncwarp();
-        ++pv_it;
+        ++q_it;
+        const int g = (MODE == kModeDecode) ? it.head : it.head / p.group;
+        // consumption order: K_0, K_1, V_0, K_2, V_1, ...
+        bool fail = false;
+        for (int j = 0; j <= it.nb && !fail; ++j) {
+          if (j < it.nb && !load_kv(it, g, it.blk0 + j, false)) fail = true;
+          if (!fail && j >= 1 && !load_kv(it, g, it.blk0 + j - 1, true)) fail = true;
+        }
+        if (fail || *abort) break;
       }
-      if (fail) break;
-      kv_it += it.nb;
-      s_it += it.nb;
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdescS = idesc_bf16(128, B, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, false, true);
+      uint32_t k_it = 0, v_it = 0, s_it = 0, pv_it = 0, q_it = 0;
+      for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+        const ItemInfo it = item_info<MODE>(p, item);
+        bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x201);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        ++q_it;
+        const uint32_t kb = k_it, vb = v_it, sb = s_it, pb = pv_it;
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t ki = kb + j;
+          const uint32_t stage = ki % SK;
+          bool w = mbar_wait(&bars[L::kKFull + stage], (ki / SK) & 1, abort, p.err, 0x202);
+          if (!__all_sync(0xffffffffu, w)) return false;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t k_addr = smem_u32(k_base + stage * L::kKVBytes);
+            const uint32_t d = tm_s + ((sb + j) & 1) * 128;
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+              const uint32_t half = k >> 2, sub = (k & 3) * 32;
+              const uint64_t ad = sdesc_sw128(q_addr + half * L::kQHalf + sub, 16, 1024);
+              const uint64_t bd = sdesc_sw128(k_addr + half * L::kKVHalf + sub, 16, 1024);
+              umma_ss(d, ad, bd, kIdescS, k > 0 ? 1u : 0u);
+            }
+            umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
+            umma_commit(&bars[L::kKEmpty + stage]);
+          }
+          __syncwarp();
+          return true;
+        };
+        if (!issue_s(0)) break;
+        bool fail = false;
+        for (int j = 0; j < it.nb; ++j) {
+          if (j + 1 < it.nb) {
+            if (!issue_s(j + 1)) { fail = true; break; }
+          } else {
+            if (lane == 0) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
+            __syncwarp();
+          }
+          const uint32_t sidx = sb + j, buf = sidx & 1;
+          const uint32_t vi = vb + j, vstage = vi % SV;
+          const uint32_t pvi = pb + j, pvbuf = pvi & 1;
+          bool w = mbar_wait(&bars[L::kPFull + buf], (sidx >> 1) & 1, abort, p.err, 0x203);
+          w = w && mbar_wait(&bars[L::kVFull + vstage], (vi / SV) & 1, abort, p.err, 0x204);
+          w = w && mbar_wait(&bars[L::kPVEmpty + pvbuf], ((pvi >> 1) & 1) ^ 1, abort, p.err, 0x205);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          uint8_t* vd = v_base + vstage * L::kKVBytes;
+          // V rows past the valid keys of a partial block may hold stale or
+          // non-finite data; P is exactly 0 there, so zero them (0 * NaN = NaN).
+          const int b = it.blk0 + j;
+          const int valid = min(B, it.kv_len - b * B);
+          if (valid < B) {
+            const int nrow = B - valid;
+            for (int i = lane; i < nrow * 16; i += 32) {
+              const int row = valid + (i >> 4);
+              const int part = i & 15;  // 16 B pieces: 8 per half-row, 2 halves
+              uint4* dst = reinterpret_cast<uint4*>(vd + (part >> 3) * L::kKVHalf + row * 128 + (part & 7) * 16);
+              *dst = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t v_addr = smem_u32(vd);
+            const uint32_t a0 = tm_s + buf * 128;
+            const uint32_t d = tm_pv + pvbuf * 128;
+#pragma unroll
+            for (int k = 0; k < B / 16; ++k) {
+              const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
+              umma_ts(d, a0 + 16 * k, bd, kIdescPV, k > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < B / 16; ++k) {
+              const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
+              umma_ts(d, a0 + 16 * k + 8, bd, kIdescPV, 1u);
+            }
+            umma_commit(&bars[L::kPVFull + pvbuf]);
+            umma_commit(&bars[L::kVEmpty + vstage]);
+          }
+          __syncwarp();
+        }
+        if (fail) break;
+        k_it += it.nb;
+        v_it += it.nb;
+        s_it += it.nb;
+        pv_it += it.nb;
+      }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int r = tid - 128;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -325,6 +388,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
       const ItemInfo it = item_info<MODE>(p, item);
       const bool valid = r < it.row_count;
+      // a warp none of whose rows is written (decode: all but the first)
+      // only takes part in the barriers
+      const bool warp_rows = __any_sync(0xffffffffu, valid);
       const int pos = (MODE == kModeDecode) ? it.kv_len - 1 : it.kv_len - it.q_len + it.row_begin + r;
       bool fail = false;
       for (int j = 0; j < it.nb; ++j) {
@@ -335,155 +401,194 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const uint32_t ta = tm_s + lane_off + buf * 128;
         const int nvis = valid ? visible_keys(pos, it.kv_len, b, B) : 0;
-        // pass 1: row max over the visible keys
-        float m = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < B / 32; ++c) {
-          uint32_t raw[32];
-          tmem_ld32(ta + 32 * c, raw);
-          tmem_ld_wait(raw);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            m = fmaxf(m, scaled_score(__uint_as_float(raw[e]), 32 * c + e, nvis, p.scale_log2));
-        }
-        // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo.  The
-        // words of keys 16k..16k+15 go to columns 16k..16k+15 (8 hi, then 8 lo),
-        // the columns their scores came from.
-        float part[32];
         const bool has = nvis > 0;
-#pragma unroll
-        for (int c = 0; c < B / 32; ++c) {
-          uint32_t raw[32];
-          tmem_ld32(ta + 32 * c, raw);
-          tmem_ld_wait(raw);
-          uint32_t w[32];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int key = 32 * c + e;
-            float p0 = prob(scaled_score(__uint_as_float(raw[e]), key, nvis, p.scale_log2), m);
-            float p1 = prob(scaled_score(__uint_as_float(raw[e + 1]), key + 1, nvis, p.scale_log2), m);
-            if (!has) { p0 = 0.0f; p1 = 0.0f; }
-            partial_add(part, key, p0);
-            partial_add(part, key + 1, p1);
-            uint32_t hi, lo;
-            split_pair(p0, p1, hi, lo);
-            const int slot = (e >> 4) * 16 + ((e & 15) >> 1);  // K-step (e/16), word within it
-            w[slot] = hi;
-            w[slot + 8] = lo;
-          }
-          tmem_st32(ta + 32 * c, w);
-        }
         float lse_b = -INFINITY, rcp = 0.0f;
-        if (has) block_stats(m, partial_tree(part), lse_b, rcp);
+        if (warp_rows) {
+        // pass 1: maximum raw score over the visible keys
+        float m = -INFINITY;
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(ta, r0);
+          if (B > 32) tmem_ld32(ta + 32, r1);
+          tmem_ld_wait(r0);
+          if (B > 32) tmem_ld_wait(r1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            m = fmaxf(m, e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
+            if (B > 32) m = fmaxf(m, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
+          }
+          if (B > 64) {
+            tmem_ld32(ta + 64, r0);
+            tmem_ld32(ta + 96, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              m = fmaxf(m, 64 + e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
+              m = fmaxf(m, 96 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
+            }
+          }
+        }
+        const float mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
+        const float neg_mc = -mc;
+        // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo over S
+        float part[32];
+        {
+          uint32_t cur[32], nxt[32], wv[32];
+          tmem_ld32(ta, cur);
+          tmem_ld_wait(cur);
+          tmem_ld32(ta + 32, nxt);
+          softmax_chunk<true>(cur, 0, nvis, p.scale_log2, neg_mc, has, part, wv);
+          tmem_st32(ta, wv);
+          tmem_ld_wait(nxt);
+          if (B > 64) tmem_ld32(ta + 64, cur);
+          softmax_chunk<false>(nxt, 1, nvis, p.scale_log2, neg_mc, has, part, wv);
+          tmem_st32(ta + 32, wv);
+          if (B > 64) {
+            tmem_ld_wait(cur);
+            tmem_ld32(ta + 96, nxt);
+            softmax_chunk<false>(cur, 2, nvis, p.scale_log2, neg_mc, has, part, wv);
+            tmem_st32(ta + 64, wv);
+            tmem_ld_wait(nxt);
+            softmax_chunk<false>(nxt, 3, nvis, p.scale_log2, neg_mc, has, part, wv);
+            tmem_st32(ta + 96, wv);
+          }
+        }
+        if (has) block_stats(mc, partial_tree(part), lse_b, rcp);
+        }  // warp_rows
         tmem_st_wait();
         tc_fence_before();
-        stats[(st_it & 3) * kTileRows + r] = make_float2(lse_b, rcp);
+        stats[(st_it % SR) * kTileRows + r] = make_float2(lse_b, rcp);
         mbar_arrive(&bars[L::kPFull + buf]);
-        mbar_arrive(&bars[L::kStatsFull + (st_it & 3)]);
+        mbar_arrive(&bars[L::kStatsFull + (st_it % SR)]);
         ++s_it;
         ++st_it;
       }
       if (fail) break;
     }
-  } else if (warp < 4) {
+  } else {
     // ------------------------------------------------------------ correction / epilogue
+    setmaxnreg_inc240();
     const int r = tid;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t pv_it = 0, st_it = 0;
+    float O[kHeadDim];
+#pragma unroll
+    for (int e = 0; e < kHeadDim; ++e) O[e] = 0.0f;
     for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
       const ItemInfo it = item_info<MODE>(p, item);
       const bool valid = r < it.row_count;
+      const bool warp_rows = __any_sync(0xffffffffu, valid);
       float Lrun = -INFINITY;
       bool fail = false;
       for (int j = 0; j < it.nb; ++j) {
-        bool w = mbar_wait(&bars[L::kPVFull], pv_it & 1, abort, p.err, 0x401);
-        w = w && mbar_wait(&bars[L::kStatsFull + (st_it & 3)], (st_it >> 2) & 1, abort, p.err, 0x402);
+        const uint32_t buf = pv_it & 1;
+        bool w = mbar_wait(&bars[L::kPVFull + buf], (pv_it >> 1) & 1, abort, p.err, 0x401);
+        w = w && mbar_wait(&bars[L::kStatsFull + (st_it % SR)], (st_it / SR) & 1, abort, p.err, 0x402);
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
-        const float2 st = stats[(st_it & 3) * kTileRows + r];
+        const uint32_t ta = tm_pv + lane_off + buf * 128;
+        const float2 st = stats[(st_it % SR) * kTileRows + r];
         const float lse_b = st.x, rcp = st.y;
         const bool has = valid && (lse_b != -INFINITY);
-        if (MODE == kModeStates) {
+        uint32_t x0[32], x1[32];
+        if (!warp_rows) {
+          tc_fence_before();
+          mbar_arrive(&bars[L::kPVEmpty + buf]);
+        } else if (MODE == kModeStates) {
+          tmem_ld32(ta, x0);
+          tmem_ld32(ta + 32, x1);
           const int64_t pair = it.slab_off + static_cast<int64_t>(it.head) * it.slab_rc +
                                (it.row_begin + r - it.slab_rb);
           float4* dst = reinterpret_cast<float4*>(p.state_o + pair * kHeadDim);
+          tmem_ld_wait(x0);
+          tmem_ld_wait(x1);
+          if (has) {
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 32; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tm_pv + lane_off + 32 * c, x);
-            tmem_ld_wait(x);
-            if (has) {
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                dst[(32 * c + e) / 4] = make_float4(state_elem(__uint_as_float(x[e]), rcp),
-                                                    state_elem(__uint_as_float(x[e + 1]), rcp),
-                                                    state_elem(__uint_as_float(x[e + 2]), rcp),
-                                                    state_elem(__uint_as_float(x[e + 3]), rcp));
+            for (int e = 0; e < 32; e += 4) {
+              dst[e / 4] = make_float4(state_elem(__uint_as_float(x0[e]), rcp), state_elem(__uint_as_float(x0[e + 1]), rcp),
+                                       state_elem(__uint_as_float(x0[e + 2]), rcp), state_elem(__uint_as_float(x0[e + 3]), rcp));
+              dst[8 + e / 4] = make_float4(state_elem(__uint_as_float(x1[e]), rcp), state_elem(__uint_as_float(x1[e + 1]), rcp),
+                                           state_elem(__uint_as_float(x1[e + 2]), rcp), state_elem(__uint_as_float(x1[e + 3]), rcp));
             }
           }
-          if (has) p.state_lse[pair] = lse_b;
+          tmem_ld32(ta + 64, x0);
+          tmem_ld32(ta + 96, x1);
+          tmem_ld_wait(x0);
+          tmem_ld_wait(x1);
+          tc_fence_before();
+          mbar_arrive(&bars[L::kPVEmpty + buf]);  // PV read: the buffer is free
+          if (has) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              dst[16 + e / 4] = make_float4(state_elem(__uint_as_float(x0[e]), rcp), state_elem(__uint_as_float(x0[e + 1]), rcp),
+                                            state_elem(__uint_as_float(x0[e + 2]), rcp), state_elem(__uint_as_float(x0[e + 3]), rcp));
+              dst[24 + e / 4] = make_float4(state_elem(__uint_as_float(x1[e]), rcp), state_elem(__uint_as_float(x1[e + 1]), rcp),
+                                            state_elem(__uint_as_float(x1[e + 2]), rcp), state_elem(__uint_as_float(x1[e + 3]), rcp));
+            }
+            p.state_lse[pair] = lse_b;
+          }
         } else {
+          tmem_ld32(ta, x0);
+          tmem_ld32(ta + 32, x1);
           float Lp = 0.f, alpha = 0.f, beta = 0.f;
-          if (j > 0 && has) fold_coeffs(Lrun, lse_b, Lp, alpha, beta);
+          if (j > 0 && has) fold_coeffs(Lrun, lse_b, Lp, alpha, beta);  // overlaps the PV loads
+          tmem_ld_wait(x0);
+          tmem_ld_wait(x1);
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 32; ++c) {
-            uint32_t x[32], y[32];
-            tmem_ld32(tm_pv + lane_off + 32 * c, x);
-            tmem_ld_wait(x);
-            if (j > 0) {
-              tmem_ld32(tm_o + lane_off + 32 * c, y);
-              tmem_ld_wait(y);
+          for (int e = 0; e < 32; ++e) {
+            const float o0 = state_elem(__uint_as_float(x0[e]), rcp);
+            const float o1 = state_elem(__uint_as_float(x1[e]), rcp);
+            if (j == 0) {
+              O[e] = o0;
+              O[32 + e] = o1;
+            } else if (has) {
+              O[e] = fold_elem(O[e], o0, alpha, beta);
+              O[32 + e] = fold_elem(O[32 + e], o1, alpha, beta);
             }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float o = state_elem(__uint_as_float(x[e]), rcp);
-              if (j == 0) {
-                y[e] = __float_as_uint(o);
-              } else if (has) {
-                y[e] = __float_as_uint(fold_elem(__uint_as_float(y[e]), o, alpha, beta));
-              }
-            }
-            tmem_st32(tm_o + lane_off + 32 * c, y);
           }
-          tmem_st_wait();
+          tmem_ld32(ta + 64, x0);
+          tmem_ld32(ta + 96, x1);
+          tmem_ld_wait(x0);
+          tmem_ld_wait(x1);
+          tc_fence_before();
+          mbar_arrive(&bars[L::kPVEmpty + buf]);  // PV read: the buffer is free
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float o0 = state_elem(__uint_as_float(x0[e]), rcp);
+            const float o1 = state_elem(__uint_as_float(x1[e]), rcp);
+            if (j == 0) {
+              O[64 + e] = o0;
+              O[96 + e] = o1;
+            } else if (has) {
+              O[64 + e] = fold_elem(O[64 + e], o0, alpha, beta);
+              O[96 + e] = fold_elem(O[96 + e], o1, alpha, beta);
+            }
+          }
           if (has) Lrun = (j == 0) ? lse_b : Lp;
         }
-        tc_fence_before();
-        mbar_arrive(&bars[L::kPVEmpty]);
         ++pv_it;
         ++st_it;
       }
       if (fail) break;
-      if (MODE != kModeStates) {
+      if (MODE != kModeStates && valid) {
         // epilogue: O and L are final; write FP32 / BF16 rows and lse
         int64_t row_idx;
         if (MODE == kModeDecode) row_idx = static_cast<int64_t>(it.seq) * p.hq + it.head * p.group + r;
         else row_idx = static_cast<int64_t>(it.q_tok0 + it.row_begin + r) * p.hq + it.head;
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(p.out_f32 + row_idx * kHeadDim);
 #pragma unroll
-        for (int c = 0; c < kHeadDim / 32; ++c) {
-          uint32_t y[32];
-          tmem_ld32(tm_o + lane_off + 32 * c, y);
-          tmem_ld_wait(y);
-          if (valid) {
-            if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(p.out_f32 + row_idx * kHeadDim + 32 * c);
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                dst[e / 4] = make_float4(__uint_as_float(y[e]), __uint_as_float(y[e + 1]),
-                                         __uint_as_float(y[e + 2]), __uint_as_float(y[e + 3]));
-            }
-            if (p.out_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row_idx * kHeadDim + 32 * c);
-#pragma unroll
-              for (int e = 0; e < 32; e += 8)
-                dst[e / 8] = make_uint4(pack_bf16x2(__uint_as_float(y[e]), __uint_as_float(y[e + 1])),
-                                        pack_bf16x2(__uint_as_float(y[e + 2]), __uint_as_float(y[e + 3])),
-                                        pack_bf16x2(__uint_as_float(y[e + 4]), __uint_as_float(y[e + 5])),
-                                        pack_bf16x2(__uint_as_float(y[e + 6]), __uint_as_float(y[e + 7])));
-            }
-          }
+          for (int e = 0; e < kHeadDim; e += 4) dst[e / 4] = make_float4(O[e], O[e + 1], O[e + 2], O[e + 3]);
         }
-        if (valid && p.lse) p.lse[row_idx] = Lrun;
+        if (p.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row_idx * kHeadDim);
+#pragma unroll
+          for (int e = 0; e < kHeadDim; e += 8)
+            dst[e / 8] = make_uint4(pack_bf16x2(O[e], O[e + 1]), pack_bf16x2(O[e + 2], O[e + 3]),
+                                    pack_bf16x2(O[e + 4], O[e + 5]), pack_bf16x2(O[e + 6], O[e + 7]));
+        }
+        if (p.lse) p.lse[row_idx] = Lrun;
       }
     }
   }
@@ -509,17 +614,24 @@ static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const
                                 const CUtensorMap& tv, int grid, cudaStream_t stream) {
   using L = FwdLayout<B>;
   auto kern = rlk_fwd_kernel<B, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, 384, L::kAlloc, stream>>>(p, tq, tk, tv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) {
+  static bool checked = false;
+  if (!checked) {
+    // The warpgroup register split (240 / 168 / 96) needs the launch to grant
+    // 168 registers per thread; with fewer, setmaxnreg.inc would wait forever.
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, kern) == cudaSuccess)
-      fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers, max %d threads/block, %zu B dynamic smem\n", B, MODE,
-              a.numRegs, a.maxThreadsPerBlock, static_cast<size_t>(L::kAlloc));
+    cudaError_t e = cudaFuncGetAttributes(&a, kern);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs < kRegsLaunch) {
+      fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers at launch, the warpgroup split needs %d\n", B, MODE,
+              a.numRegs, kRegsLaunch);
+      return cudaErrorInvalidConfiguration;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    checked = true;
   }
-  return e;
+  kern<<<grid, 384, L::kAlloc, stream>>>(p, tq, tk, tv);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,

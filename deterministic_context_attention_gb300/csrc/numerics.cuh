@@ -37,21 +37,22 @@ __device__ __forceinline__ float bf16_lo_as_f32(uint32_t w) { return __uint_as_f
 __device__ __forceinline__ float bf16_hi_as_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Block softmax of one row, in the canonical order every kernel follows.
-//   x_c = S_c * scale_log2 for visible keys, -inf for the others
-//   m   = max_c x_c                              (log2 domain)
-//   p_c = 2^(x_c - m)
+//   m   = max of the raw scores S_c over the visible keys
+//   mc  = m * scale_log2                     (one rounding; log2 domain)
+//   p_c = 2^fma(S_c, scale_log2, -mc)        for visible keys, 0 otherwise
 //   l   = canonical row sum of p (below)
-//   lse_b = m ln2 + ln l  (natural log),  rcp = 1/l (IEEE-rounded)
+//   lse_b = fma(mc, ln2, ln l)  (natural log),  rcp = 1/l (IEEE-rounded)
 // A row with no visible key has no state: p = 0, lse_b = -inf.
+// (scale_log2 > 0, so the maximum of the raw scores scaled once is also the
+// maximum of the scaled scores.)
 //
 // Canonical row sum: key c goes to partial c mod 32, the keys of a partial
 // added in ascending order; the 32 partials are then combined by the fixed
 // tree a[t] <- a[t] + a[t + off] for off = 16, 8, 4, 2, 1 -- the association a
 // 32-lane xor butterfly produces, so a warp-per-row kernel reproduces it.
-__device__ __forceinline__ float scaled_score(float s, int c, int n_visible, float scale_log2) {
-  return (c < n_visible) ? __fmul_rn(s, scale_log2) : -INFINITY;
+__device__ __forceinline__ float prob(float s, float scale_log2, float neg_mc) {
+  return ex2_hw(__fmaf_rn(s, scale_log2, neg_mc));
 }
-__device__ __forceinline__ float prob(float x, float m) { return ex2_hw(__fsub_rn(x, m)); }
 // add probability p of key c (keys visited in ascending order) to partials a
 __device__ __forceinline__ void partial_add(float (&a)[32], int c, float p) {
   if (c < 32) a[c & 31] = p;
@@ -65,8 +66,8 @@ __device__ __forceinline__ float partial_tree(float (&a)[32]) {
   }
   return a[0];
 }
-__device__ __forceinline__ void block_stats(float m, float l, float& lse_b, float& rcp) {
-  lse_b = __fmaf_rn(m, kLn2f, logf(l));
+__device__ __forceinline__ void block_stats(float mc, float l, float& lse_b, float& rcp) {
+  lse_b = __fmaf_rn(mc, kLn2f, logf(l));
   rcp = __frcp_rn(l);
 }
 
