@@ -129,6 +129,18 @@ def time_steps(torch, fn, steps, warmup, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def max_over_ranks(value, dist):
+    """Largest value over the ranks of the default process group (the value
+    itself without one).  The tensor lives where the backend wants it."""
+    if dist is None or not dist.is_initialized():
+        return float(value)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args):
     import torch
     import deterministic_context_attention_gb300 as rlk
@@ -174,11 +186,7 @@ def run_gpu(args):
     wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     rlk.rlk_attn_check_device_error(stream)
-    ms = float(np.mean(times))
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(times)), dist)
     value = world * flops / (ms * 1e-3) / 1e12
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -493,7 +501,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--reference-rows", type=int, default=48)
+    ap.add_argument("--reference-rows", type=int, default=512)
     ap.add_argument("--profile", default=None, choices=["prefill", "states", "merge", "decode", "backward"])
     ap.add_argument("--profile-iters", type=int, default=3)
     args = ap.parse_args()
