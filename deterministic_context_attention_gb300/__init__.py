@@ -8,7 +8,8 @@ calls raise.
 
 Entry points (same names as the C ABI):
     rlk_attn_plan_states, rlk_attn_block_manifest_hash,
-    rlk_attn_prefill_states, rlk_attn_merge_states, rlk_attn_prefill,
+    rlk_attn_prefill_states, rlk_attn_merge_states, rlk_attn_merge_states_noalloc,
+    rlk_attn_prefill,
     rlk_attn_decode_paged, rlk_attn_backward, rlk_attn_workspace_size,
     rlk_attn_check_device_error, rlk_attn_last_error, rlk_attn_core_id
 """
@@ -85,6 +86,7 @@ def load():
             "rlk_attn_block_manifest_hash": [PP, P, P, P],
             "rlk_attn_prefill_states": [PP, P, P, P, P, P, i32, i64, P, P, P],
             "rlk_attn_merge_states": [PP, P, P, P, i64, P, P, P, P, P, P, sz, P],
+            "rlk_attn_merge_states_noalloc": [PP, P, P, P, i64, P, P, P, P, P, P],
             "rlk_attn_prefill": [PP, P, P, P, P, P, i32, P, P, P, P],
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
@@ -189,6 +191,18 @@ def rlk_attn_merge_states(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, st
                                         _ptr(state_o), _ptr(state_lse), _ptr(out_f32), _ptr(out_bf16),
                                         _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "rlk_attn_merge_states")
+
+
+def rlk_attn_merge_states_noalloc(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, state_o, state_lse,
+                                  out_f32, out_bf16, lse, stream=None):
+    """rlk_attn_merge_states for callers that cannot allocate: the index
+    scratch is the library's own device array (see the C header for its
+    limit and for the rule that overlapping calls race)."""
+    cq, ck = _i32_host(cu_seqlens_q), _i32_host(cu_seqlens_k)
+    _check(load().rlk_attn_merge_states_noalloc(ctypes.byref(params), _ptr(cq), _ptr(ck), _ptr(slabs),
+                                                int(n_slabs), _ptr(state_o), _ptr(state_lse), _ptr(out_f32),
+                                                _ptr(out_bf16), _ptr(lse), _stream(stream)),
+           "rlk_attn_merge_states_noalloc")
 
 
 def rlk_attn_prefill(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank, out_f32, out_bf16, lse,

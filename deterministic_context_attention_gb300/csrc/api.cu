@@ -22,6 +22,7 @@ namespace rlk {
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream);
+cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
 rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
                         const float* out_f32, const void* dout, const float* lse,
                         const int32_t* cu, int32_t cp_rank, float* dq, float* dk, float* dv,
@@ -552,6 +553,64 @@ rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* c
     mp->cu_k[s] = cu_seqlens_k[s];
   }
   cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// Same merge as rlk_attn_merge_states, for callers that cannot allocate:
+// the index scratch is the library's own file-scope device array.
+rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                         const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
+                                         int64_t n_slabs, const float* state_o, const float* state_lse,
+                                         float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
+  if (n_slabs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "bad state table");
+  if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if ((out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) || (state_o && !aligned16(state_o)) ||
+      (slabs && !aligned16(slabs)))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  int max_blocks = 1;
+  for (int s = 0; s < params->num_seqs; ++s)
+    max_blocks = std::max(max_blocks, (cu_seqlens_k[s + 1] - cu_seqlens_k[s] + params->kv_block_size - 1) /
+                                          params->kv_block_size);
+  // size limit first: nothing touches the device for a problem the scratch cannot hold
+  if (static_cast<int64_t>(params->num_seqs) * max_blocks > rlk::kNoAllocIndexEntries)
+    return fail(RLK_ERR_UNSUPPORTED,
+                "no-alloc merge: num_seqs * max KV blocks per sequence = %lld exceeds the %lld-entry scratch",
+                static_cast<long long>(params->num_seqs) * max_blocks,
+                static_cast<long long>(rlk::kNoAllocIndexEntries));
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  int32_t* scratch = nullptr;
+  int64_t entries = 0;
+  cudaError_t e = rlk::merge_noalloc_scratch(&scratch, &entries);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "scratch address: %s", cudaGetErrorString(e));
+  const int64_t total_rows = cu_seqlens_q[params->num_seqs];
+  if (total_rows == 0) return ok();
+  auto mp = std::make_unique<rlk::MergeParams>();
+  std::memset(mp.get(), 0, sizeof(*mp));
+  mp->err = dev->err;
+  mp->num_seqs = params->num_seqs;
+  mp->hq = params->num_q_heads;
+  mp->block = params->kv_block_size;
+  mp->max_blocks = max_blocks;
+  mp->total_rows = total_rows;
+  mp->n_slabs = n_slabs;
+  mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
+  mp->state_o = state_o;
+  mp->state_lse = state_lse;
+  mp->index = scratch;
+  mp->out_f32 = out_f32;
+  mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  mp->lse = lse;
+  for (int s = 0; s <= params->num_seqs; ++s) {
+    mp->cu_q[s] = cu_seqlens_q[s];
+    mp->cu_k[s] = cu_seqlens_k[s];
+  }
+  e = rlk::launch_merge(*mp, dev->num_sms, stream);
   if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
   return ok();
 }

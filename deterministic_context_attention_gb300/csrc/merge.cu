@@ -150,3 +150,34 @@ cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream)
 }
 
 }  // namespace rlk
+
+// ---------------------------------------------------------------- no-alloc variant
+// Scratch for callers that cannot allocate device memory: the merge's
+// (sequence, block) -> slab index lives in this file-scope array instead of a
+// caller-supplied workspace.  Every GPU that loads the library holds it until
+// the process exits.
+namespace rlk {
+
+static __device__ __align__(256) int32_t g_merge_index_scratch[kNoAllocIndexEntries];
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  (In host code the array's name is
+// only a host-side stand-in; the kernels must receive this address.)
+cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries) {
+  static int32_t* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_merge_index_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<int32_t*>(a);
+  }
+  *ptr = addr[dev];
+  *entries = kNoAllocIndexEntries;
+  return cudaSuccess;
+}
+
+}  // namespace rlk

@@ -221,6 +221,30 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
                              float* dq, float* dk, float* dv, void* workspace,
                              size_t workspace_bytes, rlk_stream_t stream);
 
+/*
+ * rlk_attn_merge_states without a workspace, for callers that cannot
+ * allocate device memory -- for instance code that runs inside a CUDA graph
+ * being captured, under an allocator that must not grow, or behind an API
+ * that hands out only its input and output buffers.  The pages have no
+ * counterpart: this is a convenience of this library.
+ *   Arguments, results and device errors are those of rlk_attn_merge_states;
+ *   the caller still passes the state table and the outputs.
+ *   Scratch: the (sequence, block) index lives in a file-scope device array
+ *   of 65,536 int32 entries (256 KB) that every GPU loading the library
+ *   holds until the process exits.  num_seqs times the largest number of KV
+ *   blocks of a sequence must not exceed 65,536; larger problems return
+ *   RLK_ERR_UNSUPPORTED with a message.  Nothing is allocated or freed.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call reuses the same array and initialises it itself, so calls in
+ *   sequence are independent, but calls that overlap on the GPU (different
+ *   streams, or different host threads on one device) race on it.
+ */
+rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
+                                         const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
+                                         int64_t n_slabs, const float* state_o, const float* state_lse,
+                                         float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream);
+
 enum { RLK_OP_MERGE = 1, RLK_OP_BACKWARD = 2 };
 
 /* Workspace bytes an entry point needs (HOST cu_seqlens; 0 on bad input). */

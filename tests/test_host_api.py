@@ -137,3 +137,15 @@ def test_workspace_sizes(lib):
     with pytest.raises(rlk.RlkError) as e:
         rlk.rlk_attn_merge_states(p, cu, cu, 16, 1, 16, 16, 16, None, 16, 16, 8, stream=0)
     assert e.value.status == 3
+
+
+def test_noalloc_merge_rejects_oversized_problem_before_any_device_work(lib):
+    # 128 sequences of 262,144 keys: 128 * 2048 blocks is 4x the 65,536-entry
+    # scratch; the entry point must refuse before it touches the device (the
+    # pointers below are placeholders that are never dereferenced)
+    cu = synth.cu_seqlens([262144] * 128)
+    p = rlk.make_params(128)
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_merge_states_noalloc(p, cu, cu, 16, 1, 16, 16, 16, None, 16, stream=0)
+    assert e.value.status == 2
+    assert "scratch" in rlk.rlk_attn_last_error()
