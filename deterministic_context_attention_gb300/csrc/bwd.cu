@@ -187,7 +187,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     uint32_t res_it = 0, st_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
+      const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
+      if (item >= p.num_items) continue;
       const BwdItem it = p.items[item];
       int len, nsteps;
       item_steps(it, len, nsteps);
@@ -245,7 +248,10 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t kIdK = idesc_bf16(128, 128, false, false);  // both operands K-major
     constexpr uint32_t kIdMN = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
     uint32_t res_it = 0, st_it = 0, s_it = 0, acc_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
+      const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
+      if (item >= p.num_items) continue;
       const BwdItem it = p.items[item];
       int len, nsteps;
       item_steps(it, len, nsteps);
@@ -313,7 +319,10 @@ __global__ void __launch_bounds__(384, 1)
     const int r = tid - 128;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t s_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
+      const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
+      if (item >= p.num_items) continue;
       const BwdItem it = p.items[item];
       int len, nsteps;
       item_steps(it, len, nsteps);
@@ -411,7 +420,10 @@ __global__ void __launch_bounds__(384, 1)
     const int r = tid;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t acc_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
+      const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
+      if (item >= p.num_items) continue;
       const BwdItem it = p.items[item];
       int len, nsteps;
       item_steps(it, len, nsteps);

@@ -20,14 +20,14 @@
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r) and
-//              keeps the running O of its row in registers (240 per thread)
+//              keeps the running O of its row in registers (216 per thread)
 //   warps 4-7  softmax: thread r owns TMEM lane r; reads S, writes P_hi/P_lo
 //              over it (per 16-key MMA step: 8 columns hi, then 8 lo)
 //   warp  8    TMA producer (Q tile; K and V blocks or pages, separate rings)
 //   warp  9    TMEM allocator and MMA issuer (also zeroes V rows past the
 //              valid length of a partial block)
-//   warps 10-11 idle (registers are granted per warpgroup; warps 8-11 give
-//              theirs to warps 0-3)
+//   warps 10-11 idle (registers are granted per warpgroup: warps 8-11 run
+//              with 96, warps 4-7 with 192, warps 0-3 with 216)
 // TMEM (512 columns): S/P double buffer [0,256), PV double buffer [256,512).
 // Per block the tensor core runs S_{b+1} then PV_b, so the softmax of block
 // b+1 overlaps PV_b and the correction of block b overlaps both.
@@ -44,9 +44,10 @@ namespace rlk {
 
 // register split per warpgroup (launch: 168 per thread for 384 threads)
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsCorrection = 240;
+constexpr int kRegsCorrection = 216;
+constexpr int kRegsSoftmax = 192;
 constexpr int kRegsProducer = 96;
-static_assert(kRegsCorrection + kRegsLaunch + kRegsProducer <= 3 * kRegsLaunch, "register split");
+static_assert(kRegsCorrection + kRegsSoftmax + kRegsProducer <= 3 * kRegsLaunch, "register split");
 
 template <int B>
 struct FwdLayout {
@@ -66,7 +67,9 @@ struct FwdLayout {
                        kPVEmpty = kPVFull + 2, kStatsFull = kPVEmpty + 2, kNumBars = kStatsFull + kStatsRing;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;
-  static constexpr int kTotal = kStatsOff + kStatsRing * kTileRows * 8;
+  static constexpr int kPageWin = 1024;  // decode: page ids cached per window
+  static constexpr int kPageOff = kStatsOff + kStatsRing * kTileRows * 8;
+  static constexpr int kTotal = kPageOff + 2 * kPageWin * 4;
   static constexpr int kAlloc = kTotal + 1024;
 };
 
@@ -119,14 +122,25 @@ __device__ __forceinline__ ItemInfo item_info(const FwdParams& p, int item) {
   return it;
 }
 
+// Item of this CTA in round k of the static schedule: CTAs take one item per
+// round from the longest-first list, in ascending CTA order on even rounds
+// and descending on odd ones, which evens out the per-CTA work.
+__device__ __forceinline__ int snake_item(int round) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return round * g + ((round & 1) ? g - 1 - c : c);
+}
+
 // Keys of block b visible to a row at key position pos (prefix of the block).
 __device__ __forceinline__ int visible_keys(int pos, int kv_len, int b, int B) {
   const int last = min(pos, kv_len - 1);
   return max(0, min(B, last - b * B + 1));
 }
 
-__device__ __forceinline__ void setmaxnreg_inc240() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 240;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_inc216() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_inc192() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
 }
 __device__ __forceinline__ void setmaxnreg_dec96() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
@@ -134,8 +148,7 @@ __device__ __forceinline__ void setmaxnreg_dec96() {
 
 // Probabilities of 32 keys (chunk c of the block) for one row: writes the
 // packed hi/lo words in MMA-step order and adds the keys to the canonical
-// partial sums.
-template <bool FIRST>
+// partial sums (which start at +0).
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, int nvis, float scale_log2,
                                               float neg_mc, bool has, float (&part)[32], uint32_t (&w)[32]) {
 #pragma unroll
@@ -145,13 +158,8 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, 
     float p1 = prob(__uint_as_float(raw[e + 1]), scale_log2, neg_mc);
     p0 = (has && key < nvis) ? p0 : 0.0f;
     p1 = (has && key + 1 < nvis) ? p1 : 0.0f;
-    if (FIRST) {
-      part[e] = p0;
-      part[e + 1] = p1;
-    } else {
-      part[e] = __fadd_rn(part[e], p0);
-      part[e + 1] = __fadd_rn(part[e + 1], p1);
-    }
+    part[e] = __fadd_rn(part[e], p0);
+    part[e + 1] = __fadd_rn(part[e + 1], p1);
     uint32_t hi, lo;
     split_pair(p0, p1, hi, lo);
     const int slot = (e >> 4) * 16 + ((e & 15) >> 1);  // K-step e/16, word within it
@@ -223,6 +231,10 @@ __global__ void __launch_bounds__(384, 1)
         tma_prefetch_desc(&tm_v);
       }
       uint32_t k_it = 0, v_it = 0, q_it = 0;
+      // decode: the page ids of the current sequence, cached in two 1024-entry
+      // windows (V trails K by one block, so both may be live at a boundary)
+      int32_t* page_cache = reinterpret_cast<int32_t*>(smem + L::kPageOff);
+      int cached_win0 = -1, cached_win1 = -1;
       // load K (IS_V false) or V of block b into its ring slot; false on abort
       auto load_kv = [&](const ItemInfo& it, int g, int b, bool is_v) -> bool {
         const uint32_t idx = is_v ? v_it : k_it;
@@ -245,10 +257,23 @@ __global__ void __launch_bounds__(384, 1)
           const int ps = p.page_size;
           const int n_tok = min(B, it.kv_len - b * B);
           const int n_pg = (n_tok + ps - 1) / ps;
+          const int pg0 = b * (B / ps);           // first page of the block (B/ps divides the window)
+          const int win = pg0 / L::kPageWin, wbuf = win & 1;
+          int32_t* wc = page_cache + wbuf * L::kPageWin;
+          if ((wbuf ? cached_win1 : cached_win0) != win) {
+            const int seq_pages = (it.kv_len + ps - 1) / ps;
+            const int32_t* row = p.page_table + static_cast<int64_t>(it.seq) * p.max_pages;
+            for (int i = lane; i < L::kPageWin; i += 32) {
+              const int gp = win * L::kPageWin + i;
+              wc[i] = gp < seq_pages ? row[gp] : -1;
+            }
+            __syncwarp();
+            if (wbuf) cached_win1 = win; else cached_win0 = win;
+          }
           if (lane == 0) mbar_arrive_expect_tx(full, n_pg * ps * 256);
           __syncwarp();
           if (lane < n_pg) {
-            int32_t pe = p.page_table[static_cast<int64_t>(it.seq) * p.max_pages + b * (B / ps) + lane];
+            int32_t pe = wc[(pg0 + lane) % L::kPageWin];
             if (pe < 0 || pe >= p.n_pages) {
               report_error(p.err, kErrBadPage, 0x104);
               pe = p.n_pages;  // out of range: the copy reads the zero fill
@@ -262,7 +287,9 @@ __global__ void __launch_bounds__(384, 1)
         if (is_v) ++v_it; else ++k_it;
         return true;
       };
-      for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+        const int item = snake_item(round);
+        if (item >= p.num_items) continue;
         const ItemInfo it = item_info<MODE>(p, item);
         bool ok = mbar_wait(&bars[L::kQEmpty], (q_it & 1) ^ 1, abort, p.err, 0x101);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -280,6 +307,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         ++q_it;
         const int g = (MODE == kModeDecode) ? it.head : it.head / p.group;
+        cached_win0 = cached_win1 = -1;  // a new sequence's page ids
         // consumption order: K_0, K_1, V_0, K_2, V_1, ...
         bool fail = false;
         for (int j = 0; j <= it.nb && !fail; ++j) {
@@ -293,7 +321,9 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t kIdescS = idesc_bf16(128, B, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, false, true);
       uint32_t k_it = 0, v_it = 0, s_it = 0, pv_it = 0, q_it = 0;
-      for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+        const int item = snake_item(round);
+        if (item >= p.num_items) continue;
         const ItemInfo it = item_info<MODE>(p, item);
         bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x201);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -382,10 +412,13 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    setmaxnreg_inc192();
     const int r = tid - 128;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t s_it = 0, st_it = 0;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = snake_item(round);
+      if (item >= p.num_items) continue;
       const ItemInfo it = item_info<MODE>(p, item);
       const bool valid = r < it.row_count;
       // a warp none of whose rows is written (decode: all but the first)
@@ -404,57 +437,64 @@ __global__ void __launch_bounds__(384, 1)
         const bool has = nvis > 0;
         float lse_b = -INFINITY, rcp = 0.0f;
         if (warp_rows) {
-        // pass 1: maximum raw score over the visible keys
-        float m = -INFINITY;
-        {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(ta, r0);
-          if (B > 32) tmem_ld32(ta + 32, r1);
-          tmem_ld_wait(r0);
-          if (B > 32) tmem_ld_wait(r1);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            m = fmaxf(m, e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
-            if (B > 32) m = fmaxf(m, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
-          }
-          if (B > 64) {
-            tmem_ld32(ta + 64, r0);
-            tmem_ld32(ta + 96, r1);
+          // pass 1: maximum raw score over the visible keys (all chunks in
+          // flight, one wait)
+          float m = -INFINITY;
+          {
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            tmem_ld32(ta, r0);
+            tmem_ld32(ta + 32, r1);
+            if (B > 64) {
+              tmem_ld32(ta + 64, r2);
+              tmem_ld32(ta + 96, r3);
+            }
             tmem_ld_wait(r0);
             tmem_ld_wait(r1);
+            if (B > 64) {
+              tmem_ld_wait(r2);
+              tmem_ld_wait(r3);
+            }
+            if (nvis == B) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              m = fmaxf(m, 64 + e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
-              m = fmaxf(m, 96 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
+              for (int e = 0; e < 32; ++e) {
+                m = fmaxf(m, fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])));
+                if (B > 64) m = fmaxf(m, fmaxf(__uint_as_float(r2[e]), __uint_as_float(r3[e])));
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                m = fmaxf(m, e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
+                m = fmaxf(m, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
+                if (B > 64) {
+                  m = fmaxf(m, 64 + e < nvis ? __uint_as_float(r2[e]) : -INFINITY);
+                  m = fmaxf(m, 96 + e < nvis ? __uint_as_float(r3[e]) : -INFINITY);
+                }
+              }
             }
           }
-        }
-        const float mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
-        const float neg_mc = -mc;
-        // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo over S
-        float part[32];
-        {
+          const float mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
+          const float neg_mc = -mc;
+          // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo
+          // over S; a rolled loop over pairs of 32-key chunks keeps the code
+          // small, the next chunk's load in flight while one is processed
+          float part[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part[e] = 0.0f;  // +0 + p == p: same sums as starting from key c
           uint32_t cur[32], nxt[32], wv[32];
           tmem_ld32(ta, cur);
           tmem_ld_wait(cur);
-          tmem_ld32(ta + 32, nxt);
-          softmax_chunk<true>(cur, 0, nvis, p.scale_log2, neg_mc, has, part, wv);
-          tmem_st32(ta, wv);
-          tmem_ld_wait(nxt);
-          if (B > 64) tmem_ld32(ta + 64, cur);
-          softmax_chunk<false>(nxt, 1, nvis, p.scale_log2, neg_mc, has, part, wv);
-          tmem_st32(ta + 32, wv);
-          if (B > 64) {
-            tmem_ld_wait(cur);
-            tmem_ld32(ta + 96, nxt);
-            softmax_chunk<false>(cur, 2, nvis, p.scale_log2, neg_mc, has, part, wv);
-            tmem_st32(ta + 64, wv);
+#pragma unroll 1
+          for (int c = 0; c < B / 32; c += 2) {
+            tmem_ld32(ta + 32 * (c + 1), nxt);
+            softmax_chunk(cur, c, nvis, p.scale_log2, neg_mc, has, part, wv);
+            tmem_st32(ta + 32 * c, wv);
             tmem_ld_wait(nxt);
-            softmax_chunk<false>(nxt, 3, nvis, p.scale_log2, neg_mc, has, part, wv);
-            tmem_st32(ta + 96, wv);
+            if (c + 2 < B / 32) tmem_ld32(ta + 32 * (c + 2), cur);
+            softmax_chunk(nxt, c + 1, nvis, p.scale_log2, neg_mc, has, part, wv);
+            tmem_st32(ta + 32 * (c + 1), wv);
+            if (c + 2 < B / 32) tmem_ld_wait(cur);
           }
-        }
-        if (has) block_stats(mc, partial_tree(part), lse_b, rcp);
+          if (has) block_stats(mc, partial_tree(part), lse_b, rcp);
         }  // warp_rows
         tmem_st_wait();
         tc_fence_before();
@@ -468,14 +508,16 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     // ------------------------------------------------------------ correction / epilogue
-    setmaxnreg_inc240();
+    setmaxnreg_inc216();
     const int r = tid;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t pv_it = 0, st_it = 0;
     float O[kHeadDim];
 #pragma unroll
     for (int e = 0; e < kHeadDim; ++e) O[e] = 0.0f;
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = snake_item(round);
+      if (item >= p.num_items) continue;
       const ItemInfo it = item_info<MODE>(p, item);
       const bool valid = r < it.row_count;
       const bool warp_rows = __any_sync(0xffffffffu, valid);
@@ -616,7 +658,7 @@ static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const
   auto kern = rlk_fwd_kernel<B, MODE>;
   static bool checked = false;
   if (!checked) {
-    // The warpgroup register split (240 / 168 / 96) needs the launch to grant
+    // The warpgroup register split (216 / 192 / 96) needs the launch to grant
     // 168 registers per thread; with fewer, setmaxnreg.inc would wait forever.
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, kern);
