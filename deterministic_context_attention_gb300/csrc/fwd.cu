@@ -148,23 +148,53 @@ __device__ __forceinline__ void setmaxnreg_dec96() {
 
 // Probabilities of 32 keys (chunk c of the block) for one row: writes the
 // packed hi/lo words in MMA-step order and adds the keys to the canonical
-// partial sums (which start at +0).
+// partial sums (which start at +0).  MASKED: keys at or past nvis are set to
+// -inf first, so their probability is exactly 0.
+template <bool MASKED>
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, int nvis, float scale_log2,
-                                              float neg_mc, bool has, float (&part)[32], uint32_t (&w)[32]) {
+                                              float neg_mc, float (&part)[32], uint32_t (&w)[32]) {
+  const float2 sc = make_float2(scale_log2, scale_log2);
+  const float2 nm = make_float2(neg_mc, neg_mc);
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    const int key = 32 * c + e;
-    float p0 = prob(__uint_as_float(raw[e]), scale_log2, neg_mc);
-    float p1 = prob(__uint_as_float(raw[e + 1]), scale_log2, neg_mc);
-    p0 = (has && key < nvis) ? p0 : 0.0f;
-    p1 = (has && key + 1 < nvis) ? p1 : 0.0f;
-    part[e] = __fadd_rn(part[e], p0);
-    part[e + 1] = __fadd_rn(part[e + 1], p1);
+    float2 s = make_float2(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]));
+    if (MASKED) {
+      const int key = 32 * c + e;
+      s.x = key < nvis ? s.x : -INFINITY;
+      s.y = key + 1 < nvis ? s.y : -INFINITY;
+    }
+    const float2 x = ffma2(s, sc, nm);
+    const float2 pr = make_float2(ex2_hw(x.x), ex2_hw(x.y));
+    const float2 acc = fadd2(make_float2(part[e], part[e + 1]), pr);
+    part[e] = acc.x;
+    part[e + 1] = acc.y;
     uint32_t hi, lo;
-    split_pair(p0, p1, hi, lo);
+    split_pair2(pr, hi, lo);
     const int slot = (e >> 4) * 16 + ((e & 15) >> 1);  // K-step e/16, word within it
     w[slot] = hi;
     w[slot + 8] = lo;
+  }
+}
+
+// Pass 2 over the block's 128 (or 64) keys: a rolled loop over pairs of
+// 32-key chunks keeps the code small; the next chunk's load is in flight
+// while one is processed.
+template <int B, bool MASKED>
+__device__ __forceinline__ void softmax_pass2(uint32_t ta, int nvis, float scale_log2, float neg_mc,
+                                              float (&part)[32]) {
+  uint32_t cur[32], nxt[32], wv[32];
+  tmem_ld32(ta, cur);
+  tmem_ld_wait(cur);
+#pragma unroll 1
+  for (int c = 0; c < B / 32; c += 2) {
+    tmem_ld32(ta + 32 * (c + 1), nxt);
+    softmax_chunk<MASKED>(cur, c, nvis, scale_log2, neg_mc, part, wv);
+    tmem_st32(ta + 32 * c, wv);
+    tmem_ld_wait(nxt);
+    if (c + 2 < B / 32) tmem_ld32(ta + 32 * (c + 2), cur);
+    softmax_chunk<MASKED>(nxt, c + 1, nvis, scale_log2, neg_mc, part, wv);
+    tmem_st32(ta + 32 * (c + 1), wv);
+    if (c + 2 < B / 32) tmem_ld_wait(cur);
   }
 }
 
@@ -435,6 +465,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t ta = tm_s + lane_off + buf * 128;
         const int nvis = valid ? visible_keys(pos, it.kv_len, b, B) : 0;
         const bool has = nvis > 0;
+        // every row of the warp sees all B keys: no masking on this block
+        const bool full = __all_sync(0xffffffffu, nvis == B);
         float lse_b = -INFINITY, rcp = 0.0f;
         if (warp_rows) {
           // pass 1: maximum raw score over the visible keys (all chunks in
@@ -454,46 +486,44 @@ __global__ void __launch_bounds__(384, 1)
               tmem_ld_wait(r2);
               tmem_ld_wait(r3);
             }
-            if (nvis == B) {
+            // four independent partial maxima (the maximum is exact, so the
+            // grouping does not matter)
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+            if (full) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                m = fmaxf(m, fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])));
-                if (B > 64) m = fmaxf(m, fmaxf(__uint_as_float(r2[e]), __uint_as_float(r3[e])));
+              for (int e = 0; e < 32; e += 2) {
+                m0 = fmax3(m0, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
+                m1 = fmax3(m1, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
+                if (B > 64) {
+                  m2 = fmax3(m2, __uint_as_float(r2[e]), __uint_as_float(r2[e + 1]));
+                  m3 = fmax3(m3, __uint_as_float(r3[e]), __uint_as_float(r3[e + 1]));
+                }
               }
             } else {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                m = fmaxf(m, e < nvis ? __uint_as_float(r0[e]) : -INFINITY);
-                m = fmaxf(m, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY);
+              for (int e = 0; e < 32; e += 2) {
+                m0 = fmax3(m0, e < nvis ? __uint_as_float(r0[e]) : -INFINITY,
+                           e + 1 < nvis ? __uint_as_float(r0[e + 1]) : -INFINITY);
+                m1 = fmax3(m1, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY,
+                           33 + e < nvis ? __uint_as_float(r1[e + 1]) : -INFINITY);
                 if (B > 64) {
-                  m = fmaxf(m, 64 + e < nvis ? __uint_as_float(r2[e]) : -INFINITY);
-                  m = fmaxf(m, 96 + e < nvis ? __uint_as_float(r3[e]) : -INFINITY);
+                  m2 = fmax3(m2, 64 + e < nvis ? __uint_as_float(r2[e]) : -INFINITY,
+                             65 + e < nvis ? __uint_as_float(r2[e + 1]) : -INFINITY);
+                  m3 = fmax3(m3, 96 + e < nvis ? __uint_as_float(r3[e]) : -INFINITY,
+                             97 + e < nvis ? __uint_as_float(r3[e + 1]) : -INFINITY);
                 }
               }
             }
+            m = fmax3(fmaxf(m0, m1), m2, m3);
           }
           const float mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
           const float neg_mc = -mc;
-          // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo
-          // over S; a rolled loop over pairs of 32-key chunks keeps the code
-          // small, the next chunk's load in flight while one is processed
+          // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo over S
           float part[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) part[e] = 0.0f;  // +0 + p == p: same sums as starting from key c
-          uint32_t cur[32], nxt[32], wv[32];
-          tmem_ld32(ta, cur);
-          tmem_ld_wait(cur);
-#pragma unroll 1
-          for (int c = 0; c < B / 32; c += 2) {
-            tmem_ld32(ta + 32 * (c + 1), nxt);
-            softmax_chunk(cur, c, nvis, p.scale_log2, neg_mc, has, part, wv);
-            tmem_st32(ta + 32 * c, wv);
-            tmem_ld_wait(nxt);
-            if (c + 2 < B / 32) tmem_ld32(ta + 32 * (c + 2), cur);
-            softmax_chunk(nxt, c + 1, nvis, p.scale_log2, neg_mc, has, part, wv);
-            tmem_st32(ta + 32 * (c + 1), wv);
-            if (c + 2 < B / 32) tmem_ld_wait(cur);
-          }
+          if (full) softmax_pass2<B, false>(ta, nvis, p.scale_log2, neg_mc, part);
+          else softmax_pass2<B, true>(ta, nvis, p.scale_log2, neg_mc, part);
           if (has) block_stats(mc, partial_tree(part), lse_b, rcp);
         }  // warp_rows
         tmem_st_wait();
@@ -577,36 +607,36 @@ __global__ void __launch_bounds__(384, 1)
           if (j > 0 && has) fold_coeffs(Lrun, lse_b, Lp, alpha, beta);  // overlaps the PV loads
           tmem_ld_wait(x0);
           tmem_ld_wait(x1);
+          const float2 rc2 = make_float2(rcp, rcp), al2 = make_float2(alpha, alpha), be2 = make_float2(beta, beta);
+          // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha)  (packed, two lanes at a time)
+          auto fold64 = [&](const uint32_t (&xa)[32], const uint32_t (&xb)[32], int o0) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float o0 = state_elem(__uint_as_float(x0[e]), rcp);
-            const float o1 = state_elem(__uint_as_float(x1[e]), rcp);
-            if (j == 0) {
-              O[e] = o0;
-              O[32 + e] = o1;
-            } else if (has) {
-              O[e] = fold_elem(O[e], o0, alpha, beta);
-              O[32 + e] = fold_elem(O[32 + e], o1, alpha, beta);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 oa = fmul2(make_float2(__uint_as_float(xa[e]), __uint_as_float(xa[e + 1])), rc2);
+              const float2 ob = fmul2(make_float2(__uint_as_float(xb[e]), __uint_as_float(xb[e + 1])), rc2);
+              if (j == 0) {
+                O[o0 + e] = oa.x;
+                O[o0 + e + 1] = oa.y;
+                O[o0 + 32 + e] = ob.x;
+                O[o0 + 33 + e] = ob.y;
+              } else if (has) {
+                const float2 ra = ffma2(oa, be2, fmul2(make_float2(O[o0 + e], O[o0 + e + 1]), al2));
+                const float2 rb = ffma2(ob, be2, fmul2(make_float2(O[o0 + 32 + e], O[o0 + 33 + e]), al2));
+                O[o0 + e] = ra.x;
+                O[o0 + e + 1] = ra.y;
+                O[o0 + 32 + e] = rb.x;
+                O[o0 + 33 + e] = rb.y;
+              }
             }
-          }
+          };
+          fold64(x0, x1, 0);
           tmem_ld32(ta + 64, x0);
           tmem_ld32(ta + 96, x1);
           tmem_ld_wait(x0);
           tmem_ld_wait(x1);
           tc_fence_before();
           mbar_arrive(&bars[L::kPVEmpty + buf]);  // PV read: the buffer is free
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float o0 = state_elem(__uint_as_float(x0[e]), rcp);
-            const float o1 = state_elem(__uint_as_float(x1[e]), rcp);
-            if (j == 0) {
-              O[64 + e] = o0;
-              O[96 + e] = o1;
-            } else if (has) {
-              O[64 + e] = fold_elem(O[64 + e], o0, alpha, beta);
-              O[96 + e] = fold_elem(O[96 + e], o1, alpha, beta);
-            }
-          }
+          fold64(x0, x1, 64);
           if (has) Lrun = (j == 0) ? lse_b : Lp;
         }
         ++pv_it;

@@ -80,6 +80,57 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
   lo = pack_bf16x2(r0, r1);
 }
 
+// Packed FP32x2 forms (sm_100-class): each lane is one IEEE round-to-nearest
+// operation, bit-identical to the scalar __fmaf_rn / __fadd_rn / __fsub_rn /
+// __fmul_rn on that lane, so kernels may use either form for the same step.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// max of three (exact, so any grouping gives the same maximum)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Split a pair of probabilities into packed BF16 hi and lo words (the same
+// values as split_pair, with packed subtraction).
+__device__ __forceinline__ void split_pair2(float2 p, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(p.x, p.y);
+  const float2 h = make_float2(bf16_lo_as_f32(hi), bf16_hi_as_f32(hi));
+  const float2 r = fsub2(p, h);
+  lo = pack_bf16x2(r.x, r.y);
+}
+
 // Block output element: o = PV * (1/l).
 __device__ __forceinline__ float state_elem(float pv, float rcp) { return __fmul_rn(pv, rcp); }
 
