@@ -136,6 +136,40 @@ __device__ __forceinline__ int visible_keys(int pos, int kv_len, int b, int B) {
   return max(0, min(B, last - b * B + 1));
 }
 
+// Lean MMA issue.  A shared-memory descriptor is kept as its two 32-bit
+// halves; the start-address field is the low 14 bits (address / 16), so a
+// K-step offset is a plain 32-bit add on the low half (shared addresses stay
+// below 256 KB, so the field never carries).
+struct Desc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  const uint64_t d = sdesc_sw128(saddr, lbo, sbo);
+  return Desc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+template <int ACC>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, Desc a, uint32_t a_off, Desc b, uint32_t b_off,
+                                       uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t.reg .b32 la, lb;\n\t"
+      "add.u32 la, %1, %3;\n\tadd.u32 lb, %4, %6;\n\t"
+      "mov.b64 da, {la, %2};\n\tmov.b64 db, {lb, %5};\n\t"
+      "setp.ne.b32 p, %8, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %7, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(a_off), "r"(b.lo), "r"(b.hi), "r"(b_off), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, Desc b, uint32_t b_off, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t.reg .b32 lb;\n\t"
+      "add.u32 lb, %2, %4;\n\tmov.b64 db, {lb, %3};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(b_off), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
 __device__ __forceinline__ void setmaxnreg_inc216() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
 }
@@ -350,6 +384,7 @@ __global__ void __launch_bounds__(384, 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescS = idesc_bf16(128, B, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, false, true);
+      const Desc qd0 = make_desc(q_addr, 16, 1024);
       uint32_t k_it = 0, v_it = 0, s_it = 0, pv_it = 0, q_it = 0;
       for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
         const int item = snake_item(round);
@@ -366,15 +401,14 @@ __global__ void __launch_bounds__(384, 1)
           if (!__all_sync(0xffffffffu, w)) return false;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t k_addr = smem_u32(k_base + stage * L::kKVBytes);
+            const Desc kd0 = make_desc(smem_u32(k_base + stage * L::kKVBytes), 16, 1024);
             const uint32_t d = tm_s + ((sb + j) & 1) * 128;
+            // S = Q K^T: K-steps 0-3 in the first 64-column half, 4-7 in the second
+            mma_ss<0>(d, qd0, 0, kd0, 0, kIdescS);
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) {
-              const uint32_t half = k >> 2, sub = (k & 3) * 32;
-              const uint64_t ad = sdesc_sw128(q_addr + half * L::kQHalf + sub, 16, 1024);
-              const uint64_t bd = sdesc_sw128(k_addr + half * L::kKVHalf + sub, 16, 1024);
-              umma_ss(d, ad, bd, kIdescS, k > 0 ? 1u : 0u);
-            }
+            for (int k = 1; k < kHeadDim / 16; ++k)
+              mma_ss<1>(d, qd0, (k >> 2) * (L::kQHalf >> 4) + (k & 3) * 2, kd0, (k >> 2) * (L::kKVHalf >> 4) + (k & 3) * 2,
+                        kIdescS);
             umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
             umma_commit(&bars[L::kKEmpty + stage]);
           }
@@ -415,19 +449,15 @@ __global__ void __launch_bounds__(384, 1)
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t v_addr = smem_u32(vd);
+            const Desc vdd = make_desc(smem_u32(vd), L::kKVHalf, 1024);
             const uint32_t a0 = tm_s + buf * 128;
             const uint32_t d = tm_pv + pvbuf * 128;
+            // PV = P_hi V + P_lo V; K-step k reads V rows 16k..16k+15 (2048 B)
+            mma_ts<0>(d, a0, vdd, 0, kIdescPV);
 #pragma unroll
-            for (int k = 0; k < B / 16; ++k) {
-              const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
-              umma_ts(d, a0 + 16 * k, bd, kIdescPV, k > 0 ? 1u : 0u);
-            }
+            for (int k = 1; k < B / 16; ++k) mma_ts<1>(d, a0 + 16 * k, vdd, k * 128, kIdescPV);
 #pragma unroll
-            for (int k = 0; k < B / 16; ++k) {
-              const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, L::kKVHalf, 1024);
-              umma_ts(d, a0 + 16 * k + 8, bd, kIdescPV, 1u);
-            }
+            for (int k = 0; k < B / 16; ++k) mma_ts<1>(d, a0 + 16 * k + 8, vdd, k * 128, kIdescPV);
             umma_commit(&bars[L::kPVFull + pvbuf]);
             umma_commit(&bars[L::kVEmpty + vstage]);
           }
