@@ -40,6 +40,23 @@ WORKLOAD = ("qwen3-8b causal GQA prefill, varlen {4096,3000,1024,777} (8897 toke
             "bf16 q/k/v N(0,1) + RoPE theta=1e6, KV block 128, logical CP=1, out fp32+bf16 + lse")
 
 
+def kernel_traffic(name):
+    """DRAM bytes per launch of a kernel from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel sources changed since
+    the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    entry = json.load(open(path))["kernels"].get(name)
+    if not entry:
+        return None
+    h = hashlib.sha256()
+    for src in entry["sources"]:
+        h.update(open(os.path.join(ROOT, src), "rb").read())
+    return entry["traffic_bytes"] if h.hexdigest() == entry["sources_sha256"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -233,7 +250,9 @@ def run_gpu(args):
                     "ms_per_step": round(e2e_ms, 5)},
             "gpu_launches": args.steps,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": kernel_traffic("rlk_fwd_kernel<128, fused>"),
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "peak_source": f"{peaks['source']} bf16 dense burst",
                          "kernel": "rlk_fwd_kernel<128, fused>",
                          "physical_frac": round(1.5 * achieved / peak, 4)},
