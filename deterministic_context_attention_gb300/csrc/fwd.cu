@@ -18,16 +18,17 @@
 // Status and Acceptance: fixed merge order, full-KV arithmetic retained, max
 // abs 0.0 across ranks).
 //
-// Warp roles (384 threads, three warpgroups):
+// Warp roles (512 threads, four warpgroups):
 //   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r) and
-//              keeps the running O of its row in registers (216 per thread)
-//   warps 4-7  softmax: thread r owns TMEM lane r; reads S, writes P_hi/P_lo
+//              keeps the running O of its row in registers
+//   warps 4-7  softmax (even global blocks): thread r owns TMEM lane r; reads S, writes P_hi/P_lo
 //              over it (per 16-key MMA step: 8 columns hi, then 8 lo)
 //   warp  8    TMA producer (Q tile; K and V blocks or pages, separate rings)
 //   warp  9    TMEM allocator and MMA issuer (also zeroes V rows past the
 //              valid length of a partial block)
 //   warps 10-11 idle (registers are granted per warpgroup: warps 8-11 run
-//              with 96, warps 4-7 with 192, warps 0-3 with 216)
+//              with 48, warps 0-3 with 208)
+//   warps 12-15 second softmax group: groups alternate global blocks
 // TMEM (512 columns): S/P double buffer [0,256), PV double buffer [256,512).
 // Per block the tensor core runs S_{b+1} then PV_b, so the softmax of block
 // b+1 overlaps PV_b and the correction of block b overlaps both.
@@ -42,12 +43,15 @@
 
 namespace rlk {
 
-// register split per warpgroup (launch: 168 per thread for 384 threads)
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsCorrection = 216;
-constexpr int kRegsSoftmax = 192;
-constexpr int kRegsProducer = 96;
-static_assert(kRegsCorrection + kRegsSoftmax + kRegsProducer <= 3 * kRegsLaunch, "register split");
+// Four warpgroups (512 threads, 128 registers per thread at launch),
+// re-split per warpgroup: correction 208, two softmax groups 128 each,
+// producer / MMA 48.
+constexpr int kThreads = 512;
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsCorrection = 208;
+constexpr int kRegsSoftmax = 128;
+constexpr int kRegsProducer = 48;
+static_assert(kRegsCorrection + 2 * kRegsSoftmax + kRegsProducer <= 4 * kRegsLaunch, "register split");
 
 template <int B>
 struct FwdLayout {
@@ -170,14 +174,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, Desc b,
       : "memory");
 }
 
-__device__ __forceinline__ void setmaxnreg_inc216() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_inc208() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
 }
-__device__ __forceinline__ void setmaxnreg_inc192() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-}
-__device__ __forceinline__ void setmaxnreg_dec96() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_dec48() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
 }
 
 // Probabilities of 32 keys (chunk c of the block) for one row: writes the
@@ -210,30 +211,23 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, 
   }
 }
 
-// Pass 2 over the block's 128 (or 64) keys: a rolled loop over pairs of
-// 32-key chunks keeps the code small; the next chunk's load is in flight
-// while one is processed.
+// Pass 2 over the block's keys, one 32-key chunk at a time (a rolled loop
+// keeps the code small).
 template <int B, bool MASKED>
 __device__ __forceinline__ void softmax_pass2(uint32_t ta, int nvis, float scale_log2, float neg_mc,
                                               float (&part)[32]) {
-  uint32_t cur[32], nxt[32], wv[32];
-  tmem_ld32(ta, cur);
-  tmem_ld_wait(cur);
+  uint32_t cur[32], wv[32];
 #pragma unroll 1
-  for (int c = 0; c < B / 32; c += 2) {
-    tmem_ld32(ta + 32 * (c + 1), nxt);
+  for (int c = 0; c < B / 32; ++c) {
+    tmem_ld32(ta + 32 * c, cur);
+    tmem_ld_wait(cur);
     softmax_chunk<MASKED>(cur, c, nvis, scale_log2, neg_mc, part, wv);
     tmem_st32(ta + 32 * c, wv);
-    tmem_ld_wait(nxt);
-    if (c + 2 < B / 32) tmem_ld32(ta + 32 * (c + 2), cur);
-    softmax_chunk<MASKED>(nxt, c + 1, nvis, scale_log2, neg_mc, part, wv);
-    tmem_st32(ta + 32 * (c + 1), wv);
-    if (c + 2 < B / 32) tmem_ld_wait(cur);
   }
 }
 
 template <int B, int MODE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     rlk_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = FwdLayout<B>;
@@ -285,8 +279,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* k_base = smem + L::kKOff;
   uint8_t* v_base = smem + L::kVOff;
 
-  if (warp >= 8) {
-    setmaxnreg_dec96();
+  if (warp >= 8 && warp < 12) {
+    setmaxnreg_dec48();
     if (warp == 8) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
@@ -472,8 +466,11 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc192();
-    const int r = tid - 128;
+    // two warpgroups take alternate global blocks: group 0 (warps 4-7) the
+    // even ones, group 1 (warps 12-15) the odd ones, so each has two blocks'
+    // time for one block's softmax; row r is TMEM lane r in both
+    const int swg = warp >= 12 ? 1 : 0;
+    const int r = tid - (swg ? 384 : 128);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t s_it = 0, st_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
@@ -488,7 +485,12 @@ __global__ void __launch_bounds__(384, 1)
       bool fail = false;
       for (int j = 0; j < it.nb; ++j) {
         const int b = it.blk0 + j;
-        const uint32_t buf = s_it & 1;
+        const uint32_t buf = s_it & 1;  // == the group that owns this block
+        if (static_cast<int>(buf) != swg) {
+          ++s_it;
+          ++st_it;
+          continue;
+        }
         bool w = mbar_wait(&bars[L::kSFull + buf], (s_it >> 1) & 1, abort, p.err, 0x301);
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
@@ -503,44 +505,42 @@ __global__ void __launch_bounds__(384, 1)
           // flight, one wait)
           float m = -INFINITY;
           {
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld32(ta, r0);
-            tmem_ld32(ta + 32, r1);
-            if (B > 64) {
-              tmem_ld32(ta + 64, r2);
-              tmem_ld32(ta + 96, r3);
-            }
-            tmem_ld_wait(r0);
-            tmem_ld_wait(r1);
-            if (B > 64) {
-              tmem_ld_wait(r2);
-              tmem_ld_wait(r3);
-            }
             // four independent partial maxima (the maximum is exact, so the
-            // grouping does not matter)
+            // grouping does not matter); two 32-column chunks in flight at a time
             float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-            if (full) {
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                m0 = fmax3(m0, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
-                m1 = fmax3(m1, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
-                if (B > 64) {
-                  m2 = fmax3(m2, __uint_as_float(r2[e]), __uint_as_float(r2[e + 1]));
-                  m3 = fmax3(m3, __uint_as_float(r3[e]), __uint_as_float(r3[e + 1]));
+            for (int h = 0; h < B / 64; ++h) {
+              uint32_t r0[32], r1[32];
+              tmem_ld32(ta + 64 * h, r0);
+              tmem_ld32(ta + 64 * h + 32, r1);
+              tmem_ld_wait(r0);
+              tmem_ld_wait(r1);
+              if (full) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  if (h == 0) {
+                    m0 = fmax3(m0, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
+                    m1 = fmax3(m1, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
+                  } else {
+                    m2 = fmax3(m2, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
+                    m3 = fmax3(m3, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
+                  }
                 }
-              }
-            } else {
+              } else {
+                const int k0 = 64 * h;
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                m0 = fmax3(m0, e < nvis ? __uint_as_float(r0[e]) : -INFINITY,
-                           e + 1 < nvis ? __uint_as_float(r0[e + 1]) : -INFINITY);
-                m1 = fmax3(m1, 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY,
-                           33 + e < nvis ? __uint_as_float(r1[e + 1]) : -INFINITY);
-                if (B > 64) {
-                  m2 = fmax3(m2, 64 + e < nvis ? __uint_as_float(r2[e]) : -INFINITY,
-                             65 + e < nvis ? __uint_as_float(r2[e + 1]) : -INFINITY);
-                  m3 = fmax3(m3, 96 + e < nvis ? __uint_as_float(r3[e]) : -INFINITY,
-                             97 + e < nvis ? __uint_as_float(r3[e + 1]) : -INFINITY);
+                for (int e = 0; e < 32; e += 2) {
+                  const float a0 = k0 + e < nvis ? __uint_as_float(r0[e]) : -INFINITY;
+                  const float a1 = k0 + e + 1 < nvis ? __uint_as_float(r0[e + 1]) : -INFINITY;
+                  const float b0 = k0 + 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY;
+                  const float b1 = k0 + 33 + e < nvis ? __uint_as_float(r1[e + 1]) : -INFINITY;
+                  if (h == 0) {
+                    m0 = fmax3(m0, a0, a1);
+                    m1 = fmax3(m1, b0, b1);
+                  } else {
+                    m2 = fmax3(m2, a0, a1);
+                    m3 = fmax3(m3, b0, b1);
+                  }
                 }
               }
             }
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     // ------------------------------------------------------------ correction / epilogue
-    setmaxnreg_inc216();
+    setmaxnreg_inc208();
     const int r = tid;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t pv_it = 0, st_it = 0;
@@ -632,41 +632,37 @@ __global__ void __launch_bounds__(384, 1)
           }
         } else {
           tmem_ld32(ta, x0);
-          tmem_ld32(ta + 32, x1);
           float Lp = 0.f, alpha = 0.f, beta = 0.f;
-          if (j > 0 && has) fold_coeffs(Lrun, lse_b, Lp, alpha, beta);  // overlaps the PV loads
-          tmem_ld_wait(x0);
-          tmem_ld_wait(x1);
+          if (j > 0 && has) fold_coeffs(Lrun, lse_b, Lp, alpha, beta);  // overlaps the PV load
           const float2 rc2 = make_float2(rcp, rcp), al2 = make_float2(alpha, alpha), be2 = make_float2(beta, beta);
           // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha)  (packed, two lanes at a time)
-          auto fold64 = [&](const uint32_t (&xa)[32], const uint32_t (&xb)[32], int o0) {
+          auto fold32 = [&](const uint32_t (&xa)[32], int o0) {
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const float2 oa = fmul2(make_float2(__uint_as_float(xa[e]), __uint_as_float(xa[e + 1])), rc2);
-              const float2 ob = fmul2(make_float2(__uint_as_float(xb[e]), __uint_as_float(xb[e + 1])), rc2);
               if (j == 0) {
                 O[o0 + e] = oa.x;
                 O[o0 + e + 1] = oa.y;
-                O[o0 + 32 + e] = ob.x;
-                O[o0 + 33 + e] = ob.y;
               } else if (has) {
                 const float2 ra = ffma2(oa, be2, fmul2(make_float2(O[o0 + e], O[o0 + e + 1]), al2));
-                const float2 rb = ffma2(ob, be2, fmul2(make_float2(O[o0 + 32 + e], O[o0 + 33 + e]), al2));
                 O[o0 + e] = ra.x;
                 O[o0 + e + 1] = ra.y;
-                O[o0 + 32 + e] = rb.x;
-                O[o0 + 33 + e] = rb.y;
               }
             }
           };
-          fold64(x0, x1, 0);
-          tmem_ld32(ta + 64, x0);
-          tmem_ld32(ta + 96, x1);
           tmem_ld_wait(x0);
+          tmem_ld32(ta + 32, x1);
+          fold32(x0, 0);
+          tmem_ld_wait(x1);
+          tmem_ld32(ta + 64, x0);
+          fold32(x1, 32);
+          tmem_ld_wait(x0);
+          tmem_ld32(ta + 96, x1);
+          fold32(x0, 64);
           tmem_ld_wait(x1);
           tc_fence_before();
           mbar_arrive(&bars[L::kPVEmpty + buf]);  // PV read: the buffer is free
-          fold64(x0, x1, 64);
+          fold32(x1, 96);
           if (has) Lrun = (j == 0) ? lse_b : Lp;
         }
         ++pv_it;
@@ -718,8 +714,9 @@ static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const
   auto kern = rlk_fwd_kernel<B, MODE>;
   static bool checked = false;
   if (!checked) {
-    // The warpgroup register split (216 / 192 / 96) needs the launch to grant
-    // 168 registers per thread; with fewer, setmaxnreg.inc would wait forever.
+    // The warpgroup register split (208 / 128 / 128 / 48) needs the launch to
+    // grant 128 registers per thread; with fewer, setmaxnreg.inc would wait
+    // forever.
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, kern);
     if (e != cudaSuccess) return e;
@@ -732,7 +729,7 @@ static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const
     if (e != cudaSuccess) return e;
     checked = true;
   }
-  kern<<<grid, 384, L::kAlloc, stream>>>(p, tq, tk, tv);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
