@@ -470,7 +470,8 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
   std::vector<rlk::FwdTile> tiles;
   for (auto& c : costed) tiles.push_back(c.second);
   CUtensorMap mq, mk, mv;
-  if ((st = make_map(&mq, q, params->num_q_heads, params->num_seqs, group, 1))) return st;
+  // one query head per TMA box: the kernel places each head in its own lane quadrant
+  if ((st = make_map(&mq, q, params->num_q_heads, params->num_seqs, 1, 1))) return st;
   if ((st = make_map(&mk, k_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))
     return st;
   if ((st = make_map(&mv, v_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))

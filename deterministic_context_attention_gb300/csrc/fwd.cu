@@ -140,6 +140,16 @@ __device__ __forceinline__ int visible_keys(int pos, int kv_len, int b, int B) {
   return max(0, min(B, last - b * B + 1));
 }
 
+// Decode places query head i of a KV head's group in tile row (TMEM lane)
+// 32 * (i % 4) + i / 4, so a small group is spread over the four lane
+// quadrants and each warp of a group works on one of its rows (a warp reaches
+// only its own 32 lanes).  Prefill and states rows map one to one.
+template <int MODE>
+__device__ __forceinline__ int row_of_lane(int r) {
+  return MODE == kModeDecode ? 4 * (r & 31) + (r >> 5) : r;
+}
+__device__ __forceinline__ int decode_lane_of_row(int i) { return 32 * (i & 3) + (i >> 2); }
+
 // Lean MMA issue.  A shared-memory descriptor is kept as its two 32-bit
 // halves; the start-address field is the low 14 bits (address / 16), so a
 // K-step offset is a plain 32-bit add on the low half (shared addresses stay
@@ -353,9 +363,13 @@ __global__ void __launch_bounds__(512, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
         if (lane == 0) {
           if (MODE == kModeDecode) {
+            // one TMA row per query head, into the row of its lane quadrant
             mbar_arrive_expect_tx(&bars[L::kQFull], p.group * kHeadDim * 2);
-            tma_load_3d(smem + L::kQOff, &tm_q, &bars[L::kQFull], 0, it.head * p.group, it.seq);
-            tma_load_3d(smem + L::kQOff + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head * p.group, it.seq);
+            for (int i = 0; i < p.group; ++i) {
+              uint8_t* dst = smem + L::kQOff + decode_lane_of_row(i) * 128;
+              tma_load_3d(dst, &tm_q, &bars[L::kQFull], 0, it.head * p.group + i, it.seq);
+              tma_load_3d(dst + L::kQHalf, &tm_q, &bars[L::kQFull], 64, it.head * p.group + i, it.seq);
+            }
           } else {
             mbar_arrive_expect_tx(&bars[L::kQFull], L::kQBytes);
             const int row0 = it.q_tok0 + it.row_begin;
@@ -477,7 +491,7 @@ __global__ void __launch_bounds__(512, 1)
       const int item = snake_item(round);
       if (item >= p.num_items) continue;
       const ItemInfo it = item_info<MODE>(p, item);
-      const bool valid = r < it.row_count;
+      const bool valid = row_of_lane<MODE>(r) < it.row_count;
       // a warp none of whose rows is written (decode: all but the first)
       // only takes part in the barriers
       const bool warp_rows = __any_sync(0xffffffffu, valid);
@@ -497,8 +511,10 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t ta = tm_s + lane_off + buf * 128;
         const int nvis = valid ? visible_keys(pos, it.kv_len, b, B) : 0;
         const bool has = nvis > 0;
-        // every row of the warp sees all B keys: no masking on this block
-        const bool full = __all_sync(0xffffffffu, nvis == B);
+        // every row of the warp that is written sees all B keys: no masking
+        // on this block (a row that is not written may hold anything: MMA
+        // rows are independent and its state is never stored)
+        const bool full = __all_sync(0xffffffffu, !valid || nvis == B);
         float lse_b = -INFINITY, rcp = 0.0f;
         if (warp_rows) {
           // pass 1: maximum raw score over the visible keys (all chunks in
@@ -579,7 +595,7 @@ __global__ void __launch_bounds__(512, 1)
       const int item = snake_item(round);
       if (item >= p.num_items) continue;
       const ItemInfo it = item_info<MODE>(p, item);
-      const bool valid = r < it.row_count;
+      const bool valid = row_of_lane<MODE>(r) < it.row_count;
       const bool warp_rows = __any_sync(0xffffffffu, valid);
       float Lrun = -INFINITY;
       bool fail = false;
@@ -672,7 +688,8 @@ __global__ void __launch_bounds__(512, 1)
       if (MODE != kModeStates && valid) {
         // epilogue: O and L are final; write FP32 / BF16 rows and lse
         int64_t row_idx;
-        if (MODE == kModeDecode) row_idx = static_cast<int64_t>(it.seq) * p.hq + it.head * p.group + r;
+        if (MODE == kModeDecode)
+          row_idx = static_cast<int64_t>(it.seq) * p.hq + it.head * p.group + row_of_lane<MODE>(r);
         else row_idx = static_cast<int64_t>(it.q_tok0 + it.row_begin + r) * p.hq + it.head;
         if (p.out_f32) {
           float4* dst = reinterpret_cast<float4*>(p.out_f32 + row_idx * kHeadDim);
