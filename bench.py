@@ -448,7 +448,7 @@ def run_reference(args):
 
 def run_profile(args):
     """Run one entry point a few times without timing, for ncu captures:
-    --profile prefill|states|merge|decode|backward."""
+    --profile prefill|states|merge|decode|decode-small|backward."""
     import torch
     import deterministic_context_attention_gb300 as rlk
     from deterministic_context_attention_gb300 import build as rbuild
@@ -461,10 +461,13 @@ def run_profile(args):
         prob, p, (q, k, v, out, do, lse, dq, dk, dvv, ws), _ = backward_workload(torch, rlk, dv)
         for _ in range(n):
             rlk.rlk_attn_backward(p, q, k, v, out, do, lse, prob.cu_q, -1, dq, dk, dvv, ws, stream=stream)
-    elif args.profile == "decode":
+    elif args.profile in ("decode", "decode-small"):
+        # decode-small: the same shape with contexts up to 4096 tokens (about
+        # 0.6 GB of pages, above L2) for captures that replay many passes
         g = torch.Generator(device="cuda")
         g.manual_seed(3)
-        ctx = synth.rng(3, synth.T_LENS).integers(512, 32769, size=64).astype(np.int32)
+        hi = 4097 if args.profile == "decode-small" else 32769
+        ctx = synth.rng(3, synth.T_LENS).integers(512, hi, size=64).astype(np.int32)
         pages_per = (ctx + 15) // 16
         n_pages = int(pages_per.sum())
         perm = synth.rng(3, synth.T_PAGES).permutation(n_pages).astype(np.int32)
@@ -521,7 +524,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-rows", type=int, default=512)
-    ap.add_argument("--profile", default=None, choices=["prefill", "states", "merge", "decode", "backward"])
+    ap.add_argument("--profile", default=None,
+                    choices=["prefill", "states", "merge", "decode", "decode-small", "backward"])
     ap.add_argument("--profile-iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile:

@@ -22,6 +22,9 @@ namespace rlk {
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream);
+bool decode_transposed_supported(const FwdParams& p);
+cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int grid, cudaStream_t stream);
 cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
 rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
                         const float* out_f32, const void* dout, const float* lse,
@@ -486,7 +489,21 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
   fp->max_pages = max_pages;
   fp->page_size = page_size;
   fp->n_pages = n_pages;
-  if ((st = launch_fwd_tiles(fp.get(), tiles, 1, mq, mk, mv, dev, stream))) return st;
+  if (!rlk::decode_transposed_supported(*fp)) {
+    if ((st = launch_fwd_tiles(fp.get(), tiles, 1, mq, mk, mv, dev, stream))) return st;
+    return ok();
+  }
+  // KV blocks of 128 keys and up to 8 query heads per KV head: the
+  // transposed decode kernel (keys on the MMA's M side)
+  for (size_t t0 = 0; t0 < tiles.size(); t0 += rlk::kMaxTilesPerLaunch) {
+    const size_t n = std::min(tiles.size() - t0, static_cast<size_t>(rlk::kMaxTilesPerLaunch));
+    std::copy(tiles.begin() + t0, tiles.begin() + t0 + n, fp->tiles);
+    fp->num_tiles = static_cast<int32_t>(n);
+    fp->num_items = static_cast<int32_t>(n);
+    const int grid = std::min(fp->num_items, dev->num_sms);
+    cudaError_t e = rlk::launch_decode(*fp, mq, mk, mv, grid, stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  }
   return ok();
 }
 

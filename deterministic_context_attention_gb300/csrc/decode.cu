@@ -1,0 +1,551 @@
+// decode.cu -- paged-KV decode for sm_103a in transposed form.
+//
+// A decode step has one query token per sequence, so the query rows of one
+// (sequence, KV head) item are only the group's query heads (4 for 32 / 8).
+// The forward engine's 128-row tile would leave 124 of its 128 MMA rows
+// idle; this kernel instead puts the KV block's 128 keys on the MMA's M side:
+//   S^T = K_b Q^T        (M = 128 keys, N = 16 query columns, K = 128 dims)
+//   O^T = V_b^T P^T      (M = 128 dims, N = 16 query columns, K = 128 keys)
+// with the group padded to N = 16 by zero rows.  The block state of every
+// query head is the same as the prefill's ("WS2 Attention PR5 Drift
+// Benchmark", Transformer Engine Reuse: state_b = (o_b, lse_b, b)) and every
+// floating-point step is the one numerics.cuh defines, in the same order:
+// the block maximum (exact), p = 2^fma(S, scale_log2, -m scale_log2), the
+// canonical row sum (key c to partial c mod 32 in ascending key order, then
+// the fixed 16-8-4-2-1 tree), P = P_hi + P_lo, PV accumulated over the hi
+// K-steps then the lo K-steps, o_b = PV / l and the canonical fold in
+// ascending global_block_index order.  The tensor core gives the same bits
+// for a product and for its transposed formulation, so a decode row equals
+// the prefill's last row of the same sequence bit for bit.
+//
+// Warp roles (480 threads):
+//   warps 0-3   correction / epilogue: thread d owns TMEM lane d (head
+//               dimension d) and keeps the running O of every query head
+//   warps 4-7   softmax of the even blocks, warps 8-11 of the odd blocks:
+//               thread t owns TMEM lane t (key t of the block)
+//   warp  12    TMA producer of the group's query rows and the K pages
+//   warp  13    TMA producer of the V pages
+//   warp  14    TMEM allocator and MMA issuer
+// TMEM (128 columns): S^T ring [0,64), O^T ring [64,128), 16 columns a slot.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+
+#include "numerics.cuh"
+#include "ptx.cuh"
+#include "rlk_internal.h"
+
+namespace rlk {
+namespace {
+
+constexpr int kDThreads = 480;
+constexpr int kDN = 16;  // MMA N: the group's query heads, padded with zero rows
+
+struct DecLayout {
+  static constexpr int B = 128;
+  static constexpr int kSK = 3, kSV = 2;  // K and V rings
+  static constexpr int kPS = 2;           // P^T operand slots
+  static constexpr int kSS = 4, kOS = 4;  // TMEM rings of S^T and O^T
+  static constexpr int kSR = 8;           // statistics ring
+  static constexpr int kKVHalf = B * 128;                 // one 64-dim half of a K or V block
+  static constexpr int kKVBytes = 2 * kKVHalf;
+  static constexpr int kTHalf = kDN * 128;                // one 64-column half of a 16-row operand
+  static constexpr int kTBytes = 2 * kTHalf;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kTBytes;
+  static constexpr int kVOff = kKOff + kSK * kKVBytes;
+  static constexpr int kPOff = kVOff + kSV * kKVBytes;    // [slot][hi, lo] tiles
+  // per softmax group: block maxima float [2][4][kDecodeMaxGroup] and
+  // partial sums float [2][4][kDecodeMaxGroup][32], double-buffered by block
+  static constexpr int kRedBytes = 2 * 4 * kDecodeMaxGroup * 4;
+  static constexpr int kPartBytes = 2 * 4 * kDecodeMaxGroup * 32 * 4;
+  static constexpr int kRedOff = kPOff + kPS * 2 * kTBytes;
+  static constexpr int kPartOff = kRedOff + 2 * kRedBytes;
+  static constexpr int kStatsOff = kPartOff + 2 * kPartBytes;  // float2 [kSR][kDecodeMaxGroup]
+  static constexpr int kBarOff = kStatsOff + kSR * kDecodeMaxGroup * 8;
+  static constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kSK, kVFull = kKEmpty + kSK,
+                       kVEmpty = kVFull + kSV, kSFull = kVEmpty + kSV, kSEmpty = kSFull + kSS,
+                       kPFull = kSEmpty + kSS, kPEmpty = kPFull + kPS, kOFull = kPEmpty + kPS,
+                       kOEmpty = kOFull + kOS, kStatsFull = kOEmpty + kOS, kSyncMax = kStatsFull + kSR,
+                       kSyncPart = kSyncMax + 4, kNumBars = kSyncPart + 4;  // sync: [group][parity]
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
+  static constexpr int kPageWin = 512;                     // page ids cached per window (one per producer)
+  static constexpr int kPageOff = (kMiscOff + 16 + 15) / 16 * 16;
+  static constexpr int kTotal = kPageOff + 2 * kPageWin * 4;
+  static constexpr int kAlloc = kTotal + 1024;
+};
+static_assert(DecLayout::kAlloc <= 232448, "decode shared memory");
+static_assert(DecLayout::kKOff % 1024 == 0 && DecLayout::kVOff % 1024 == 0 && DecLayout::kPOff % 1024 == 0,
+              "128-byte-swizzled tiles start on 1024-byte boundaries");
+
+// Byte offset of element (row, col) of a 16-row operand tile of 128 BF16
+// columns, stored K-major as two 64-column halves in the 128-byte swizzle
+// (the layout a TMA load with 128-byte swizzle produces).
+__device__ __forceinline__ uint32_t tile16_off(int row, int col) {
+  const int half = col >> 6, c = col & 63;
+  const uint32_t chunk = static_cast<uint32_t>(c >> 3) ^ static_cast<uint32_t>(row & 7);
+  return static_cast<uint32_t>(half * DecLayout::kTHalf + row * 128) + chunk * 16 + static_cast<uint32_t>(c & 7) * 2;
+}
+
+__device__ __forceinline__ int dec_snake_item(int round) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return round * g + ((round & 1) ? g - 1 - c : c);
+}
+
+__device__ __forceinline__ float bf16_bits_as_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+// Row maximum of the 32 lanes of a warp (exact; every lane receives it).
+__device__ __forceinline__ float warp_max(float v) {
+  float m;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
+}
+
+// MG: the group's query heads rounded up to 1, 2, 4 or 8 (heads at or past
+// the group size are skipped at run time).
+template <int MG>
+__global__ void __launch_bounds__(kDThreads, 1)
+    rlk_decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using L = DecLayout;
+  constexpr int B = L::B, SK = L::kSK, SV = L::kSV, PS = L::kPS, SS = L::kSS, OS = L::kOS, SR = L::kSR;
+  static_assert(MG <= kDecodeMaxGroup && PS == 2, "decode layout");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int G = p.group;
+
+  // operand rows at or past G are never written: they must read as zero
+  for (int i = tid; i < L::kTBytes / 16; i += kDThreads)
+    reinterpret_cast<uint4*>(smem + L::kQOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < PS * 2 * L::kTBytes / 16; i += kDThreads)
+    reinterpret_cast<uint4*>(smem + L::kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bars[L::kQFull], 1);
+    mbar_init(&bars[L::kQEmpty], 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&bars[L::kKFull + s], 1);
+      mbar_init(&bars[L::kKEmpty + s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&bars[L::kVFull + s], 1);
+      mbar_init(&bars[L::kVEmpty + s], 1);
+    }
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(&bars[L::kSFull + s], 1);
+      mbar_init(&bars[L::kSEmpty + s], 128);
+    }
+    for (int s = 0; s < PS; ++s) {
+      mbar_init(&bars[L::kPFull + s], 128);
+      mbar_init(&bars[L::kPEmpty + s], 1);
+    }
+    for (int s = 0; s < OS; ++s) {
+      mbar_init(&bars[L::kOFull + s], 1);
+      mbar_init(&bars[L::kOEmpty + s], 128);
+    }
+    for (int s = 0; s < SR; ++s) mbar_init(&bars[L::kStatsFull + s], 128);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars[L::kSyncMax + s], 128);
+      mbar_init(&bars[L::kSyncPart + s], 128);
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 14) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_s = tmem;       // S^T slots: + 16 * slot
+  const uint32_t tm_o = tmem + 64;  // O^T slots: + 16 * slot
+  uint8_t* q_tile = smem + L::kQOff;
+  uint8_t* k_base = smem + L::kKOff;
+  uint8_t* v_base = smem + L::kVOff;
+  uint8_t* p_base = smem + L::kPOff;
+
+  if (warp == 12 || warp == 13) {
+    // ------------------------------------------------------------ producers
+    // warp 12 loads the query rows and K, warp 13 V, so neither ring waits
+    // on the other's free slots
+    const bool is_v = warp == 13;
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    if (lane == 0) {
+      if (!is_v) tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(map);
+    }
+    const int S = is_v ? SV : SK;
+    uint64_t* full_b = &bars[is_v ? L::kVFull : L::kKFull];
+    uint64_t* empty_b = &bars[is_v ? L::kVEmpty : L::kKEmpty];
+    uint8_t* ring = is_v ? v_base : k_base;
+    // the page ids of the current sequence, one window cached per producer
+    int32_t* wc = reinterpret_cast<int32_t*>(smem + L::kPageOff) + (is_v ? L::kPageWin : 0);
+    uint32_t it_n = 0, q_it = 0;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = dec_snake_item(round);
+      if (item >= p.num_items) continue;
+      const FwdTile& t = p.tiles[item];
+      const int seq = t.seq, g = t.row_begin, kv_len = p.cu_k[seq];
+      const int nb = (kv_len + B - 1) / B;
+      if (!is_v) {
+        bool ok = mbar_wait(&bars[L::kQEmpty], (q_it & 1) ^ 1, abort, p.err, 0x501);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) {
+          // the group's query rows 0..G-1 of the 16-row operand tile
+          mbar_arrive_expect_tx(&bars[L::kQFull], G * kHeadDim * 2);
+          for (int i = 0; i < G; ++i) {
+            tma_load_3d(q_tile + i * 128, &tm_q, &bars[L::kQFull], 0, g * G + i, seq);
+            tma_load_3d(q_tile + L::kTHalf + i * 128, &tm_q, &bars[L::kQFull], 64, g * G + i, seq);
+          }
+        }
+        ++q_it;
+      }
+      const int ps = p.page_size;
+      const int seq_pages = (kv_len + ps - 1) / ps;
+      const int32_t* prow = p.page_table + static_cast<int64_t>(seq) * p.max_pages;
+      int cached = -1;  // a new sequence's page ids
+      bool fail = false;
+      for (int b = 0; b < nb; ++b) {
+        const uint32_t stage = it_n % S;
+        bool ok = mbar_wait(empty_b + stage, ((it_n / S) & 1) ^ 1, abort, p.err, is_v ? 0x503 : 0x502);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        uint8_t* dst = ring + stage * L::kKVBytes;
+        const int n_tok = min(B, kv_len - b * B);
+        const int n_pg = (n_tok + ps - 1) / ps;
+        const int pg0 = b * (B / ps);  // B / ps divides the window
+        const int win = pg0 / L::kPageWin;
+        if (cached != win) {
+          for (int i = lane; i < L::kPageWin; i += 32) {
+            const int gp = win * L::kPageWin + i;
+            wc[i] = gp < seq_pages ? prow[gp] : -1;
+          }
+          __syncwarp();
+          cached = win;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(full_b + stage, n_pg * ps * 256);
+        __syncwarp();
+        if (lane < n_pg) {
+          int32_t pe = wc[(pg0 + lane) % L::kPageWin];
+          if (pe < 0 || pe >= p.n_pages) {
+            report_error(p.err, kErrBadPage, 0x504);
+            pe = p.n_pages;  // out of range: the copy reads the zero fill
+          }
+          const int r = pe * ps;
+          const int off = lane * ps * 128;
+          tma_load_3d(dst + off, map, full_b + stage, 0, g, r);
+          tma_load_3d(dst + L::kKVHalf + off, map, full_b + stage, 64, g, r);
+        }
+        ++it_n;
+      }
+      if (fail || *abort) break;
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16(128, kDN, false, false);  // A = K (K-major), B = Q (K-major)
+    constexpr uint32_t kIdO = idesc_bf16(128, kDN, true, false);   // A = V^T (dims contiguous), B = P^T
+    const Desc qd = make_desc(smem_u32(q_tile), 16, 1024);
+    uint32_t k_it = 0, v_it = 0, s_it = 0, o_it = 0, q_it = 0;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = dec_snake_item(round);
+      if (item >= p.num_items) continue;
+      const FwdTile& t = p.tiles[item];
+      const int kv_len = p.cu_k[t.seq];
+      const int nb = (kv_len + B - 1) / B;
+      bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x601);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ++q_it;
+      const uint32_t kb = k_it, vb = v_it, sb = s_it, ob = o_it;
+      // S^T_j = K_j Q^T into S^T slot (sb + j) mod SS
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t ki = kb + j, stage = ki % SK;
+        const uint32_t si = sb + j, slot = si % SS;
+        bool w = mbar_wait(&bars[L::kKFull + stage], (ki / SK) & 1, abort, p.err, 0x602);
+        w = w && mbar_wait(&bars[L::kSEmpty + slot], ((si / SS) & 1) ^ 1, abort, p.err, 0x603);
+        if (!__all_sync(0xffffffffu, w)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const Desc kd = make_desc(smem_u32(k_base + stage * L::kKVBytes), 16, 1024);
+          const uint32_t d = tm_s + slot * 16;
+          // K-steps over head dimensions: 0-3 in the first 64-dim half, 4-7 in the second
+          mma_ss<0>(d, kd, 0, qd, 0, kIdS);
+#pragma unroll
+          for (int s = 1; s < kHeadDim / 16; ++s)
+            mma_ss<1>(d, kd, (s >> 2) * (L::kKVHalf >> 4) + (s & 3) * 2, qd, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2,
+                      kIdS);
+          umma_commit(&bars[L::kSFull + slot]);
+          umma_commit(&bars[L::kKEmpty + stage]);
+          if (j + 1 == nb) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
+        }
+        __syncwarp();
+        return true;
+      };
+      // S runs up to three blocks ahead of O (the S^T ring has four slots)
+      const int ahead = min(nb, 3);
+      bool fail = false;
+      for (int j = 0; j < ahead && !fail; ++j)
+        if (!issue_s(j)) fail = true;
+      if (fail) break;
+      for (int j = 0; j < nb; ++j) {
+        if (j + 3 < nb && !issue_s(j + 3)) { fail = true; break; }
+        const uint32_t vi = vb + j, vstage = vi % SV;
+        const uint32_t oi = ob + j, oslot = oi % OS, pslot = oi % PS;
+        bool w = mbar_wait(&bars[L::kPFull + pslot], (oi / PS) & 1, abort, p.err, 0x604);
+        w = w && mbar_wait(&bars[L::kVFull + vstage], (vi / SV) & 1, abort, p.err, 0x605);
+        w = w && mbar_wait(&bars[L::kOEmpty + oslot], ((oi / OS) & 1) ^ 1, abort, p.err, 0x606);
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+        uint8_t* vd = v_base + vstage * L::kKVBytes;
+        // V rows past the context may hold stale or non-finite data; P is
+        // exactly 0 there, so zero them (0 * NaN = NaN)
+        const int valid = min(B, kv_len - j * B);
+        if (valid < B) {
+          const int nrow = B - valid;
+          for (int i = lane; i < nrow * 16; i += 32) {
+            const int row = valid + (i >> 4);
+            const int piece = i & 15;  // 16 B pieces: 8 per half-row, 2 halves
+            *reinterpret_cast<uint4*>(vd + (piece >> 3) * L::kKVHalf + row * 128 + (piece & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          // O^T = V^T P_hi^T + V^T P_lo^T: K-step s covers keys 16s..16s+15
+          // (V rows: 2048 B a step; P^T columns: 32 B a step within a half)
+          const Desc vdd = make_desc(smem_u32(vd), L::kKVHalf, 1024);
+          const Desc ph = make_desc(smem_u32(p_base + pslot * 2 * L::kTBytes), 16, 1024);
+          const Desc pl = make_desc(smem_u32(p_base + pslot * 2 * L::kTBytes + L::kTBytes), 16, 1024);
+          const uint32_t d = tm_o + oslot * 16;
+          mma_ss<0>(d, vdd, 0, ph, 0, kIdO);
+#pragma unroll
+          for (int s = 1; s < B / 16; ++s)
+            mma_ss<1>(d, vdd, s * 128, ph, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
+#pragma unroll
+          for (int s = 0; s < B / 16; ++s)
+            mma_ss<1>(d, vdd, s * 128, pl, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
+          umma_commit(&bars[L::kOFull + oslot]);
+          umma_commit(&bars[L::kVEmpty + vstage]);
+          umma_commit(&bars[L::kPEmpty + pslot]);
+        }
+        __syncwarp();
+      }
+      if (fail) break;
+      k_it += nb;
+      v_it += nb;
+      s_it += nb;
+      o_it += nb;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    // two groups of four warps take alternate blocks (group = block parity,
+    // which is also the block's P^T slot)
+    const int grp = warp >= 8 ? 1 : 0;
+    const int t = tid - (grp ? 256 : 128);  // key lane
+    const int w = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(w * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + L::kRedOff + grp * L::kRedBytes);
+    float* part = reinterpret_cast<float*>(smem + L::kPartOff + grp * L::kPartBytes);
+    const float sl = p.scale_log2;
+    uint32_t s_it = 0, sy_it = 0;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = dec_snake_item(round);
+      if (item >= p.num_items) continue;
+      const int kv_len = p.cu_k[p.tiles[item].seq];
+      const int nb = (kv_len + B - 1) / B;
+      bool fail = false;
+      for (int j = 0; j < nb; ++j, ++s_it) {
+        if (static_cast<int>(s_it & 1) != grp) continue;  // the other group's block
+        const uint32_t slot = s_it % SS;
+        bool ok = mbar_wait(&bars[L::kSFull + slot], (s_it / SS) & 1, abort, p.err, 0x701);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        tc_fence_after();
+        uint32_t raw[16];
+        tmem_ld16(tm_s + lane_off + slot * 16, raw);
+        tmem_ld_wait(raw);
+        tc_fence_before();
+        mbar_arrive(&bars[L::kSEmpty + slot]);
+        const bool vis = j * B + t < kv_len;
+        const int rb = static_cast<int>(sy_it & 1);
+        const uint32_t sy_par = (sy_it >> 1) & 1;
+        // block maximum of every query head over the visible keys (exact)
+#pragma unroll
+        for (int q = 0; q < MG; ++q) {
+          const float m = warp_max((q < G && vis) ? __uint_as_float(raw[q]) : -INFINITY);
+          if (lane == 0) red[(rb * 4 + w) * MG + q] = m;
+        }
+        mbar_arrive(&bars[L::kSyncMax + grp * 2 + rb]);
+        ok = mbar_wait(&bars[L::kSyncMax + grp * 2 + rb], sy_par, abort, p.err, 0x702);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        float mc[MG], pr[MG];
+#pragma unroll
+        for (int q = 0; q < MG; ++q) {
+          const float* r4 = red + rb * 4 * MG + q;
+          const float m = fmaxf(fmaxf(fmaxf(r4[0], r4[MG]), r4[2 * MG]), r4[3 * MG]);
+          mc[q] = __fmul_rn(m, sl);
+          pr[q] = (q < G && vis) ? prob(__uint_as_float(raw[q]), sl, -mc[q]) : 0.0f;
+        }
+        // P^T = P_hi^T + P_lo^T into the operand tiles of P slot grp
+        ok = mbar_wait(&bars[L::kPEmpty + grp], ((s_it / PS) & 1) ^ 1, abort, p.err, 0x703);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        uint8_t* ph = p_base + grp * 2 * L::kTBytes;
+#pragma unroll
+        for (int q = 0; q < MG; ++q) {
+          if (q < G) {
+            const uint16_t hi = f32_to_bf16_rn(pr[q]);
+            const uint16_t lo = f32_to_bf16_rn(__fsub_rn(pr[q], bf16_bits_as_f32(hi)));
+            const uint32_t o = tile16_off(q, t);
+            *reinterpret_cast<uint16_t*>(ph + o) = hi;
+            *reinterpret_cast<uint16_t*>(ph + L::kTBytes + o) = lo;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[L::kPFull + grp]);
+        // canonical row sums: key c goes to partial c mod 32 (this lane); the
+        // partial adds the four warps' keys of the lane in ascending order,
+        // then the 16-8-4-2-1 tree runs as a butterfly (lane 0 holds the sum)
+#pragma unroll
+        for (int q = 0; q < MG; ++q) part[((rb * 4 + w) * MG + q) * 32 + lane] = pr[q];
+        mbar_arrive(&bars[L::kSyncPart + grp * 2 + rb]);
+        ok = mbar_wait(&bars[L::kSyncPart + grp * 2 + rb], sy_par, abort, p.err, 0x704);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        const uint32_t sslot = s_it % SR;
+#pragma unroll
+        for (int q = 0; q < MG; ++q) {
+          if (q >= G || (q & 3) != w) continue;  // warp w sums query heads w, w + 4
+          const float* pq = part + (rb * 4 * MG + q) * 32 + lane;
+          float a = pq[0];
+          a = __fadd_rn(a, pq[MG * 32]);
+          a = __fadd_rn(a, pq[2 * MG * 32]);
+          a = __fadd_rn(a, pq[3 * MG * 32]);
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
+          if (lane == 0) {
+            float lse_b, rcp;
+            block_stats(mc[q], a, lse_b, rcp);
+            stats[sslot * kDecodeMaxGroup + q] = make_float2(lse_b, rcp);
+          }
+        }
+        mbar_arrive(&bars[L::kStatsFull + sslot]);
+        ++sy_it;
+      }
+      if (fail) break;
+    }
+  } else {
+    // ------------------------------------------------------------ correction / epilogue
+    const int d = tid;  // head dimension lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t o_it = 0;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = dec_snake_item(round);
+      if (item >= p.num_items) continue;
+      const FwdTile& tl = p.tiles[item];
+      const int seq = tl.seq, g = tl.row_begin;
+      const int kv_len = p.cu_k[seq];
+      const int nb = (kv_len + B - 1) / B;
+      float O[MG];
+#pragma unroll
+      for (int q = 0; q < MG; ++q) O[q] = 0.0f;
+      float Lrun = -INFINITY;  // lane q: running lse of query head q
+      bool fail = false;
+      for (int j = 0; j < nb; ++j) {
+        const uint32_t sslot = o_it % SR, oslot = o_it % OS;
+        bool ok = mbar_wait(&bars[L::kStatsFull + sslot], (o_it / SR) & 1, abort, p.err, 0x801);
+        ok = ok && mbar_wait(&bars[L::kOFull + oslot], (o_it / OS) & 1, abort, p.err, 0x802);
+        if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
+        tc_fence_after();
+        uint32_t raw[16];
+        tmem_ld16(tm_o + lane_off + oslot * 16, raw);
+        // fold coefficients of query head `lane` (overlap the TMEM load)
+        float lb = -INFINITY, rc = 0.0f, al = 0.0f, be = 0.0f, Lp = 0.0f;
+        if (lane < G) {
+          const float2 st = stats[sslot * kDecodeMaxGroup + lane];
+          lb = st.x;
+          rc = st.y;
+          if (j > 0) fold_coeffs(Lrun, lb, Lp, al, be);
+        }
+        tmem_ld_wait(raw);
+        tc_fence_before();
+        mbar_arrive(&bars[L::kOEmpty + oslot]);
+        // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha)
+#pragma unroll
+        for (int q = 0; q < MG; ++q) {
+          const float rq = __shfl_sync(0xffffffffu, rc, q);
+          const float aq = __shfl_sync(0xffffffffu, al, q);
+          const float bq = __shfl_sync(0xffffffffu, be, q);
+          if (q < G) {
+            const float oa = __fmul_rn(__uint_as_float(raw[q]), rq);
+            O[q] = (j == 0) ? oa : __fmaf_rn(oa, bq, __fmul_rn(O[q], aq));
+          }
+        }
+        if (lane < G) Lrun = (j == 0) ? lb : Lp;
+        ++o_it;
+      }
+      if (fail) break;
+      // epilogue: O and L are final
+#pragma unroll
+      for (int q = 0; q < MG; ++q) {
+        if (q < G) {
+          const int64_t row = static_cast<int64_t>(seq) * p.hq + g * G + q;
+          if (p.out_f32) p.out_f32[row * kHeadDim + d] = O[q];
+          if (p.out_bf16) p.out_bf16[row * kHeadDim + d] = f32_to_bf16_rn(O[q]);
+        }
+      }
+      if (warp == 0 && lane < G && p.lse) p.lse[static_cast<int64_t>(seq) * p.hq + g * G + lane] = Lrun;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 14) {
+    if (*abort) {
+      // let copies already in flight land before the CTA's memory is released
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+template <int MG>
+cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(rlk_decode_kernel<MG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DecLayout::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  rlk_decode_kernel<MG><<<grid, kDThreads, DecLayout::kAlloc, stream>>>(p, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_transposed_supported(const FwdParams& p) {
+  return p.block == DecLayout::B && p.group >= 1 && p.group <= kDecodeMaxGroup && p.page_size >= 8 &&
+         DecLayout::kPageWin % (DecLayout::B / p.page_size) == 0;
+}
+
+cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int grid, cudaStream_t stream) {
+  if (p.group <= 1) return launch_decode_t<1>(p, tq, tk, tv, grid, stream);
+  if (p.group <= 2) return launch_decode_t<2>(p, tq, tk, tv, grid, stream);
+  if (p.group <= 4) return launch_decode_t<4>(p, tq, tk, tv, grid, stream);
+  return launch_decode_t<8>(p, tq, tk, tv, grid, stream);
+}
+
+}  // namespace rlk

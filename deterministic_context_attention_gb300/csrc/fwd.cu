@@ -150,40 +150,6 @@ __device__ __forceinline__ int row_of_lane(int r) {
 }
 __device__ __forceinline__ int decode_lane_of_row(int i) { return 32 * (i & 3) + (i >> 2); }
 
-// Lean MMA issue.  A shared-memory descriptor is kept as its two 32-bit
-// halves; the start-address field is the low 14 bits (address / 16), so a
-// K-step offset is a plain 32-bit add on the low half (shared addresses stay
-// below 256 KB, so the field never carries).
-struct Desc {
-  uint32_t lo, hi;
-};
-__device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  const uint64_t d = sdesc_sw128(saddr, lbo, sbo);
-  return Desc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
-}
-template <int ACC>
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, Desc a, uint32_t a_off, Desc b, uint32_t b_off,
-                                       uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t.reg .b32 la, lb;\n\t"
-      "add.u32 la, %1, %3;\n\tadd.u32 lb, %4, %6;\n\t"
-      "mov.b64 da, {la, %2};\n\tmov.b64 db, {lb, %5};\n\t"
-      "setp.ne.b32 p, %8, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %7, p;\n\t}" ::"r"(d_tmem),
-      "r"(a.lo), "r"(a.hi), "r"(a_off), "r"(b.lo), "r"(b.hi), "r"(b_off), "r"(idesc), "n"(ACC)
-      : "memory");
-}
-template <int ACC>
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, Desc b, uint32_t b_off, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t.reg .b32 lb;\n\t"
-      "add.u32 lb, %2, %4;\n\tmov.b64 db, {lb, %3};\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(b_off), "r"(idesc), "n"(ACC)
-      : "memory");
-}
-
 __device__ __forceinline__ void setmaxnreg_inc208() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
 }

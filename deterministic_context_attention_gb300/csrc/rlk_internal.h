@@ -9,6 +9,7 @@ constexpr int kHeadDim = 128;           // D, the only head size the kernels tak
 constexpr int kMaxSeqs = 128;           // sequences per call (they ride in kernel params)
 constexpr int kMaxTilesPerLaunch = 880; // work tiles per launch (kernel param space)
 constexpr int kTileRows = 128;          // MMA M: query rows per tile
+constexpr int kDecodeMaxGroup = 8;     // query heads per KV head the transposed decode kernel takes
 constexpr int64_t kNoAllocIndexEntries = 65536;  // no-alloc merge scratch: (sequence, block) index entries
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded mbarrier waits: 1 s
 

@@ -13,7 +13,7 @@ from tests.gpu_helpers import assert_bitwise, assert_forward_parity, empty_outpu
 pytestmark = pytest.mark.gpu
 
 
-def run_decode(dec, page_table=None, k_bits=None, v_bits=None, seqs=None):
+def run_decode(dec, page_table=None, k_bits=None, v_bits=None, seqs=None, block=128):
     torch = torch_cuda()
     rlk = lib()
     from deterministic_context_attention_gb300 import device as dv
@@ -26,7 +26,7 @@ def run_decode(dec, page_table=None, k_bits=None, v_bits=None, seqs=None):
     vp = torch.from_numpy(vb.view(np.int16)).cuda().view(torch.bfloat16)
     ptd = dv.i32_to_device(pt[seqs])
     out, outb, lse = empty_outputs(torch, len(seqs), dec.hq)
-    p = rlk.make_params(len(seqs), dec.hq, dec.hkv, 128, softmax_scale=dec.scale)
+    p = rlk.make_params(len(seqs), dec.hq, dec.hkv, block, softmax_scale=dec.scale)
     rlk.rlk_attn_decode_paged(p, q, kp, vp, kb.shape[0], dec.page_size, ptd, pt.shape[1], dec.seqlens[seqs],
                               out, outb, lse)
     rlk.rlk_attn_check_device_error()
@@ -88,3 +88,25 @@ def test_bad_page_id_reported(small_dec):
     assert e.value.status == 8  # RLK_ERR_BAD_PAGE
     rlk.rlk_attn_check_device_error()  # cleared
     del torch
+
+
+# Query heads per KV head 1, 2, 4 and 8 run the transposed decode kernel (keys
+# on the MMA's M side, one instantiation per padded group size); 16 heads per
+# KV head and 64-key blocks run the forward engine's decode mode.  Every one
+# matches the oracle and equals the last row of the same prefill bit for bit.
+@pytest.mark.parametrize("hq,hkv,block", [(8, 8, 128), (16, 8, 128), (24, 8, 128), (32, 4, 128), (32, 2, 128),
+                                          (32, 8, 64)])
+def test_decode_group_sizes_and_block(hq, hkv, block):
+    dec = synth.paged_decode_problem(ctx=[1, 64, 129, 300, 777], hq=hq, hkv=hkv, seed=41, spare_pages=3)
+    out, outb, lse = run_decode(dec, block=block)
+    ref_out, ref_lse = oracle.decode_paged_f64(dec.q, dec.k_pool, dec.v_pool, dec.page_table, dec.seqlens, dec.scale)
+    assert_forward_parity(out, outb, lse, ref_out, ref_lse, f"decode hq{hq}/hkv{hkv} block {block}")
+    for s in range(len(dec.seqlens)):
+        ctx = int(dec.seqlens[s])
+        ks, vs = dec.seq_kv(s)
+        q = np.zeros((ctx, dec.hq, 128), np.float32)
+        q[-1] = dec.q[s]
+        cu = np.array([0, ctx], np.int32)
+        prob = synth.Prefill(q, ks, vs, cu, cu, dec.hq, dec.hkv, 128, dec.scale, block)
+        po, pb, pl = run_fused(prob)
+        assert_bitwise((out[s], outb[s], lse[s]), (po[-1], pb[-1], pl[-1]), f"sequence {s} (ctx {ctx})")
