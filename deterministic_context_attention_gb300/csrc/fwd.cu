@@ -73,8 +73,13 @@ struct FwdLayout {
   static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;
   static constexpr int kPageWin = 1024;  // decode: page ids cached per window
   static constexpr int kPageOff = kStatsOff + kStatsRing * kTileRows * 8;
-  static constexpr int kTotal = kPageOff + 2 * kPageWin * 4;
+  // epilogue staging: per correction warp 32 rows x 128 B (one column chunk)
+  static constexpr int kEpiOff = kPageOff + 2 * kPageWin * 4;
+  static constexpr int kEpiBytes = 4 * 32 * 128;
+  static constexpr int kTotal = kEpiOff + kEpiBytes;
   static constexpr int kAlloc = kTotal + 1024;
+  static_assert(kAlloc <= 232448, "forward shared memory");
+  static_assert(kEpiOff % 16 == 0, "staging alignment");
 };
 
 struct ItemInfo {
@@ -651,12 +656,59 @@ __global__ void __launch_bounds__(512, 1)
         ++st_it;
       }
       if (fail) break;
-      if (MODE != kModeStates && valid) {
-        // epilogue: O and L are final; write FP32 / BF16 rows and lse
-        int64_t row_idx;
-        if (MODE == kModeDecode)
-          row_idx = static_cast<int64_t>(it.seq) * p.hq + it.head * p.group + row_of_lane<MODE>(r);
-        else row_idx = static_cast<int64_t>(it.q_tok0 + it.row_begin + r) * p.hq + it.head;
+      if (MODE == kModeFused) {
+        // epilogue: O and L are final.  Each warp stages its 32 rows through
+        // shared memory one 128-byte column chunk at a time (chunk j of a
+        // row in slot j ^ (row & 7), so neither side conflicts on banks) and
+        // writes four whole rows' chunks per store instruction.
+        float4* stg = reinterpret_cast<float4*>(smem + L::kEpiOff + (warp & 3) * (32 * 128));
+        const int r0 = (warp & 3) * 32;
+        const int64_t row_base = static_cast<int64_t>(it.q_tok0 + it.row_begin) * p.hq + it.head;
+        auto write_chunks = [&](auto&& store) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), jj = lane & 7;
+            const int tr = r0 + rr;
+            const float4 v = stg[rr * 8 + (jj ^ (rr & 7))];
+            if (tr < it.row_count) store(row_base + static_cast<int64_t>(tr) * p.hq, jj, v);
+          }
+        };
+        if (p.out_f32) {
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 32; ++c) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              stg[lane * 8 + (j ^ (lane & 7))] =
+                  make_float4(O[32 * c + 4 * j], O[32 * c + 4 * j + 1], O[32 * c + 4 * j + 2], O[32 * c + 4 * j + 3]);
+            __syncwarp();
+            write_chunks([&](int64_t row_idx, int jj, const float4& v) {
+              reinterpret_cast<float4*>(p.out_f32 + row_idx * kHeadDim + 32 * c)[jj] = v;
+            });
+            __syncwarp();
+          }
+        }
+        if (p.out_bf16) {
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 64; ++c) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int e = 64 * c + 8 * j;
+              const uint4 w = make_uint4(pack_bf16x2(O[e], O[e + 1]), pack_bf16x2(O[e + 2], O[e + 3]),
+                                         pack_bf16x2(O[e + 4], O[e + 5]), pack_bf16x2(O[e + 6], O[e + 7]));
+              stg[lane * 8 + (j ^ (lane & 7))] = *reinterpret_cast<const float4*>(&w);
+            }
+            __syncwarp();
+            write_chunks([&](int64_t row_idx, int jj, const float4& v) {
+              reinterpret_cast<float4*>(p.out_bf16 + row_idx * kHeadDim + 64 * c)[jj] = v;
+            });
+            __syncwarp();
+          }
+        }
+        if (p.lse && valid) p.lse[row_base + static_cast<int64_t>(r) * p.hq] = Lrun;
+      } else if (MODE == kModeDecode && valid) {
+        // epilogue (decode): the group's rows are spread over the lane
+        // quadrants; few rows, written directly
+        const int64_t row_idx = static_cast<int64_t>(it.seq) * p.hq + it.head * p.group + row_of_lane<MODE>(r);
         if (p.out_f32) {
           float4* dst = reinterpret_cast<float4*>(p.out_f32 + row_idx * kHeadDim);
 #pragma unroll
