@@ -50,15 +50,59 @@ __global__ void __launch_bounds__(1024) rlk_merge_index_kernel(const __grid_cons
   }
 }
 
-// One warp per (query row, head); lane l holds elements 4l..4l+3.
-__global__ void __launch_bounds__(256) rlk_merge_fold_kernel(const __grid_constant__ MergeParams p) {
-  const int lane = threadIdx.x & 31;
+// Four threads per (query row, head) pair, eight heads of one row per warp:
+// thread q of a pair holds elements 16m + 4q .. 16m + 4q + 3 (m = 0..7), so
+// a pair's four threads move 64 contiguous bytes per instruction, and each
+// thread follows its pair's fold coefficients itself (the coefficient chain
+// is serial per pair; a quarter of a row per thread keeps it cheap).  The
+// warp's pairs share the row's blocks: lane j resolves the slab of block
+// b0 + j for all of them.  State rows stream through a per-thread ring of
+// asynchronous copies into shared memory (kMergeStages deep), so two blocks
+// per pair are in flight while one folds; a thread reads only its own slots.
+constexpr int kMergeHeadsPerWarp = 8;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeStages = 3;
+constexpr int kMergeSmem = kMergeStages * (8 * kMergeThreads * 16 + kMergeThreads * 4);
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 2) rlk_merge_fold_kernel(const __grid_constant__ MergeParams p) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  float4* ring = reinterpret_cast<float4*>(msm);  // [stage][m][thread]
+  float* lring = reinterpret_cast<float*>(msm + kMergeStages * 8 * kMergeThreads * 16);  // [stage][thread]
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int sub = lane >> 2;  // pair within the warp
+  const int qq = lane & 3;    // element quarter
+  const int chunks = (p.hq + kMergeHeadsPerWarp - 1) / kMergeHeadsPerWarp;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  const int64_t total = p.total_rows * p.hq;
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
-       w += warps) {
-    const int64_t tok = w / p.hq;
-    const int h = static_cast<int>(w - tok * p.hq);
+  const int64_t total = p.total_rows * chunks;
+  // issue the copies of one state row quarter (and its lse) into ring slot st;
+  // a missing state gets lse = -inf and no data (the fold skips it)
+  auto issue = [&](int64_t pr, int st) {
+    if (pr >= 0) {
+      const float4* src = reinterpret_cast<const float4*>(p.state_o + pr * kHeadDim) + qq;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) cp_async16(&ring[(st * 8 + m) * kMergeThreads + tid], src + 4 * m);
+      cp_async4(&lring[st * kMergeThreads + tid], p.state_lse + pr);
+    } else {
+      lring[st * kMergeThreads + tid] = -INFINITY;
+    }
+  };
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (tid >> 5); w < total; w += warps) {
+    const int64_t tok = w / chunks;
+    const int h = static_cast<int>(w - tok * chunks) * kMergeHeadsPerWarp + sub;
+    const bool hv = h < p.hq;  // lanes past the last head take part in the warp's shuffles only
     int s = 0;
     {  // sequence of packed row tok
       int lo = 0, hi = p.num_seqs - 1;
@@ -73,14 +117,16 @@ __global__ void __launch_bounds__(256) rlk_merge_fold_kernel(const __grid_consta
     const int i = static_cast<int>(tok - p.cu_q[s]);
     const int pos = kv_len - q_len + i;
     const int nb = pos / p.block + 1;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 O[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) O[m] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
     bool bad = false;
-    // Blocks are visited in groups of 32: lane j resolves block b0 + j (slab,
-    // pair, lse) and the group's state rows are then streamed in order.
     for (int b0 = 0; b0 < nb; b0 += 32) {
-      int64_t my_pair = -1;
-      float my_lse = -INFINITY;
+      // lane j: the slab of block b0 + j (same for every head of the row)
+      int64_t my_off = 0;
+      int my_rb = 0, my_rc = 0;
+      bool my_ok = false;
       const int b = b0 + lane;
       if (b < nb) {
         const int sid = p.index[s * p.max_blocks + b];
@@ -88,51 +134,77 @@ __global__ void __launch_bounds__(256) rlk_merge_fold_kernel(const __grid_consta
           const Slab sl = p.slabs[sid];
           const int r = i - sl.row_begin;
           if (r >= 0 && r < sl.row_count) {
-            my_pair = sl.offset + static_cast<int64_t>(h) * sl.row_count + r;
-            my_lse = p.state_lse[my_pair];
+            my_off = sl.offset;
+            my_rb = sl.row_begin;
+            my_rc = sl.row_count;
+            my_ok = true;
           }
         }
       }
-      if (__any_sync(0xffffffffu, b < nb && my_pair < 0)) bad = true;
+      if (__any_sync(0xffffffffu, b < nb && !my_ok)) bad = true;
       const int n_here = min(32, nb - b0);
-      int64_t pair = __shfl_sync(0xffffffffu, my_pair, 0);
-      float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (pair >= 0) cur = *reinterpret_cast<const float4*>(p.state_o + pair * kHeadDim + 4 * lane);
+      // state pair of this thread's head for block b0 + j (-1: none)
+      auto pair_of = [&](int j) -> int64_t {
+        const int64_t off = __shfl_sync(0xffffffffu, my_off, j);
+        const int rb = __shfl_sync(0xffffffffu, my_rb, j);
+        const int rc = __shfl_sync(0xffffffffu, my_rc, j);
+        const bool ok = __shfl_sync(0xffffffffu, my_ok, j);
+        return (ok && hv) ? off + static_cast<int64_t>(h) * rc + (i - rb) : -1;
+      };
+      // prologue: blocks 0 and 1 of the group in flight
+#pragma unroll
+      for (int j = 0; j < kMergeStages - 1; ++j) {
+        if (j < n_here) issue(pair_of(j), j);
+        cp_async_commit();
+      }
       for (int j = 0; j < n_here; ++j) {
-        const float lb = __shfl_sync(0xffffffffu, my_lse, j);
-        float4 nxt = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j + 1 < n_here) {
-          const int64_t np = __shfl_sync(0xffffffffu, my_pair, j + 1);
-          if (np >= 0) nxt = *reinterpret_cast<const float4*>(p.state_o + np * kHeadDim + 4 * lane);
-        }
-        if (lb != -INFINITY) {
+        const int jn = j + kMergeStages - 1;
+        if (jn < n_here) issue(pair_of(jn), jn % kMergeStages);
+        cp_async_commit();
+        cp_async_wait<kMergeStages - 1>();  // this thread's copies of block j have landed
+        const int st = j % kMergeStages;
+        const float lc = lring[st * kMergeThreads + tid];
+        if (lc != -INFINITY) {
           if (L == -INFINITY) {
-            O = cur;
-            L = lb;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) O[m] = ring[(st * 8 + m) * kMergeThreads + tid];
+            L = lc;
           } else {
             float Lp, alpha, beta;
-            fold_coeffs(L, lb, Lp, alpha, beta);
-            O.x = fold_elem(O.x, cur.x, alpha, beta);
-            O.y = fold_elem(O.y, cur.y, alpha, beta);
-            O.z = fold_elem(O.z, cur.z, alpha, beta);
-            O.w = fold_elem(O.w, cur.w, alpha, beta);
+            fold_coeffs(L, lc, Lp, alpha, beta);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const float4 c = ring[(st * 8 + m) * kMergeThreads + tid];
+              O[m].x = fold_elem(O[m].x, c.x, alpha, beta);
+              O[m].y = fold_elem(O[m].y, c.y, alpha, beta);
+              O[m].z = fold_elem(O[m].z, c.z, alpha, beta);
+              O[m].w = fold_elem(O[m].w, c.w, alpha, beta);
+            }
             L = Lp;
           }
         }
-        cur = nxt;
       }
+      cp_async_wait<0>();  // no copy outlives the group (the ring is reused)
     }
+    if (!hv) continue;
     if (bad) {
       if (lane == 0) report_error(p.err, kErrMissingBlock, 0x503);
-      O = make_float4(NAN, NAN, NAN, NAN);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) O[m] = make_float4(NAN, NAN, NAN, NAN);
       L = NAN;
     }
     const int64_t row = tok * p.hq + h;
-    if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + row * kHeadDim + 4 * lane) = O;
-    if (p.out_bf16)
-      *reinterpret_cast<uint2*>(p.out_bf16 + row * kHeadDim + 4 * lane) =
-          make_uint2(pack_bf16x2(O.x, O.y), pack_bf16x2(O.z, O.w));
-    if (p.lse && lane == 0) p.lse[row] = L;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(p.out_f32 + row * kHeadDim) + qq;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) dst[4 * m] = O[m];
+    }
+    if (p.out_bf16) {
+      uint2* dst = reinterpret_cast<uint2*>(p.out_bf16 + row * kHeadDim) + qq;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) dst[4 * m] = make_uint2(pack_bf16x2(O[m].x, O[m].y), pack_bf16x2(O[m].z, O[m].w));
+    }
+    if (p.lse && qq == 0) p.lse[row] = L;
   }
 }
 
@@ -140,12 +212,18 @@ cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream)
   rlk_merge_index_kernel<<<1, 1024, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t warps = p.total_rows * p.hq;
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(rlk_merge_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t warps = p.total_rows * ((p.hq + kMergeHeadsPerWarp - 1) / kMergeHeadsPerWarp);
   int64_t blocks = (warps + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // 8 CTAs of 256 threads per SM
+  const int64_t cap = static_cast<int64_t>(num_sms) * 2;  // 2 CTAs of 256 threads per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  rlk_merge_fold_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  rlk_merge_fold_kernel<<<static_cast<int>(blocks), kMergeThreads, kMergeSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
