@@ -102,9 +102,9 @@ struct BwdLayout {
   static constexpr int kResOff = 0;                 // resident pair (K_j,V_j) or (Q_i,dO_i)
   static constexpr int kStreamOff = 2 * kTile;      // 2 stages x streamed pair
   static constexpr int kStages = 2;
-  // per-warp copies of a step's column statistics: [buf 2][warp 4][lse2, Delta][128] floats
+  // per-warp copies of a step's column statistics: [buf 2][warp 8][lse2, Delta][64] floats
   static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;
-  static constexpr int kBarOff = kVecOff + 2 * 4 * 2 * 128 * 4;
+  static constexpr int kBarOff = kVecOff + 2 * 8 * 2 * 64 * 4;
   // barriers
   static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 7,
                        kAccFull = 8, kAccEmpty = 9, kNumBars = 10;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars[L::kStEmpty + s], 1);
     }
     mbar_init(&bars[L::kSFull], 1);
-    mbar_init(&bars[L::kPFull], 128);
+    mbar_init(&bars[L::kPFull], 256);  // both column halves
     mbar_init(&bars[L::kAccFull], 1);
     mbar_init(&bars[L::kAccEmpty], 128);
     *abort = 0;
@@ -314,11 +314,16 @@ __global__ void __launch_bounds__(384, 1)
       if (fail) break;
       ++acc_it;
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ P / dS
-    const int r = tid - 128;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ P / dS (+ epilogue)
+    // warps 4-7 take columns 0-63 of each step, warps 0-3 columns 64-127
+    // (P and dS are elementwise given the column or row statistics, so the
+    // halves need no exchange); warps 0-3 also write the item's results.
+    const int half = warp < 4 ? 1 : 0;
+    const int r = tid - (half ? 0 : 128);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t s_it = 0;
+    const int cbase = 64 * half;  // first column of this half
+    uint32_t s_it = 0, acc_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
       const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
@@ -343,21 +348,21 @@ __global__ void __launch_bounds__(384, 1)
       const int key_pos = (KIND == 0) ? it.block * 128 + r : 0;
       bool fail = false;
       for (int t = 0; t < nsteps; ++t) {
-        float* vb = vecs + ((s_it & 1) * 4 + (warp & 3)) * 256;
+        float* vb = vecs + ((s_it & 1) * 8 + warp) * 128;  // [lse2 64][Delta 64] of this half
         int col0;  // position of column 0 of this step
         if (KIND == 0) {
           const int i = it.block + t / p.group;
           const int h = it.head * p.group + t % p.group;
           col0 = i * 128;
-          // column statistics of the step's query block: each warp stages its
-          // own copy (warp-local sync only)
+          // column statistics of this half: each warp stages its own copy
+          // (warp-local sync only)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 2; ++u) {
             const int col = lane + 32 * u;
-            const int qp = col0 + col;
+            const int qp = col0 + cbase + col;
             const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
             vb[col] = qp < len ? __fmul_rn(p.lse_t[idx], kLog2e) : 0.f;
-            vb[128 + col] = qp < len ? p.delta_t[idx] : 0.f;
+            vb[64 + col] = qp < len ? p.delta_t[idx] : 0.f;
           }
           __syncwarp();
         } else {
@@ -367,46 +372,53 @@ __global__ void __launch_bounds__(384, 1)
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
+          const int colc = cbase + 32 * c;
           uint32_t sr[32], dr[32];
-          tmem_ld32(tm_s + lane_off + 32 * c, sr);
-          tmem_ld32(tm_dp + lane_off + 32 * c, dr);
+          tmem_ld32(tm_s + lane_off + colc, sr);
+          tmem_ld32(tm_dp + lane_off + colc, dr);
           tmem_ld_wait(sr);
           tmem_ld_wait(dr);
           uint32_t pw[32], dw[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dsv[2];
+          for (int e = 0; e < 32; e += 4) {
+            float4 l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
+            float4 d4 = make_float4(row_delta, row_delta, row_delta, row_delta);
+            if (KIND == 0) {
+              l4 = *reinterpret_cast<const float4*>(vb + 32 * c + e);
+              d4 = *reinterpret_cast<const float4*>(vb + 64 + 32 * c + e);
+            }
+            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int col = 32 * c + e + u;
+            for (int u = 0; u < 4; ++u) {
+              const int col = colc + e + u;
               bool ok;
-              float lse2, delta;
               if (KIND == 0) {
                 const int qp = col0 + col;
                 ok = key_pos < len && qp < len && qp >= key_pos;
-                lse2 = vb[col];
-                delta = vb[128 + col];
               } else {
                 const int kp = col0 + col;
                 ok = row_ok && kp <= row_pos;
-                lse2 = row_lse2;
-                delta = row_delta;
               }
-              p_and_ds(__uint_as_float(sr[e + u]), __uint_as_float(dr[e + u]), lse2, delta, ok, p.scale_log2,
+              p_and_ds(__uint_as_float(sr[e + u]), __uint_as_float(dr[e + u]), la[u], da[u], ok, p.scale_log2,
                        pv[u], dsv[u]);
             }
-            const int slot = (e >> 4) * 16 + ((e & 15) >> 1);
-            uint32_t hi, lo;
-            split_pair(pv[0], pv[1], hi, lo);
-            pw[slot] = hi;
-            pw[slot + 8] = lo;
-            split_pair(dsv[0], dsv[1], hi, lo);
-            dw[slot] = hi;
-            dw[slot + 8] = lo;
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const int slot = ((e + u) >> 4) * 16 + (((e + u) & 15) >> 1);
+              uint32_t hi, lo;
+              split_pair(pv[u], pv[u + 1], hi, lo);
+              pw[slot] = hi;
+              pw[slot + 8] = lo;
+              split_pair(dsv[u], dsv[u + 1], hi, lo);
+              dw[slot] = hi;
+              dw[slot + 8] = lo;
+            }
           }
-          tmem_st32(tm_s + lane_off + 32 * c, pw);
-          tmem_st32(tm_dp + lane_off + 32 * c, dw);
+          tmem_st32(tm_s + lane_off + colc, pw);
+          tmem_st32(tm_dp + lane_off + colc, dw);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -414,20 +426,8 @@ __global__ void __launch_bounds__(384, 1)
         ++s_it;
       }
       if (fail) break;
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ epilogue
-    const int r = tid;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t acc_it = 0;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
-      const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
-      const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
-      if (item >= p.num_items) continue;
-      const BwdItem it = p.items[item];
-      int len, nsteps;
-      item_steps(it, len, nsteps);
-      const int tok0 = p.cu[it.seq];
+      if (!half) continue;
+      // ---------------------------------------------------------- epilogue
       bool w = mbar_wait(&bars[L::kAccFull], acc_it & 1, abort, p.err, 0x631);
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
