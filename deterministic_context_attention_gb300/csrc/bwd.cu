@@ -120,16 +120,9 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int k) {  // MN-major 
   return sdesc_sw128(tile + k * 16 * 128, BwdLayout::kHalf, 1024);
 }
 
-// Per-element backward arithmetic shared by both kernels:
-//   p  = 2^(s * scale_log2 - lse * log2 e)    (0 where masked)
-//   ds = p * (dp - Delta)                      (0 where masked)
-__device__ __forceinline__ void p_and_ds(float s, float dp, float lse2, float delta, bool ok, float scale_log2,
-                                         float& p, float& ds) {
-  const float x = __fsub_rn(__fmul_rn(s, scale_log2), lse2);
-  p = ok ? ex2_hw(x) : 0.0f;
-  ds = ok ? __fmul_rn(p, __fsub_rn(dp, delta)) : 0.0f;
-}
-
+// Per-element backward arithmetic of both kernels (one rounding per step):
+//   p  = 2^fma(s, scale_log2, -lse log2 e)     (0 where masked)
+//   ds = p * (dp - Delta)
 // KIND 0: dK/dV (rows = keys of block j, columns = query rows);
 // KIND 1: dQ    (rows = query rows,       columns = keys of block j).
 template <int KIND>
@@ -371,6 +364,13 @@ __global__ void __launch_bounds__(384, 1)
         bool w = mbar_wait(&bars[L::kSFull], s_it & 1, abort, p.err, 0x621);
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
+        // every element of this warp's half is visible: no per-element mask
+        bool full;
+        if (KIND == 0)
+          full = __all_sync(0xffffffffu, key_pos < len && col0 + cbase + 63 < len && col0 + cbase >= key_pos);
+        else
+          full = __all_sync(0xffffffffu, row_ok && col0 + cbase + 63 <= row_pos);
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           const int colc = cbase + 32 * c;
@@ -390,29 +390,34 @@ __global__ void __launch_bounds__(384, 1)
             }
             const float la[4] = {l4.x, l4.y, l4.z, l4.w};
             const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = colc + e + u;
-              bool ok;
-              if (KIND == 0) {
-                const int qp = col0 + col;
-                ok = key_pos < len && qp < len && qp >= key_pos;
-              } else {
-                const int kp = col0 + col;
-                ok = row_ok && kp <= row_pos;
-              }
-              p_and_ds(__uint_as_float(sr[e + u]), __uint_as_float(dr[e + u]), la[u], da[u], ok, p.scale_log2,
-                       pv[u], dsv[u]);
-            }
 #pragma unroll
             for (int u = 0; u < 4; u += 2) {
+              // p = 2^(s scale_log2 - lse log2 e), ds = p (dp - Delta); a masked
+              // element has p = 0, hence ds = 0
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2,
+                                     make_float2(-la[u], -la[u + 1]));
+              float2 pp = make_float2(ex2_hw(x.x), ex2_hw(x.y));
+              if (!full) {
+                const int cA = colc + e + u, cB = cA + 1;
+                bool okA, okB;
+                if (KIND == 0) {
+                  okA = key_pos < len && col0 + cA < len && col0 + cA >= key_pos;
+                  okB = key_pos < len && col0 + cB < len && col0 + cB >= key_pos;
+                } else {
+                  okA = row_ok && col0 + cA <= row_pos;
+                  okB = row_ok && col0 + cB <= row_pos;
+                }
+                pp.x = okA ? pp.x : 0.0f;
+                pp.y = okB ? pp.y : 0.0f;
+              }
+              const float2 ds = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                                                make_float2(da[u], da[u + 1])));
               const int slot = ((e + u) >> 4) * 16 + (((e + u) & 15) >> 1);
               uint32_t hi, lo;
-              split_pair(pv[u], pv[u + 1], hi, lo);
+              split_pair2(pp, hi, lo);
               pw[slot] = hi;
               pw[slot + 8] = lo;
-              split_pair(dsv[u], dsv[u + 1], hi, lo);
+              split_pair2(ds, hi, lo);
               dw[slot] = hi;
               dw[slot + 8] = lo;
             }
