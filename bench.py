@@ -341,6 +341,7 @@ def measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args):
     del kp, vp
     torch.cuda.empty_cache()
     res["backward"] = measure_backward(torch, rlk, dv, peaks, flush, stream, args)
+    res["chunked"] = measure_chunked(torch, rlk, dv, peaks, flush, stream, args)
     return res
 
 
@@ -376,6 +377,41 @@ def measure_backward(torch, rlk, dv, peaks, flush, stream, args):
     return {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": flops,
             "frac": round(tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
             "workload": "2 x 4096 causal, Hq32/Hkv8/D128, dout ~ N(0,1) bf16; preprocess + dK/dV + dQ kernels"}
+
+
+def measure_chunked(torch, rlk, dv, peaks, flush, stream, args, chunk=2048):
+    """Chunked-prefill replay (TP=2 shard: 2 x 8192 tokens, Hq16/Hkv4/D128):
+    each sequence's queries in chunks of `chunk` tokens against the growing
+    KV cache, one launch per chunk; algorithmic TFLOP/s of the causal
+    attention the replay computes (the same flops as the full prefill)."""
+    cfg = dict(synth.CFG_CHUNKED)
+    prob = synth.prefill_problem(**cfg)
+    q, k, v = dv.bf16_to_device(prob.q), dv.bf16_to_device(prob.k), dv.bf16_to_device(prob.v)
+    rows = q.shape[0]
+    out = torch.empty((rows, prob.hq, 128), dtype=torch.float32, device="cuda")
+    outb = torch.empty((rows, prob.hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, prob.hq), dtype=torch.float32, device="cuda")
+    p1 = rlk.make_params(1, prob.hq, prob.hkv, prob.block, 1, rlk.ZIGZAG, prob.scale)
+    calls = []
+    for s_ in range(len(prob.cu_q) - 1):
+        q0, q1, k0 = int(prob.cu_q[s_]), int(prob.cu_q[s_ + 1]), int(prob.cu_k[s_])
+        for c0 in range(0, q1 - q0, chunk):
+            c1 = min(c0 + chunk, q1 - q0)
+            calls.append((q[q0 + c0:q0 + c1], k[k0:k0 + c1], v[k0:k0 + c1], [0, c1 - c0], [0, c1],
+                          out[q0 + c0:q0 + c1], outb[q0 + c0:q0 + c1], lse[q0 + c0:q0 + c1]))
+
+    def step():
+        for (qq, kk, vv, cq, ck, oo, ob, ll) in calls:
+            rlk.rlk_attn_prefill(p1, qq, kk, vv, cq, ck, -1, oo, ob, ll, stream=stream)
+
+    t = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    ms = float(np.mean(t))
+    flops = synth.prefill_flops(prob.cu_q, prob.cu_k, prob.hq, prob.d)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": flops, "chunk": chunk,
+            "launches_per_step": len(calls), "frac": round(tf / peaks["bf16_tflops"], 4),
+            "workload": "2 x 8192 (TP=2 shard, Hq16/Hkv4/D128), queries in chunks against the growing cache"}
 
 
 def cpu_baseline(seconds_target):
