@@ -11,7 +11,13 @@ table) in this library's own schema ``rlk_attn_cp_drift/v1``:
   rounding; nonzero by construction);
 * ``merge_order_probe`` -- max |merge(reversed arrival) - merge(sorted)|;
   strict 0.0;
-* ``backward`` -- max |dQ/dK/dV(CP=r) - dQ/dK/dV(CP=1)|; strict 0.0.
+* ``backward`` -- max |dQ/dK/dV(CP=r) - dQ/dK/dV(CP=1)|; strict 0.0;
+* ``drift.dlogp`` -- the active-token log-probability drift: each output row
+  (all heads, FP32) is projected through a seeded synthetic FP32 lm_head
+  (the pages' dlogp check, "[WS2][Attention] H100 validation and
+  reproduction guide", Status: Out/LSE/dlogp max abs 0.0) and the
+  log-probability of a seeded token per row is compared with the CP=1
+  fused path's; strict 0.0.
 
 Each case records its topology, the block size, the block manifest hash and
 per-logical-rank counts; the root records ``merge_order`` =
@@ -30,6 +36,21 @@ import numpy as np
 from . import synth
 
 SCHEMA = "rlk_attn_cp_drift/v1"
+
+
+def _dlogp(out, vocab=512, seed=7):
+    """Log-probability of a seeded token per row after a seeded FP32 lm_head
+    (N(0, 1/width)) over the row's outputs of all heads; FP32 throughout,
+    the same numpy arithmetic for every path compared."""
+    rows = out.shape[0]
+    x = np.ascontiguousarray(out.reshape(rows, -1), dtype=np.float32)
+    rng = np.random.default_rng([seed, x.shape[1], vocab])
+    w = (rng.standard_normal((x.shape[1], vocab)) / np.sqrt(x.shape[1])).astype(np.float32)
+    tok = rng.integers(0, vocab, size=rows)
+    logits = x @ w
+    m = logits.max(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(logits - m).sum(axis=1, dtype=np.float32), dtype=np.float32)
+    return logits[np.arange(rows), tok] - lse
 
 
 def _maxabs(a, b):
@@ -89,6 +110,7 @@ def drift_report(lens=(4096, 3000, 1024, 777), hq=32, hkv=8, block=128, seed=1, 
         return (o.cpu().numpy(), ob.float().cpu().numpy(), l.cpu().numpy()), per_rank
 
     base = fused(1, rlk.ZIGZAG, [-1])
+    base_dlogp = _dlogp(base[0])
     root = {"schema_version": SCHEMA, "core_id": rlk.rlk_attn_core_id(),
             "merge_order": "global_block_index", "downcast_at": "final_write",
             "target": {"heads_q": hq, "heads_kv": hkv, "head_dim": 128, "kv_block": block,
@@ -111,6 +133,7 @@ def drift_report(lens=(4096, 3000, 1024, 777), hq=32, hkv=8, block=128, seed=1, 
                 "block_manifest_hash": f"{rlk.rlk_attn_block_manifest_hash(p, prob.cu_q, prob.cu_k):016x}",
                 "drift": {"cp_merge_fp32": max(_maxabs(f[0], base[0]), _maxabs(sm[0], base[0])),
                           "lse": max(_maxabs(f[2], base[2]), _maxabs(sm[2], base[2])),
+                          "dlogp": max(_maxabs(_dlogp(f[0]), base_dlogp), _maxabs(_dlogp(sm[0]), base_dlogp)),
                           "dtype_path_vs_fp32": _maxabs(f[1], f[0])},
                 "per_logical_cp_rank": per_rank})
     # chunked replay: each sequence's queries in chunks against the growing cache
@@ -124,9 +147,11 @@ def drift_report(lens=(4096, 3000, 1024, 777), hq=32, hkv=8, block=128, seed=1, 
                 rlk.rlk_attn_prefill(p, q[q0 + c0:q0 + c1], k[k0:k0 + c1], v[k0:k0 + c1], [0, c1 - c0], [0, c1], -1,
                                      o[q0 + c0:q0 + c1], ob[q0 + c0:q0 + c1], l[q0 + c0:q0 + c1])
         rlk.rlk_attn_check_device_error()
+        on = o.cpu().numpy()
         root["cases"].append({"mode": "chunked_prefill", "chunk": chunk, "topology": {"tp": 1, "cp": 1},
-                              "drift": {"cp_merge_fp32": _maxabs(o.cpu().numpy(), base[0]),
-                                        "lse": _maxabs(l.cpu().numpy(), base[2])}})
+                              "drift": {"cp_merge_fp32": _maxabs(on, base[0]),
+                                        "lse": _maxabs(l.cpu().numpy(), base[2]),
+                                        "dlogp": _maxabs(_dlogp(on), base_dlogp)}})
     # backward drift across logical CP sizes
     bprob = synth.prefill_problem(list(backward_lens), hq=hq, hkv=hkv, block=128, seed=seed + 3)
     bq, bk, bv = dv.bf16_to_device(bprob.q), dv.bf16_to_device(bprob.k), dv.bf16_to_device(bprob.v)
@@ -155,6 +180,7 @@ def drift_report(lens=(4096, 3000, 1024, 777), hq=32, hkv=8, block=128, seed=1, 
                               "backward": {n: _maxabs(a, b) for n, a, b in zip(("dq", "dk", "dv"), gc, g1)}})
     strict = [c["drift"]["cp_merge_fp32"] for c in root["cases"] if "drift" in c]
     strict += [c["drift"]["lse"] for c in root["cases"] if "drift" in c]
+    strict += [c["drift"]["dlogp"] for c in root["cases"] if "drift" in c]
     strict += [x for c in root["cases"] if "backward" in c for x in c["backward"].values()]
     strict += list(root["merge_order_probe"].values())
     root["strict_max_abs"] = max(strict) if strict else 0.0
