@@ -30,7 +30,7 @@ STATUS_NAMES = {
     3: "RLK_ERR_WORKSPACE_TOO_SMALL", 4: "RLK_ERR_DUPLICATE_BLOCK", 5: "RLK_ERR_MISSING_BLOCK",
     6: "RLK_ERR_DEVICE_TIMEOUT", 7: "RLK_ERR_CUDA", 8: "RLK_ERR_BAD_PAGE", 9: "RLK_ERR_BAD_STATE_TABLE",
 }
-RLK_OP_MERGE, RLK_OP_BACKWARD = 1, 2
+RLK_OP_MERGE, RLK_OP_BACKWARD, RLK_OP_DECODE_SPLIT = 1, 2, 3
 CONTIGUOUS, ZIGZAG = 0, 1
 
 
@@ -89,6 +89,7 @@ def load():
             "rlk_attn_merge_states_noalloc": [PP, P, P, P, i64, P, P, P, P, P, P],
             "rlk_attn_prefill": [PP, P, P, P, P, P, i32, P, P, P, P],
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
+            "rlk_attn_decode_paged_splitk": [PP, P, P, P, i32, i32, P, i32, P, i32, P, P, P, P, sz, P],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
             "rlk_attn_workspace_size": [PP, i32, P, P],
             "rlk_attn_check_device_error": [P],
@@ -169,7 +170,9 @@ def rlk_attn_block_manifest_hash(params, cu_seqlens_q, cu_seqlens_k) -> int:
 
 
 def rlk_attn_workspace_size(params, op, cu_seqlens_q, cu_seqlens_k=None) -> int:
-    cq = _i32_host(cu_seqlens_q)
+    """RLK_OP_DECODE_SPLIT: pass the decode context lengths as cu_seqlens_k
+    (cu_seqlens_q may be None)."""
+    cq = None if cu_seqlens_q is None else _i32_host(cu_seqlens_q)
     ck = _i32_host(cu_seqlens_k if cu_seqlens_k is not None else cu_seqlens_q)
     return int(load().rlk_attn_workspace_size(ctypes.byref(params), int(op), _ptr(cq), _ptr(ck)))
 
@@ -220,6 +223,18 @@ def rlk_attn_decode_paged(params, q, k_pool, v_pool, n_pages, page_size, page_ta
                                         int(n_pages), int(page_size), _ptr(page_table), int(max_pages),
                                         _ptr(sl), _ptr(out_f32), _ptr(out_bf16), _ptr(lse), _stream(stream)),
            "rlk_attn_decode_paged")
+
+
+def rlk_attn_decode_paged_splitk(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                                 split_k, out_f32, out_bf16, lse, workspace, workspace_bytes=None, stream=None):
+    sl = _i32_host(seqlens)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().rlk_attn_decode_paged_splitk(ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                               int(n_pages), int(page_size), _ptr(page_table), int(max_pages),
+                                               _ptr(sl), int(split_k), _ptr(out_f32), _ptr(out_bf16), _ptr(lse),
+                                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "rlk_attn_decode_paged_splitk")
 
 
 def rlk_attn_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,

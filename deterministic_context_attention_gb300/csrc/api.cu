@@ -23,6 +23,7 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensor
                        const CUtensorMap& tv, int grid, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream);
 bool decode_transposed_supported(const FwdParams& p);
+cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t stream);
 cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
@@ -507,9 +508,117 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
   return ok();
 }
 
+
+rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                        const void* v_pool, int32_t n_pages, int32_t page_size,
+                                        const int32_t* page_table, int32_t max_pages,
+                                        const int32_t* seqlens, int32_t split_k, float* out_f32,
+                                        void* out_bf16, float* lse, void* workspace,
+                                        size_t workspace_bytes, rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if (split_k < 1 || split_k > 64) return fail(RLK_ERR_INVALID_ARGUMENT, "split_k %d not in 1..64", split_k);
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out_f32 && !aligned16(out_f32)) ||
+      (out_bf16 && !aligned16(out_bf16)) || !aligned16(workspace))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const int B = params->kv_block_size;
+  const int group = params->num_q_heads / params->num_kv_heads;
+  if (B != 128 || group > rlk::kDecodeMaxGroup)
+    return fail(RLK_ERR_UNSUPPORTED, "split decode needs kv_block_size 128 and at most %d query heads per KV head",
+                rlk::kDecodeMaxGroup);
+  if (page_size < 8 || page_size > B || B % page_size)
+    return fail(RLK_ERR_UNSUPPORTED, "page_size %d must be >= 8 and divide kv_block_size %d", page_size, B);
+  if (n_pages < 1 || max_pages < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "n_pages / max_pages < 1");
+  if (static_cast<int64_t>(n_pages + 1) * page_size >= (int64_t(1) << 31))
+    return fail(RLK_ERR_UNSUPPORTED, "page pool too large for 32-bit token coordinates");
+  for (int s = 0; s < params->num_seqs; ++s)
+    if (seqlens[s] < 1 || static_cast<int64_t>(seqlens[s]) > static_cast<int64_t>(max_pages) * page_size)
+      return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: context length %d not in 1..max_pages*page_size", s,
+                  seqlens[s]);
+  const size_t need = rlk_attn_workspace_size(params, RLK_OP_DECODE_SPLIT, nullptr, seqlens);
+  if (!workspace || workspace_bytes < need)
+    return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  // state table: pair (block_base[s] + b) * Hq + head; o_b FP32 [pair][128], then lse_b [pair]
+  std::vector<int32_t> block_base(params->num_seqs + 1, 0);
+  for (int s = 0; s < params->num_seqs; ++s) block_base[s + 1] = block_base[s] + (seqlens[s] + B - 1) / B;
+  const int64_t pairs = static_cast<int64_t>(block_base[params->num_seqs]) * params->num_q_heads;
+  std::vector<std::pair<int, rlk::FwdTile>> costed;
+  for (int s = 0; s < params->num_seqs; ++s) {
+    const int nb = (seqlens[s] + B - 1) / B;
+    for (int g = 0; g < params->num_kv_heads; ++g)
+      for (int r = 0; r < split_k; ++r) {
+        const int b0 = static_cast<int>(static_cast<int64_t>(r) * nb / split_k);
+        const int b1 = static_cast<int>(static_cast<int64_t>(r + 1) * nb / split_k);
+        if (b1 <= b0) continue;
+        rlk::FwdTile t;
+        std::memset(&t, 0, sizeof(t));
+        t.seq = s;
+        t.row_begin = g;
+        t.row_count = group;
+        t.block = b0;
+        t.slab_row_count = b1 - b0;
+        costed.push_back({b1 - b0, t});
+      }
+  }
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
+                     return a.first > b.first;
+                   });
+  CUtensorMap mq, mk, mv;
+  // one query head per TMA box: the kernel places each head in its own operand row
+  if ((st = make_map(&mq, q, params->num_q_heads, params->num_seqs, 1, 1))) return st;
+  if ((st = make_map(&mk, k_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))
+    return st;
+  if ((st = make_map(&mv, v_pool, params->num_kv_heads, static_cast<uint64_t>(n_pages) * page_size, 1, page_size)))
+    return st;
+  auto fp = std::make_unique<rlk::FwdParams>();
+  base_fwd(fp.get(), params, dev, rlk::kModeDecode);
+  for (int s = 0; s < params->num_seqs; ++s) {
+    fp->cu_k[s] = seqlens[s];
+    fp->cu_q[s] = block_base[s];
+  }
+  fp->state_o = static_cast<float*>(workspace);
+  fp->state_lse = static_cast<float*>(workspace) + pairs * rlk::kHeadDim;
+  fp->page_table = page_table;
+  fp->max_pages = max_pages;
+  fp->page_size = page_size;
+  fp->n_pages = n_pages;
+  for (size_t t0 = 0; t0 < costed.size(); t0 += rlk::kMaxTilesPerLaunch) {
+    const size_t n = std::min(costed.size() - t0, static_cast<size_t>(rlk::kMaxTilesPerLaunch));
+    for (size_t i = 0; i < n; ++i) fp->tiles[i] = costed[t0 + i].second;
+    fp->num_tiles = static_cast<int32_t>(n);
+    fp->num_items = static_cast<int32_t>(n);
+    const int grid = std::min(fp->num_items, dev->num_sms);
+    cudaError_t e = rlk::launch_decode(*fp, mq, mk, mv, grid, stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "split decode launch: %s", cudaGetErrorString(e));
+  }
+  // fold: num_tiles carries the sequence count for the merge
+  fp->num_tiles = params->num_seqs;
+  fp->out_f32 = out_f32;
+  fp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  fp->lse = lse;
+  cudaError_t e = rlk::launch_decode_merge(*fp, dev->num_sms, stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "split decode merge launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const int32_t* cu_seqlens_q,
                                const int32_t* cu_seqlens_k) {
   if (check_params(params) != RLK_OK) return 0;
+  if (op == RLK_OP_DECODE_SPLIT) {
+    if (!cu_seqlens_k) return 0;
+    int64_t blocks = 0;
+    for (int s = 0; s < params->num_seqs; ++s) {
+      if (cu_seqlens_k[s] < 1) return 0;
+      blocks += (cu_seqlens_k[s] + params->kv_block_size - 1) / params->kv_block_size;
+    }
+    const int64_t pairs = blocks * params->num_q_heads;
+    return static_cast<size_t>((pairs * (rlk::kHeadDim + 1) * 4 + 255) / 256 * 256);
+  }
   if (op == RLK_OP_MERGE) {
     if (check_cu(params, cu_seqlens_q, cu_seqlens_k) != RLK_OK) return 0;
     int max_blocks = 1;

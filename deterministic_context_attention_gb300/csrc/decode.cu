@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 
 #include "numerics.cuh"
@@ -94,6 +95,30 @@ __device__ __forceinline__ int dec_snake_item(int round) {
 }
 
 __device__ __forceinline__ float bf16_bits_as_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+// One item: the query heads of KV head g of sequence seq against the global
+// blocks [b0, b0 + nb).  Plain decode: all of the sequence's blocks, folded on
+// chip.  Split decode (state_o set): a fixed range of them, whose block states
+// are written to the state table at pair (cu_q[seq] + b) * hq + head for the
+// merge to fold.
+struct DecItem {
+  int seq, g, kv_len, b0, nb;
+};
+__device__ __forceinline__ DecItem dec_item(const FwdParams& p, int item) {
+  const FwdTile& t = p.tiles[item];
+  DecItem d;
+  d.seq = t.seq;
+  d.g = t.row_begin;
+  d.kv_len = p.cu_k[t.seq];
+  if (p.state_o) {
+    d.b0 = t.block;
+    d.nb = t.slab_row_count;
+  } else {
+    d.b0 = 0;
+    d.nb = (d.kv_len + DecLayout::B - 1) / DecLayout::B;
+  }
+  return d;
+}
 
 // Row maximum of the 32 lanes of a warp (exact; every lane receives it).
 __device__ __forceinline__ float warp_max(float v) {
@@ -194,9 +219,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
-      const FwdTile& t = p.tiles[item];
-      const int seq = t.seq, g = t.row_begin, kv_len = p.cu_k[seq];
-      const int nb = (kv_len + B - 1) / B;
+      const DecItem di = dec_item(p, item);
+      const int seq = di.seq, g = di.g, kv_len = di.kv_len, nb = di.nb;
       if (!is_v) {
         bool ok = mbar_wait(&bars[L::kQEmpty], (q_it & 1) ^ 1, abort, p.err, 0x501);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -215,7 +239,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const int32_t* prow = p.page_table + static_cast<int64_t>(seq) * p.max_pages;
       int cached = -1;  // a new sequence's page ids
       bool fail = false;
-      for (int b = 0; b < nb; ++b) {
+      for (int j = 0; j < nb; ++j) {
+        const int b = di.b0 + j;  // global block
         const uint32_t stage = it_n % S;
         bool ok = mbar_wait(empty_b + stage, ((it_n / S) & 1) ^ 1, abort, p.err, is_v ? 0x503 : 0x502);
         if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
@@ -258,9 +283,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
-      const FwdTile& t = p.tiles[item];
-      const int kv_len = p.cu_k[t.seq];
-      const int nb = (kv_len + B - 1) / B;
+      const DecItem di = dec_item(p, item);
+      const int kv_len = di.kv_len, nb = di.nb;
       bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x601);
       if (!__all_sync(0xffffffffu, ok)) break;
       ++q_it;
@@ -306,7 +330,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         uint8_t* vd = v_base + vstage * L::kKVBytes;
         // V rows past the context may hold stale or non-finite data; P is
         // exactly 0 there, so zero them (0 * NaN = NaN)
-        const int valid = min(B, kv_len - j * B);
+        const int valid = min(B, kv_len - (di.b0 + j) * B);
         if (valid < B) {
           const int nrow = B - valid;
           for (int i = lane; i < nrow * 16; i += 32) {
@@ -360,8 +384,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
-      const int kv_len = p.cu_k[p.tiles[item].seq];
-      const int nb = (kv_len + B - 1) / B;
+      const DecItem di = dec_item(p, item);
+      const int kv_len = di.kv_len, nb = di.nb;
       bool fail = false;
       for (int j = 0; j < nb; ++j, ++s_it) {
         if (static_cast<int>(s_it & 1) != grp) continue;  // the other group's block
@@ -374,7 +398,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         tmem_ld_wait(raw);
         tc_fence_before();
         mbar_arrive(&bars[L::kSEmpty + slot]);
-        const bool vis = j * B + t < kv_len;
+        const bool vis = (di.b0 + j) * B + t < kv_len;
         const int rb = static_cast<int>(sy_it & 1);
         const uint32_t sy_par = (sy_it >> 1) & 1;
         // block maximum of every query head over the visible keys (exact)
@@ -448,10 +472,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
-      const FwdTile& tl = p.tiles[item];
-      const int seq = tl.seq, g = tl.row_begin;
-      const int kv_len = p.cu_k[seq];
-      const int nb = (kv_len + B - 1) / B;
+      const DecItem di = dec_item(p, item);
+      const int seq = di.seq, g = di.g, nb = di.nb;
+      const bool split = p.state_o != nullptr;
       float O[MG];
 #pragma unroll
       for (int q = 0; q < MG; ++q) O[q] = 0.0f;
@@ -471,12 +494,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
           const float2 st = stats[sslot * kDecodeMaxGroup + lane];
           lb = st.x;
           rc = st.y;
-          if (j > 0) fold_coeffs(Lrun, lb, Lp, al, be);
+          if (j > 0 && !split) fold_coeffs(Lrun, lb, Lp, al, be);
         }
         tmem_ld_wait(raw);
         tc_fence_before();
         mbar_arrive(&bars[L::kOEmpty + oslot]);
-        // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha)
+        // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha), or (split) the
+        // block state written out
+        const int64_t pair_b = static_cast<int64_t>(p.cu_q[seq] + di.b0 + j) * p.hq + g * G;
 #pragma unroll
         for (int q = 0; q < MG; ++q) {
           const float rq = __shfl_sync(0xffffffffu, rc, q);
@@ -484,13 +509,19 @@ __global__ void __launch_bounds__(kDThreads, 1)
           const float bq = __shfl_sync(0xffffffffu, be, q);
           if (q < G) {
             const float oa = __fmul_rn(__uint_as_float(raw[q]), rq);
-            O[q] = (j == 0) ? oa : __fmaf_rn(oa, bq, __fmul_rn(O[q], aq));
+            if (split) p.state_o[(pair_b + q) * kHeadDim + d] = oa;
+            else O[q] = (j == 0) ? oa : __fmaf_rn(oa, bq, __fmul_rn(O[q], aq));
           }
         }
-        if (lane < G) Lrun = (j == 0) ? lb : Lp;
+        if (split) {
+          if (warp == 0 && lane < G) p.state_lse[pair_b + lane] = lb;
+        } else if (lane < G) {
+          Lrun = (j == 0) ? lb : Lp;
+        }
         ++o_it;
       }
       if (fail) break;
+      if (split) continue;
       // epilogue: O and L are final
 #pragma unroll
       for (int q = 0; q < MG; ++q) {
@@ -533,11 +564,68 @@ cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& tq, const CUt
   return cudaGetLastError();
 }
 
+// Split decode, second step: one warp per (sequence, query head) folds the
+// sequence's block states in ascending global block order with the canonical
+// fold -- the same operations the single-pass kernel applies on chip, so the
+// result is the same bit for bit.  Lane l holds elements 4l..4l+3; the next
+// two states are in flight while one folds.
+__global__ void __launch_bounds__(256) rlk_decode_merge_kernel(const __grid_constant__ FwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t total = static_cast<int64_t>(p.num_tiles) * p.hq;  // num_tiles: sequences
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+       w += warps) {
+    const int seq = static_cast<int>(w / p.hq);
+    const int h = static_cast<int>(w - static_cast<int64_t>(seq) * p.hq);
+    const int nb = (p.cu_k[seq] + DecLayout::B - 1) / DecLayout::B;
+    const int64_t pair0 = static_cast<int64_t>(p.cu_q[seq]) * p.hq + h;
+    auto load = [&](int b, float4& o, float& lb) {
+      if (b < nb) {
+        const int64_t pr = pair0 + static_cast<int64_t>(b) * p.hq;
+        o = reinterpret_cast<const float4*>(p.state_o + pr * kHeadDim)[lane];
+        lb = p.state_lse[pr];
+      }
+    };
+    float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0, c2 = c0;
+    float l0 = -INFINITY, l1 = -INFINITY, l2 = -INFINITY;
+    load(0, c0, l0);
+    load(1, c1, l1);
+    float4 O = c0;
+    float L = l0;
+    for (int b = 1; b < nb; ++b) {
+      load(b + 1, c2, l2);
+      float Lp, alpha, beta;
+      fold_coeffs(L, l1, Lp, alpha, beta);
+      O.x = fold_elem(O.x, c1.x, alpha, beta);
+      O.y = fold_elem(O.y, c1.y, alpha, beta);
+      O.z = fold_elem(O.z, c1.z, alpha, beta);
+      O.w = fold_elem(O.w, c1.w, alpha, beta);
+      L = Lp;
+      c1 = c2;
+      l1 = l2;
+    }
+    const int64_t row = static_cast<int64_t>(seq) * p.hq + h;
+    if (p.out_f32) reinterpret_cast<float4*>(p.out_f32 + row * kHeadDim)[lane] = O;
+    if (p.out_bf16)
+      reinterpret_cast<uint2*>(p.out_bf16 + row * kHeadDim)[lane] =
+          make_uint2(pack_bf16x2(O.x, O.y), pack_bf16x2(O.z, O.w));
+    if (p.lse && lane == 0) p.lse[row] = L;
+  }
+}
+
 }  // namespace
 
 bool decode_transposed_supported(const FwdParams& p) {
   return p.block == DecLayout::B && p.group >= 1 && p.group <= kDecodeMaxGroup && p.page_size >= 8 &&
          DecLayout::kPageWin % (DecLayout::B / p.page_size) == 0;
+}
+
+cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t stream) {
+  const int64_t warps = static_cast<int64_t>(p.num_tiles) * p.hq;
+  int64_t blocks = (warps + 7) / 8;
+  blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), static_cast<int64_t>(num_sms) * 8);
+  rlk_decode_merge_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

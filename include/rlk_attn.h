@@ -201,6 +201,33 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
                                  rlk_stream_t stream);
 
 /*
+ * Paged-KV decode with each sequence's KV blocks split into split_k fixed,
+ * contiguous ranges of global blocks (range r: blocks floor(r*nb/k) up to
+ * floor((r+1)*nb/k), nb = the sequence's blocks) that different SMs process:
+ * every range writes the block states (o_b, lse_b) of its blocks to a state
+ * table in the workspace, and a second kernel folds each (sequence, query
+ * head) in ascending block order with the canonical fold.  The arithmetic is
+ * the single-pass decode's step for step, so the result equals
+ * rlk_attn_decode_paged (and the last row of the equivalent prefill) bit for
+ * bit whatever split_k; it spreads few long sequences over all SMs.
+ *   Arguments as rlk_attn_decode_paged, plus
+ *   split_k: 1 .. 64 ranges per (sequence, KV head);
+ *   workspace: device, >= rlk_attn_workspace_size(params,
+ *     RLK_OP_DECODE_SPLIT, NULL, seqlens) bytes (the state table:
+ *     516 bytes per (sequence, block, query head)).
+ * Needs kv_block_size 128 and at most 8 query heads per KV head
+ * (RLK_ERR_UNSUPPORTED otherwise).
+ * [P3] PR stack: decode KV-cache replay; Status: fixed global_block_index
+ * merge; [P4] split-KV policy as an explicit, fixed knob.
+ */
+rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                        const void* v_pool, int32_t n_pages, int32_t page_size,
+                                        const int32_t* page_table, int32_t max_pages,
+                                        const int32_t* seqlens, int32_t split_k, float* out_f32,
+                                        void* out_bf16, float* lse, void* workspace,
+                                        size_t workspace_bytes, rlk_stream_t stream);
+
+/*
  * Deterministic backward of causal prefill (q_len == kv_len per sequence):
  *   q, k, v, dout: device BF16; out_f32: device FP32 forward output;
  *   lse: device FP32 forward lse; cu_seqlens: HOST [num_seqs + 1];
@@ -245,9 +272,11 @@ rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const in
                                          int64_t n_slabs, const float* state_o, const float* state_lse,
                                          float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream);
 
-enum { RLK_OP_MERGE = 1, RLK_OP_BACKWARD = 2 };
+enum { RLK_OP_MERGE = 1, RLK_OP_BACKWARD = 2, RLK_OP_DECODE_SPLIT = 3 };
 
-/* Workspace bytes an entry point needs (HOST cu_seqlens; 0 on bad input). */
+/* Workspace bytes an entry point needs (HOST cu_seqlens; 0 on bad input).
+ * RLK_OP_DECODE_SPLIT takes the decode context lengths (seqlens) as
+ * cu_seqlens_k and ignores cu_seqlens_q. */
 size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op,
                                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k);
 

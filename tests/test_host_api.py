@@ -149,3 +149,35 @@ def test_noalloc_merge_rejects_oversized_problem_before_any_device_work(lib):
         rlk.rlk_attn_merge_states_noalloc(p, cu, cu, 16, 1, 16, 16, 16, None, 16, stream=0)
     assert e.value.status == 2
     assert "scratch" in rlk.rlk_attn_last_error()
+
+
+def test_split_decode_rejects_before_any_launch(lib):
+    # every case below fails validation on the host, before the library
+    # touches the device, so placeholder pointers never reach a kernel
+    p = rlk.make_params(1)
+    for k in (0, 65):  # split_k outside 1..64
+        with pytest.raises(rlk.RlkError) as e:
+            rlk.rlk_attn_decode_paged_splitk(p, 16, 16, 16, 4, 16, 16, 4, [10], k, 16, None, 16, 16, 1 << 20,
+                                             stream=0)
+        assert e.value.status == 1
+    with pytest.raises(rlk.RlkError) as e:  # workspace smaller than the state table
+        rlk.rlk_attn_decode_paged_splitk(p, 16, 16, 16, 4, 16, 16, 4, [10], 2, 16, None, 16, 16, 64, stream=0)
+    assert e.value.status == 3
+    p64 = rlk.make_params(1, kv_block_size=64)
+    with pytest.raises(rlk.RlkError) as e:  # 64-key blocks: the transposed kernel takes 128
+        rlk.rlk_attn_decode_paged_splitk(p64, 16, 16, 16, 4, 16, 16, 4, [10], 2, 16, None, 16, 16, 1 << 20,
+                                         stream=0)
+    assert e.value.status == 2
+    pg = rlk.make_params(1, num_q_heads=32, num_kv_heads=2)
+    with pytest.raises(rlk.RlkError) as e:  # 16 query heads per KV head
+        rlk.rlk_attn_decode_paged_splitk(pg, 16, 16, 16, 4, 16, 16, 4, [10], 2, 16, None, 16, 16, 1 << 20,
+                                         stream=0)
+    assert e.value.status == 2
+
+
+def test_split_decode_workspace_size(lib):
+    p = rlk.make_params(2)  # Hq 32
+    # 300 and 129 tokens: 3 + 2 blocks of 128; 516 bytes per (block, query head), rounded up to 256
+    got = rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 129])
+    assert got == (5 * 32 * 129 * 4 + 255) // 256 * 256
+    assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 0]) == 0
