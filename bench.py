@@ -379,6 +379,7 @@ def measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args):
                      "sum_ctx": int(ctx.sum())}
     del kp, vp
     torch.cuda.empty_cache()
+    res["decode_long"] = measure_decode_long(torch, rlk, dv, peaks, flush, stream, args)
     res["backward"] = measure_backward(torch, rlk, dv, peaks, flush, stream, args)
     res["chunked"] = measure_chunked(torch, rlk, dv, peaks, flush, stream, args)
     return res
@@ -416,6 +417,47 @@ def measure_backward(torch, rlk, dv, peaks, flush, stream, args):
     return {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": flops,
             "frac": round(tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
             "workload": "2 x 4096 causal, Hq32/Hkv8/D128, dout ~ N(0,1) bf16; preprocess + dK/dV + dQ kernels"}
+
+
+def measure_decode_long(torch, rlk, dv, peaks, flush, stream, args, n=4, ctx_len=32768, split_k=(4, 8, 19)):
+    """Few long sequences: n sequences of ctx_len tokens (n x 8 (sequence, KV
+    head) items leave most SMs idle in a single pass), single-pass decode
+    against the split decode with the library's automatic split_k and a few
+    fixed ones; GB/s of the
+    K+V bytes read (the split's state table traffic is counted as overhead,
+    not work)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    ctx = np.full(n, ctx_len, np.int32)
+    pages_per = (ctx + 15) // 16
+    n_pages = int(pages_per.sum())
+    perm = synth.rng(5, synth.T_PAGES).permutation(n_pages).astype(np.int32)
+    pt = perm.reshape(n, -1).copy()
+    kp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    vp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    qd = torch.randn((n, 32, 128), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    ptd = dv.i32_to_device(pt)
+    pd = rlk.make_params(n, 32, 8, 128)
+    o = torch.empty((n, 32, 128), dtype=torch.float32, device="cuda")
+    ob = torch.empty((n, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lo = torch.empty((n, 32), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rlk.rlk_attn_workspace_size(pd, rlk.RLK_OP_DECODE_SPLIT, None, ctx), dtype=torch.uint8,
+                     device="cuda")
+    kv_bytes = int(ctx.astype(np.int64).sum()) * 8 * 128 * 2 * 2
+    t1 = time_steps(torch, lambda: rlk.rlk_attn_decode_paged(pd, qd, kp, vp, n_pages, 16, ptd, pt.shape[1], ctx, o, ob,
+                                                              lo, stream=stream), args.steps, args.warmup, flush, stream)
+    split = {"auto_k": rlk.rlk_attn_decode_auto_split(pd, ctx, torch.cuda.get_device_properties(0).multi_processor_count)}
+    for k in (0,) + tuple(split_k):
+        ts = time_steps(torch, lambda: rlk.rlk_attn_decode_paged_splitk(pd, qd, kp, vp, n_pages, 16, ptd, pt.shape[1],
+                                                                         ctx, k, o, ob, lo, ws, stream=stream),
+                        args.steps, args.warmup, flush, stream)
+        mss = float(np.mean(ts))
+        split["auto" if k == 0 else str(k)] = {"ms": round(mss, 4), "gbs": round(kv_bytes / (mss * 1e-3) / 1e9, 1)}
+    rlk.rlk_attn_check_device_error(stream)
+    ms1 = float(np.mean(t1))
+    return {"single_pass_gbs": round(kv_bytes / (ms1 * 1e-3) / 1e9, 1), "single_pass_ms": round(ms1, 4),
+            "split": split, "kv_bytes": kv_bytes, "peak": peaks["hbm_gbs"],
+            "workload": f"{n} seqs x {ctx_len} tokens, 16-token pages, Hq32/Hkv8/D128"}
 
 
 def measure_chunked(torch, rlk, dv, peaks, flush, stream, args, chunk=2048):

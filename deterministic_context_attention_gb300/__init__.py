@@ -90,6 +90,7 @@ def load():
             "rlk_attn_prefill": [PP, P, P, P, P, P, i32, P, P, P, P],
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
             "rlk_attn_decode_paged_splitk": [PP, P, P, P, i32, i32, P, i32, P, i32, P, P, P, P, sz, P],
+            "rlk_attn_decode_auto_split": [PP, P, i32],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
             "rlk_attn_workspace_size": [PP, i32, P, P],
             "rlk_attn_check_device_error": [P],
@@ -235,6 +236,12 @@ def rlk_attn_decode_paged_splitk(params, q, k_pool, v_pool, n_pages, page_size, 
                                                _ptr(sl), int(split_k), _ptr(out_f32), _ptr(out_bf16), _ptr(lse),
                                                _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "rlk_attn_decode_paged_splitk")
+
+
+def rlk_attn_decode_auto_split(params, seqlens, num_sms) -> int:
+    """Split factor rlk_attn_decode_paged_splitk picks for split_k=0 (-1: invalid input)."""
+    sl = _i32_host(seqlens)
+    return int(load().rlk_attn_decode_auto_split(ctypes.byref(params), _ptr(sl), int(num_sms)))
 
 
 def rlk_attn_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,

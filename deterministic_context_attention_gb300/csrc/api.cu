@@ -509,6 +509,64 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
 }
 
 
+namespace {
+
+// Split factor for split_k == 0.  Cost of a candidate k, in units of one KV
+// block's processing time on one SM: the busiest CTA's load when the items
+// (sorted by size, largest first) are dealt to min(items, SMs) CTAs in the
+// decode kernel's snake order, each item adding a fixed start-up, plus -- for
+// k > 1 -- the fold kernel, whose serial lse chain walks the longest
+// sequence's blocks.  Candidates stay within one launch's item list; ties go
+// to the smaller k (less state traffic).
+constexpr double kSplitItemStartup = 1.0;  // blocks' worth of start-up per item
+constexpr double kSplitFoldPerBlock = 0.08;  // fold chain step / KV block step
+int choose_split(const int32_t* seqlens, int num_seqs, int hkv, int B, int num_sms) {
+  std::vector<int> nbs(num_seqs);
+  int nb_max = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    nbs[s] = (seqlens[s] + B - 1) / B;
+    nb_max = std::max(nb_max, nbs[s]);
+  }
+  int best_k = 1;
+  double best = 0.0;
+  std::vector<int> sizes;
+  std::vector<double> load;
+  for (int k = 1; k <= 64; ++k) {
+    sizes.clear();
+    for (int s = 0; s < num_seqs; ++s)
+      for (int r = 0; r < k; ++r) {
+        const int n = static_cast<int>(static_cast<int64_t>(r + 1) * nbs[s] / k - static_cast<int64_t>(r) * nbs[s] / k);
+        if (n > 0)
+          for (int g = 0; g < hkv; ++g) sizes.push_back(n);
+      }
+    if (k > 1 && sizes.size() > static_cast<size_t>(rlk::kMaxTilesPerLaunch)) break;
+    std::sort(sizes.begin(), sizes.end(), [](int a, int b) { return a > b; });
+    const int grid = std::min(static_cast<int>(sizes.size()), num_sms);
+    load.assign(grid, 0.0);
+    for (size_t i = 0; i < sizes.size(); ++i) {
+      const int round = static_cast<int>(i / grid), c = static_cast<int>(i % grid);
+      load[(round & 1) ? grid - 1 - c : c] += sizes[i] + kSplitItemStartup;
+    }
+    double cost = *std::max_element(load.begin(), load.end());
+    if (k > 1) cost += nb_max * kSplitFoldPerBlock;
+    if (k == 1 || cost < best) {
+      best = cost;
+      best_k = k;
+    }
+  }
+  return best_k;
+}
+
+}  // namespace
+
+int32_t rlk_attn_decode_auto_split(const rlk_attn_params* params, const int32_t* seqlens, int32_t num_sms) {
+  if (check_params(params) || !seqlens || num_sms < 1) return -1;
+  const int B = params->kv_block_size;
+  for (int s = 0; s < params->num_seqs; ++s)
+    if (seqlens[s] < 1) return -1;
+  return choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, num_sms);
+}
+
 rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const void* q, const void* k_pool,
                                         const void* v_pool, int32_t n_pages, int32_t page_size,
                                         const int32_t* page_table, int32_t max_pages,
@@ -519,7 +577,7 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
   if (st) return st;
   if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
-  if (split_k < 1 || split_k > 64) return fail(RLK_ERR_INVALID_ARGUMENT, "split_k %d not in 1..64", split_k);
+  if (split_k < 0 || split_k > 64) return fail(RLK_ERR_INVALID_ARGUMENT, "split_k %d not in 0..64", split_k);
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && !aligned16(out_bf16)) || !aligned16(workspace))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
@@ -542,6 +600,13 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", workspace_bytes, need);
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
+  if (split_k == 0) {
+    split_k = choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, dev->num_sms);
+    // one range per sequence is the single-pass decode, which needs no state table
+    if (split_k == 1)
+      return rlk_attn_decode_paged(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                                   out_f32, out_bf16, lse, stream);
+  }
   // state table: pair (block_base[s] + b) * Hq + head; o_b FP32 [pair][128], then lse_b [pair]
   std::vector<int32_t> block_base(params->num_seqs + 1, 0);
   for (int s = 0; s < params->num_seqs; ++s) block_base[s + 1] = block_base[s] + (seqlens[s] + B - 1) / B;

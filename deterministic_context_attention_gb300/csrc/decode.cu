@@ -564,52 +564,93 @@ cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& tq, const CUt
   return cudaGetLastError();
 }
 
-// Split decode, second step: one warp per (sequence, query head) folds the
-// sequence's block states in ascending global block order with the canonical
-// fold -- the same operations the single-pass kernel applies on chip, so the
-// result is the same bit for bit.  Lane l holds elements 4l..4l+3; the next
-// two states are in flight while one folds.
-__global__ void __launch_bounds__(256) rlk_decode_merge_kernel(const __grid_constant__ FwdParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+// Split decode, second step: the canonical fold of one (sequence, query head)
+// pair's block states in ascending global block order -- the operations the
+// single-pass kernel applies on chip, so the result is the same bit for bit.
+// One 128-thread CTA per pair, thread t owning head dimension t.  The fold is a
+// chain over the blocks, so what bounds it is how many state bytes are in
+// flight: chunks of kDmChunk block states (512 B of o plus the lse each) are
+// staged through a kDmStages-deep ring of asynchronous copies, whole chunks
+// landing while an earlier one folds.  Every thread recomputes the same fold
+// coefficients from the staged lse values.
+constexpr int kDmChunk = 32;
+constexpr int kDmStages = 4;
+constexpr int kDmThreads = kHeadDim;
+constexpr int kDmStageBytes = kDmChunk * kHeadDim * 4 + kDmChunk * 4;
+constexpr int kDmSmem = kDmStages * kDmStageBytes;
+static_assert(kDmThreads == 128 && (kDmChunk * kHeadDim / 4) % kDmThreads == 0, "decode fold staging layout");
+
+__global__ void __launch_bounds__(kDmThreads) rlk_decode_merge_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int t = threadIdx.x;
   const int64_t total = static_cast<int64_t>(p.num_tiles) * p.hq;  // num_tiles: sequences
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
-       w += warps) {
+  for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
     const int seq = static_cast<int>(w / p.hq);
     const int h = static_cast<int>(w - static_cast<int64_t>(seq) * p.hq);
     const int nb = (p.cu_k[seq] + DecLayout::B - 1) / DecLayout::B;
+    const int nchunks = (nb + kDmChunk - 1) / kDmChunk;
     const int64_t pair0 = static_cast<int64_t>(p.cu_q[seq]) * p.hq + h;
-    auto load = [&](int b, float4& o, float& lb) {
-      if (b < nb) {
-        const int64_t pr = pair0 + static_cast<int64_t>(b) * p.hq;
-        o = reinterpret_cast<const float4*>(p.state_o + pr * kHeadDim)[lane];
-        lb = p.state_lse[pr];
+    // chunk c -> stage c % kDmStages; a warp copies one block's 512 B of o
+    auto issue = [&](int c) {
+      if (c < nchunks) {
+        uint8_t* st = dsm + (c % kDmStages) * kDmStageBytes;
+        float* so = reinterpret_cast<float*>(st);
+        float* sl = reinterpret_cast<float*>(st + kDmChunk * kHeadDim * 4);
+#pragma unroll
+        for (int k = 0; k < kDmChunk * kHeadDim / 4 / kDmThreads; ++k) {
+          const int i = t + k * kDmThreads;
+          const int j = i >> 5, seg = i & 31;
+          const int b = c * kDmChunk + j;
+          if (b < nb) {
+            const int64_t pr = pair0 + static_cast<int64_t>(b) * p.hq;
+            cp_async16(so + j * kHeadDim + seg * 4, p.state_o + pr * kHeadDim + seg * 4);
+          }
+        }
+        if (t < kDmChunk && c * kDmChunk + t < nb) {
+          const int64_t pr = pair0 + static_cast<int64_t>(c * kDmChunk + t) * p.hq;
+          cp_async4(sl + t, p.state_lse + pr);
+        }
       }
+      cp_async_commit();  // empty groups keep the count uniform
     };
-    float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0, c2 = c0;
-    float l0 = -INFINITY, l1 = -INFINITY, l2 = -INFINITY;
-    load(0, c0, l0);
-    load(1, c1, l1);
-    float4 O = c0;
-    float L = l0;
-    for (int b = 1; b < nb; ++b) {
-      load(b + 1, c2, l2);
-      float Lp, alpha, beta;
-      fold_coeffs(L, l1, Lp, alpha, beta);
-      O.x = fold_elem(O.x, c1.x, alpha, beta);
-      O.y = fold_elem(O.y, c1.y, alpha, beta);
-      O.z = fold_elem(O.z, c1.z, alpha, beta);
-      O.w = fold_elem(O.w, c1.w, alpha, beta);
-      L = Lp;
-      c1 = c2;
-      l1 = l2;
+#pragma unroll
+    for (int c = 0; c < kDmStages - 1; ++c) issue(c);
+    float O = 0.f, L = -INFINITY;
+    for (int c = 0; c < nchunks; ++c) {
+      issue(c + kDmStages - 1);
+      cp_async_wait<kDmStages - 1>();
+      __syncthreads();
+      const uint8_t* st = dsm + (c % kDmStages) * kDmStageBytes;
+      const float* so = reinterpret_cast<const float*>(st);
+      const float* sl = reinterpret_cast<const float*>(st + kDmChunk * kHeadDim * 4);
+      const int jn = min(kDmChunk, nb - c * kDmChunk);
+      const int j0 = c == 0 ? 1 : 0;
+      if (c == 0) {
+        O = so[t];
+        L = sl[0];
+      }
+      auto fold1 = [&](int j) {
+        float Lp, alpha, beta;
+        fold_coeffs(L, sl[j], Lp, alpha, beta);
+        O = fold_elem(O, so[j * kHeadDim + t], alpha, beta);
+        L = Lp;
+      };
+      if (jn == kDmChunk) {
+        // whole chunk: unrolled, so the loads and the O update sit beside
+        // the serial lse chain instead of on it
+#pragma unroll
+        for (int j = 0; j < kDmChunk; ++j)
+          if (j >= j0) fold1(j);
+      } else {
+        for (int j = j0; j < jn; ++j) fold1(j);
+      }
+      __syncthreads();  // the stage is refilled by the next iteration's issue
     }
+    cp_async_wait<0>();
     const int64_t row = static_cast<int64_t>(seq) * p.hq + h;
-    if (p.out_f32) reinterpret_cast<float4*>(p.out_f32 + row * kHeadDim)[lane] = O;
-    if (p.out_bf16)
-      reinterpret_cast<uint2*>(p.out_bf16 + row * kHeadDim)[lane] =
-          make_uint2(pack_bf16x2(O.x, O.y), pack_bf16x2(O.z, O.w));
-    if (p.lse && lane == 0) p.lse[row] = L;
+    if (p.out_f32) p.out_f32[row * kHeadDim + t] = O;
+    if (p.out_bf16) p.out_bf16[row * kHeadDim + t] = f32_to_bf16_rn(O);
+    if (p.lse && t == 0) p.lse[row] = L;
   }
 }
 
@@ -621,10 +662,15 @@ bool decode_transposed_supported(const FwdParams& p) {
 }
 
 cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t stream) {
-  const int64_t warps = static_cast<int64_t>(p.num_tiles) * p.hq;
-  int64_t blocks = (warps + 7) / 8;
-  blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), static_cast<int64_t>(num_sms) * 8);
-  rlk_decode_merge_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(rlk_decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDmSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t pairs = static_cast<int64_t>(p.num_tiles) * p.hq;
+  const int64_t blocks = std::min<int64_t>(std::max<int64_t>(pairs, 1), static_cast<int64_t>(num_sms) * 3);
+  rlk_decode_merge_kernel<<<static_cast<int>(blocks), kDmThreads, kDmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -64,18 +64,6 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeStages = 3;
 constexpr int kMergeSmem = kMergeStages * (8 * kMergeThreads * 16 + kMergeThreads * 4);
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __global__ void __launch_bounds__(kMergeThreads, 2) rlk_merge_fold_kernel(const __grid_constant__ MergeParams p) {
   extern __shared__ __align__(16) uint8_t msm[];
   float4* ring = reinterpret_cast<float4*>(msm);  // [stage][m][thread]

@@ -211,7 +211,10 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
  * rlk_attn_decode_paged (and the last row of the equivalent prefill) bit for
  * bit whatever split_k; it spreads few long sequences over all SMs.
  *   Arguments as rlk_attn_decode_paged, plus
- *   split_k: 1 .. 64 ranges per (sequence, KV head);
+ *   split_k: 1 .. 64 ranges per (sequence, KV head), or 0 to let the
+ *     library pick k from the context lengths and the SM count (a model of
+ *     the busiest SM's blocks plus the fold; k = 1 runs the single-pass
+ *     decode) -- the result is the same for every k;
  *   workspace: device, >= rlk_attn_workspace_size(params,
  *     RLK_OP_DECODE_SPLIT, NULL, seqlens) bytes (the state table:
  *     516 bytes per (sequence, block, query head)).
@@ -226,6 +229,15 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
                                         const int32_t* seqlens, int32_t split_k, float* out_f32,
                                         void* out_bf16, float* lse, void* workspace,
                                         size_t workspace_bytes, rlk_stream_t stream);
+
+/*
+ * The split factor rlk_attn_decode_paged_splitk uses for split_k == 0 on a
+ * device with num_sms SMs (host only, no device work): 1 .. 64, or -1 for
+ * invalid params, a NULL seqlens, a context length < 1 or num_sms < 1.
+ *   seqlens: HOST [num_seqs] context lengths.
+ * [P4] split-KV policy as an explicit, fixed knob.
+ */
+int32_t rlk_attn_decode_auto_split(const rlk_attn_params* params, const int32_t* seqlens, int32_t num_sms);
 
 /*
  * Deterministic backward of causal prefill (q_len == kv_len per sequence):

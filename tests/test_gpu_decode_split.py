@@ -39,7 +39,7 @@ def dec():
     return synth.paged_decode_problem(ctx=[1, 17, 128, 129, 1000, 2049, 4096], seed=51, spare_pages=4)
 
 
-@pytest.mark.parametrize("split_k", [1, 2, 3, 8, 64])
+@pytest.mark.parametrize("split_k", [0, 1, 2, 3, 8, 64])  # 0: the library picks k
 def test_split_decode_equals_single_pass(dec, split_k):
     assert_bitwise(run_split(dec, split_k), run_decode(dec), f"split_k {split_k}")
 

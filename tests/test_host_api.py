@@ -155,7 +155,7 @@ def test_split_decode_rejects_before_any_launch(lib):
     # every case below fails validation on the host, before the library
     # touches the device, so placeholder pointers never reach a kernel
     p = rlk.make_params(1)
-    for k in (0, 65):  # split_k outside 1..64
+    for k in (-1, 65):  # split_k outside 0..64
         with pytest.raises(rlk.RlkError) as e:
             rlk.rlk_attn_decode_paged_splitk(p, 16, 16, 16, 4, 16, 16, 4, [10], k, 16, None, 16, 16, 1 << 20,
                                              stream=0)
@@ -181,3 +181,19 @@ def test_split_decode_workspace_size(lib):
     got = rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 129])
     assert got == (5 * 32 * 129 * 4 + 255) // 256 * 256
     assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 0]) == 0
+
+
+def test_decode_auto_split_choice(lib):
+    # host-only policy query: few long sequences spread over the SMs, a batch
+    # that already fills them stays single-pass
+    p4 = rlk.make_params(4)  # Hq 32 / Hkv 8: 32 (sequence, KV head) pairs
+    k = rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 152)
+    assert 4 <= k <= 27  # 32k items stay within one launch's 880-entry item list
+    assert rlk.rlk_attn_decode_auto_split(p4, [128] * 4, 152) == 1  # one block each: nothing to split
+    p64 = rlk.make_params(64)
+    assert rlk.rlk_attn_decode_auto_split(p64, [32768] * 64, 152) == 1  # 512 pairs already cover 152 SMs
+    p1 = rlk.make_params(1)
+    assert rlk.rlk_attn_decode_auto_split(p1, [131072], 152) > 8  # one very long sequence
+    assert rlk.rlk_attn_decode_auto_split(p1, [131072], 1) == 1  # a single SM gains nothing from splitting
+    assert rlk.rlk_attn_decode_auto_split(p4, [32768, 0, 5, 5], 152) == -1
+    assert rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 0) == -1
