@@ -580,16 +580,28 @@ constexpr int kDmStageBytes = kDmChunk * kHeadDim * 4 + kDmChunk * 4;
 constexpr int kDmSmem = kDmStages * kDmStageBytes;
 static_assert(kDmThreads == 128 && (kDmChunk * kHeadDim / 4) % kDmThreads == 0, "decode fold staging layout");
 
-__global__ void __launch_bounds__(kDmThreads) rlk_decode_merge_kernel(const __grid_constant__ FwdParams p) {
+// The fold's own parameters: the decode's item list stays out of this launch.
+struct DecFoldParams {
+  const float* state_o;
+  const float* state_lse;
+  float* out_f32;
+  uint16_t* out_bf16;
+  float* lse;
+  int32_t num_seqs, hq;
+  int32_t block_base[kMaxSeqs + 1];  // first state-table block of each sequence
+  int32_t ctx[kMaxSeqs + 1];         // context length of each sequence
+};
+
+__global__ void __launch_bounds__(kDmThreads) rlk_decode_merge_kernel(const __grid_constant__ DecFoldParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   const int t = threadIdx.x;
-  const int64_t total = static_cast<int64_t>(p.num_tiles) * p.hq;  // num_tiles: sequences
+  const int64_t total = static_cast<int64_t>(p.num_seqs) * p.hq;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
     const int seq = static_cast<int>(w / p.hq);
     const int h = static_cast<int>(w - static_cast<int64_t>(seq) * p.hq);
-    const int nb = (p.cu_k[seq] + DecLayout::B - 1) / DecLayout::B;
+    const int nb = (p.ctx[seq] + DecLayout::B - 1) / DecLayout::B;
     const int nchunks = (nb + kDmChunk - 1) / kDmChunk;
-    const int64_t pair0 = static_cast<int64_t>(p.cu_q[seq]) * p.hq + h;
+    const int64_t pair0 = static_cast<int64_t>(p.block_base[seq]) * p.hq + h;
     // chunk c -> stage c % kDmStages; a warp copies one block's 512 B of o
     auto issue = [&](int c) {
       if (c < nchunks) {
@@ -668,9 +680,21 @@ cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t st
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int64_t pairs = static_cast<int64_t>(p.num_tiles) * p.hq;
+  DecFoldParams f;
+  f.state_o = p.state_o;
+  f.state_lse = p.state_lse;
+  f.out_f32 = p.out_f32;
+  f.out_bf16 = p.out_bf16;
+  f.lse = p.lse;
+  f.num_seqs = p.num_tiles;  // the caller passes the sequence count here
+  f.hq = p.hq;
+  for (int s = 0; s <= kMaxSeqs; ++s) {
+    f.block_base[s] = p.cu_q[s];
+    f.ctx[s] = p.cu_k[s];
+  }
+  const int64_t pairs = static_cast<int64_t>(f.num_seqs) * f.hq;
   const int64_t blocks = std::min<int64_t>(std::max<int64_t>(pairs, 1), static_cast<int64_t>(num_sms) * 3);
-  rlk_decode_merge_kernel<<<static_cast<int>(blocks), kDmThreads, kDmSmem, stream>>>(p);
+  rlk_decode_merge_kernel<<<static_cast<int>(blocks), kDmThreads, kDmSmem, stream>>>(f);
   return cudaGetLastError();
 }
 
