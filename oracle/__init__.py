@@ -69,9 +69,12 @@ def _load():
                                               i32, i32, P, i32, P, P, P]
         lib.rlko_backward_f64.argtypes = [i32, P, i32, i32, i32, dbl, P, P, P, P,
                                           i32, i32, P, P, P]
+        lib.rlko_rope_f32.argtypes = [i64, i32, i32, dbl, P, P, P]
+        lib.rlko_rope_f64.argtypes = [i64, i32, i32, dbl, P, P, P]
         lib.rlko_num_threads.argtypes = []
         for f in (lib.rlko_attention_f64, lib.rlko_row_block_states_f64, lib.rlko_fold_f32,
-                  lib.rlko_decode_paged_f64, lib.rlko_backward_f64, lib.rlko_num_threads):
+                  lib.rlko_decode_paged_f64, lib.rlko_backward_f64, lib.rlko_rope_f32,
+                  lib.rlko_rope_f64, lib.rlko_num_threads):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -198,3 +201,28 @@ def backward_f64(q, k, v, dout, cu, scale, only_seq=-1, only_group=-1):
                                _ptr(dq), _ptr(dk), _ptr(dv))
     _check(rc, "rlko_backward_f64")
     return dq, dk, dv
+
+
+def rope_f32(x, pos, theta):
+    """Canonical FP32 RoPE of rows x [T, H, D] (exact BF16 values) at
+    positions pos [T]; returns the BF16 results as float32."""
+    lib = _load()
+    x = _f32(x)
+    pos = _i32(pos)
+    t, h, d = x.shape
+    assert pos.shape == (t,)
+    y = np.empty_like(x)
+    _check(lib.rlko_rope_f32(t, h, d, float(theta), _ptr(pos), _ptr(x), _ptr(y)), "rlko_rope_f32")
+    return y
+
+
+def rope_f64(x, pos, theta):
+    """The exact rotation of rows x [T, H, D] at positions pos [T], float64."""
+    lib = _load()
+    x = _f32(x)
+    pos = _i32(pos)
+    t, h, d = x.shape
+    assert pos.shape == (t,)
+    y = np.empty(x.shape, np.float64)
+    _check(lib.rlko_rope_f64(t, h, d, float(theta), _ptr(pos), _ptr(x), _ptr(y)), "rlko_rope_f64")
+    return y

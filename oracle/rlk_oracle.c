@@ -29,6 +29,16 @@
  *   rlko_backward_f64         dQ/dK/dV of the attention above by its
  *                             definition ("WS2 Attention PR5 Drift Benchmark",
  *                             Scope: optional backward dq, dk, dv), FP64.
+ *   rlko_rope_f32             rotary position embedding of Q or K rows in
+ *                             the canonical FP32 form, BF16 result
+ *                             ("WS2 Attention PR5 Drift Benchmark", Scope:
+ *                             optional RoPE composition before Attention,
+ *                             Attention consuming post-RoPE Q/K; "H100
+ *                             validation and reproduction guide", PR stack:
+ *                             decode KV-cache replay and cache/position/RoPE
+ *                             identity).
+ *   rlko_rope_f64             the same rotation exactly, in double (for the
+ *                             pins of rlko_rope_f32).
  *
  * Inputs are float32 arrays holding exact BF16 values; every arithmetic step
  * of the FP64 functions is done in double.  Build with -ffp-contract=off so
@@ -411,6 +421,84 @@ int rlko_backward_f64(int num_seqs, const int32_t* cu, int hq, int hkv, int d,
     free(sc);
     free(ds);
     free(orow);
+  }
+  return RLKO_OK;
+}
+
+/* ---------------------------------------------------------------- RoPE
+ * The pages name RoPE only as a step composed before attention, with the
+ * attention reading post-RoPE Q/K and decode replay keeping the cache,
+ * position and RoPE identical to prefill.  Convention and precision are not
+ * on the pages; the reading taken (rotate-half pairs (i, i + D/2), the
+ * Qwen/NeoX layout, frequencies theta^(-2i/D)):
+ *   angle = p * theta^(-2i/D)                  in double
+ *   c = (float)cos(angle), s = (float)sin(angle)   one rounding each
+ *   y_i       = bf16_rn(fmaf(x_i, c, -(x_{i+D/2} * s)))      product in float
+ *   y_{i+D/2} = bf16_rn(fmaf(x_{i+D/2}, c, x_i * s))
+ * x holds BF16 values (exact in float).  Rows are [n_tok][h][d]; pos[t] is
+ * the position of row t. */
+static double rope_angle(double theta, int d, int i, int32_t p) {
+  const double inv = pow(theta, (-2.0 * (double)i) / (double)d);
+  return (double)p * inv;
+}
+
+/* float -> nearest BF16 (ties to even), returned as the float it denotes. */
+static float round_bf16(float v) {
+  uint32_t b;
+  memcpy(&b, &v, 4);
+  if ((b & 0x7F800000u) == 0x7F800000u) return v;  /* inf / nan unchanged */
+  b += 0x7FFFu + ((b >> 16) & 1u);
+  b &= 0xFFFF0000u;
+  float r;
+  memcpy(&r, &b, 4);
+  return r;
+}
+
+int rlko_rope_f32(int64_t n_tok, int h, int d, double theta, const int32_t* pos, const float* x,
+                  float* y) {
+  if (n_tok < 0 || h < 1 || d < 2 || (d & 1) || !(theta > 1.0) || (n_tok && (!pos || !x || !y)))
+    return RLKO_EINVAL;
+  const int half = d / 2;
+  for (int64_t t = 0; t < n_tok; ++t)
+    if (pos[t] < 0) return RLKO_EINVAL;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < n_tok; ++t) {
+    for (int i = 0; i < half; ++i) {
+      const double a = rope_angle(theta, d, i, pos[t]);
+      const float c = (float)cos(a), s = (float)sin(a);
+      for (int hh = 0; hh < h; ++hh) {
+        const float* xr = x + (t * h + hh) * (int64_t)d;
+        float* yr = y + (t * h + hh) * (int64_t)d;
+        const float x0 = xr[i], x1 = xr[i + half];
+        const float p1 = x1 * s, p0 = x0 * s;
+        yr[i] = round_bf16(fmaf(x0, c, -p1));
+        yr[i + half] = round_bf16(fmaf(x1, c, p0));
+      }
+    }
+  }
+  return RLKO_OK;
+}
+
+int rlko_rope_f64(int64_t n_tok, int h, int d, double theta, const int32_t* pos, const float* x,
+                  double* y) {
+  if (n_tok < 0 || h < 1 || d < 2 || (d & 1) || !(theta > 1.0) || (n_tok && (!pos || !x || !y)))
+    return RLKO_EINVAL;
+  const int half = d / 2;
+  for (int64_t t = 0; t < n_tok; ++t)
+    if (pos[t] < 0) return RLKO_EINVAL;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < n_tok; ++t) {
+    for (int i = 0; i < half; ++i) {
+      const double a = rope_angle(theta, d, i, pos[t]);
+      const double c = cos(a), s = sin(a);
+      for (int hh = 0; hh < h; ++hh) {
+        const float* xr = x + (t * h + hh) * (int64_t)d;
+        double* yr = y + (t * h + hh) * (int64_t)d;
+        const double x0 = xr[i], x1 = xr[i + half];
+        yr[i] = x0 * c - x1 * s;
+        yr[i + half] = x1 * c + x0 * s;
+      }
+    }
   }
   return RLKO_OK;
 }

@@ -386,3 +386,81 @@ def test_backward_restriction_matches_full():
     assert np.array_equal(dq1[a:b, 2:4], dq[a:b, 2:4])
     assert np.array_equal(dk1[a:b, 1], dk[a:b, 1]) and np.array_equal(dv1[a:b, 1], dv[a:b, 1])
     assert np.isnan(dq1[:a]).all()
+
+
+# --- RoPE -------------------------------------------------------------------
+
+def test_rope_handworked_golden():
+    cases = json.load(open(os.path.join(GOLDEN, "rope_handworked.json")))["cases"]
+    for c in cases:
+        d = c["d"]
+        x = np.zeros((1, 1, d), np.float32)
+        for i, v in c["x"].items():
+            x[0, 0, int(i)] = v
+        want = np.zeros(d, np.float32)
+        for i, v in c["y"].items():
+            want[int(i)] = v
+        y = oracle.rope_f32(x, [c["pos"]], c["theta"])
+        np.testing.assert_array_equal(y[0, 0], want, err_msg=c["name"])
+
+
+def _bf16_round(a):
+    b = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32)
+
+
+def _rope_rows(t, h, d, seed):
+    rng = np.random.default_rng(seed)
+    return _bf16_round(rng.standard_normal((t, h, d)).astype(np.float32))
+
+
+def test_rope_exact_equals_complex_rotation():
+    # the rotation of pair (i, i + D/2) is multiplication of x_i + j x_{i+D/2}
+    # by exp(j * p * theta^(-2i/D)): a second formulation, in numpy complex
+    t, h, d, theta = 37, 3, 16, 1e4
+    x = _rope_rows(t, h, d, 1)
+    pos = np.random.default_rng(2).integers(0, 50000, t).astype(np.int32)
+    y = oracle.rope_f64(x, pos, theta)
+    f = theta ** (-np.arange(d // 2) * 2.0 / d)
+    z = (x[..., : d // 2] + 1j * x[..., d // 2:].astype(np.float64)) * np.exp(1j * pos[:, None, None] * f[None, None, :])
+    np.testing.assert_allclose(y[..., : d // 2], z.real, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y[..., d // 2:], z.imag, rtol=0, atol=1e-12)
+
+
+def test_rope_exact_relative_position_property():
+    # <R(m) q, R(n) k> depends on m - n only
+    d, theta = 128, 1e6
+    q = _rope_rows(1, 1, d, 3)
+    k = _rope_rows(1, 1, d, 4)
+    for m, n, s in [(5, 2, 1000), (0, 0, 31), (4000, 17, 12345)]:
+        a = np.dot(oracle.rope_f64(q, [m], theta)[0, 0], oracle.rope_f64(k, [n], theta)[0, 0])
+        b = np.dot(oracle.rope_f64(q, [m + s], theta)[0, 0], oracle.rope_f64(k, [n + s], theta)[0, 0])
+        assert abs(a - b) <= 1e-9 * (1 + abs(a))
+
+
+@pytest.mark.parametrize("theta", [1e6, 1e4])
+def test_rope_f32_is_bf16_rounding_of_exact_rotation(theta):
+    # the canonical FP32 form differs from the exact rotation only by the
+    # FP32 steps (a few 2^-24 relative) before the one BF16 rounding: within
+    # one BF16 ulp everywhere, and equal to bf16_rn(exact) almost everywhere
+    t, h, d = 300, 4, 128
+    x = _rope_rows(t, h, d, 5)
+    pos = np.random.default_rng(6).integers(0, 40000, t).astype(np.int32)
+    y32 = oracle.rope_f32(x, pos, theta).astype(np.float64)
+    y64 = oracle.rope_f64(x, pos, theta)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(y64), 1e-30))) - 7)
+    assert np.all(np.abs(y32 - y64) <= ulp + 1e-30)
+    same = np.mean(y32 == _bf16_round(y64.astype(np.float32)).astype(np.float64))
+    assert same > 0.999
+    assert np.all(_bf16_round(y32.astype(np.float32)) == y32.astype(np.float32))  # results are BF16 values
+
+
+def test_rope_position_zero_is_identity_and_rows_are_independent():
+    t, h, d = 9, 2, 128
+    x = _rope_rows(t, h, d, 7)
+    np.testing.assert_array_equal(oracle.rope_f32(x, np.zeros(t, np.int32), 1e6), x)
+    pos = np.arange(t, dtype=np.int32) * 100
+    full = oracle.rope_f32(x, pos, 1e6)
+    for i in (0, 4, 8):
+        np.testing.assert_array_equal(oracle.rope_f32(x[i:i + 1], pos[i:i + 1], 1e6), full[i:i + 1])
