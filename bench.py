@@ -380,6 +380,7 @@ def measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args):
     del kp, vp
     torch.cuda.empty_cache()
     res["decode_long"] = measure_decode_long(torch, rlk, dv, peaks, flush, stream, args)
+    res["rope"] = measure_rope(torch, rlk, dv, peaks, flush, stream, args)
     res["backward"] = measure_backward(torch, rlk, dv, peaks, flush, stream, args)
     res["chunked"] = measure_chunked(torch, rlk, dv, peaks, flush, stream, args)
     return res
@@ -417,6 +418,33 @@ def measure_backward(torch, rlk, dv, peaks, flush, stream, args):
     return {"value": round(tf, 2), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": flops,
             "frac": round(tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
             "workload": "2 x 4096 causal, Hq32/Hkv8/D128, dout ~ N(0,1) bf16; preprocess + dK/dV + dQ kernels"}
+
+
+def measure_rope(torch, rlk, dv, peaks, flush, stream, args):
+    """The RoPE pass over the varlen prefill workload's Q (32 heads) and K
+    (8 heads), in place: 256 B read + 256 B written per (token, head) row."""
+    cfg = synth.CFG_PREFILL
+    cu = synth.cu_seqlens(cfg["lens"])
+    t = int(cu[-1])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    q = torch.randn((t, cfg["hq"], 128), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((t, cfg["hkv"], 128), generator=g, device="cuda").to(torch.bfloat16)
+    max_pos = max(cfg["lens"])
+    table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
+    pr = rlk.make_params(len(cfg["lens"]))
+
+    def step():
+        rlk.rlk_attn_rope(pr, q, q, cfg["hq"], cu, None, table, max_pos, stream=stream)
+        rlk.rlk_attn_rope(pr, k, k, cfg["hkv"], cu, None, table, max_pos, stream=stream)
+    ts = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    nbytes = t * (cfg["hq"] + cfg["hkv"]) * 512
+    ms = float(np.mean(ts))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": nbytes, "launches_per_step": 2,
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
+            "workload": "RoPE in place on the varlen prefill Q [8897,32,128] and K [8897,8,128] (BF16)"}
 
 
 def measure_decode_long(torch, rlk, dv, peaks, flush, stream, args, n=4, ctx_len=32768, split_k=(4, 8, 19)):

@@ -91,6 +91,9 @@ def load():
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
             "rlk_attn_decode_paged_splitk": [PP, P, P, P, i32, i32, P, i32, P, i32, P, P, P, P, sz, P],
             "rlk_attn_decode_auto_split": [PP, P, i32],
+            "rlk_attn_rope_table": [ctypes.c_double, i32, P],
+            "rlk_attn_rope": [PP, P, P, i32, P, P, P, i32, P],
+            "rlk_attn_decode_paged_rope": [PP, P, P, P, i32, i32, P, i32, P, P, i32, P, P, P, P],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
             "rlk_attn_workspace_size": [PP, i32, P, P],
             "rlk_attn_check_device_error": [P],
@@ -242,6 +245,30 @@ def rlk_attn_decode_auto_split(params, seqlens, num_sms) -> int:
     """Split factor rlk_attn_decode_paged_splitk picks for split_k=0 (-1: invalid input)."""
     sl = _i32_host(seqlens)
     return int(load().rlk_attn_decode_auto_split(ctypes.byref(params), _ptr(sl), int(num_sms)))
+
+
+def rlk_attn_rope_table(theta, max_pos):
+    """Host RoPE table [max_pos, 128] float32 (cos 64 | sin 64 per position)."""
+    table = np.empty((int(max_pos), 128), np.float32)
+    _check(load().rlk_attn_rope_table(float(theta), int(max_pos), _ptr(table)), "rlk_attn_rope_table")
+    return table
+
+
+def rlk_attn_rope(params, x, y, num_heads, cu_seqlens, pos_offset, table, max_pos, stream=None):
+    cu = _i32_host(cu_seqlens)
+    po = None if pos_offset is None else _i32_host(pos_offset)
+    _check(load().rlk_attn_rope(ctypes.byref(params), _ptr(x), _ptr(y), int(num_heads), _ptr(cu), _ptr(po),
+                                _ptr(table), int(max_pos), _stream(stream)), "rlk_attn_rope")
+
+
+def rlk_attn_decode_paged_rope(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                               rope_table, rope_max_pos, out_f32, out_bf16, lse, stream=None):
+    sl = _i32_host(seqlens)
+    _check(load().rlk_attn_decode_paged_rope(ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                             int(n_pages), int(page_size), _ptr(page_table), int(max_pages),
+                                             _ptr(sl), _ptr(rope_table), int(rope_max_pos), _ptr(out_f32),
+                                             _ptr(out_bf16), _ptr(lse), _stream(stream)),
+           "rlk_attn_decode_paged_rope")
 
 
 def rlk_attn_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librlk_attn.so")
-SOURCES = ["api.cu", "fwd.cu", "decode.cu", "merge.cu", "bwd.cu"]
+SOURCES = ["api.cu", "fwd.cu", "decode.cu", "merge.cu", "bwd.cu", "rope.cu"]
 HEADERS = ["ptx.cuh", "numerics.cuh", "rlk_internal.h", os.path.join("..", "..", "include", "rlk_attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

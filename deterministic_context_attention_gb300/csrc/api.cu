@@ -24,6 +24,7 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream);
 bool decode_transposed_supported(const FwdParams& p);
 cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_rope(const RopeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t stream);
 cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
@@ -432,10 +433,12 @@ rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const 
   return ok();
 }
 
-rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, const void* k_pool,
-                                 const void* v_pool, int32_t n_pages, int32_t page_size,
-                                 const int32_t* page_table, int32_t max_pages, const int32_t* seqlens,
-                                 float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+namespace {
+
+rlk_status decode_paged_impl(const rlk_attn_params* params, const void* q, const void* k_pool, const void* v_pool,
+                             int32_t n_pages, int32_t page_size, const int32_t* page_table, int32_t max_pages,
+                             const int32_t* seqlens, const float* rope_table, int32_t rope_max_pos,
+                             float* out_f32, void* out_bf16, float* lse, cudaStream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
@@ -453,6 +456,16 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
     if (seqlens[s] < 1 || static_cast<int64_t>(seqlens[s]) > static_cast<int64_t>(max_pages) * page_size)
       return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: context length %d not in 1..max_pages*page_size", s,
                   seqlens[s]);
+  if (rope_table) {
+    if (!aligned16(rope_table)) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table must be 16-byte aligned");
+    if (B != 128 || params->num_q_heads / params->num_kv_heads > rlk::kDecodeMaxGroup)
+      return fail(RLK_ERR_UNSUPPORTED, "decode with RoPE needs kv_block_size 128 and at most %d query heads per KV head",
+                  rlk::kDecodeMaxGroup);
+    for (int s = 0; s < params->num_seqs; ++s)
+      if (seqlens[s] > rope_max_pos)
+        return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: position %d is past the RoPE table (%d positions)", s,
+                    seqlens[s] - 1, rope_max_pos);
+  }
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   const int group = params->num_q_heads / params->num_kv_heads;
@@ -490,6 +503,7 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
   fp->max_pages = max_pages;
   fp->page_size = page_size;
   fp->n_pages = n_pages;
+  fp->rope_table = rope_table;
   if (!rlk::decode_transposed_supported(*fp)) {
     if ((st = launch_fwd_tiles(fp.get(), tiles, 1, mq, mk, mv, dev, stream))) return st;
     return ok();
@@ -505,6 +519,81 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
     cudaError_t e = rlk::launch_decode(*fp, mq, mk, mv, grid, stream);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   }
+  return ok();
+}
+
+}  // namespace
+
+rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                 const void* v_pool, int32_t n_pages, int32_t page_size,
+                                 const int32_t* page_table, int32_t max_pages, const int32_t* seqlens,
+                                 float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+  return decode_paged_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens, nullptr, 0,
+                           out_f32, out_bf16, lse, stream);
+}
+
+rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                      const void* v_pool, int32_t n_pages, int32_t page_size,
+                                      const int32_t* page_table, int32_t max_pages, const int32_t* seqlens,
+                                      const float* rope_table, int32_t rope_max_pos, float* out_f32,
+                                      void* out_bf16, float* lse, rlk_stream_t stream) {
+  if (!rope_table) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table is NULL");
+  return decode_paged_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                           rope_table, rope_max_pos, out_f32, out_bf16, lse, stream);
+}
+
+rlk_status rlk_attn_rope_table(double theta, int32_t max_pos, float* table) {
+  if (!(theta > 1.0) || !std::isfinite(theta)) return fail(RLK_ERR_INVALID_ARGUMENT, "theta must be finite and > 1");
+  if (max_pos < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "max_pos %d < 1", max_pos);
+  if (!table) return fail(RLK_ERR_INVALID_ARGUMENT, "table is NULL");
+  constexpr int kHalf = rlk::kHeadDim / 2;
+  for (int i = 0; i < kHalf; ++i) {
+    // frequency theta^(-2i/D) and the angle in double, one rounding to FP32
+    const double inv = std::pow(theta, (-2.0 * static_cast<double>(i)) / static_cast<double>(rlk::kHeadDim));
+    for (int32_t p = 0; p < max_pos; ++p) {
+      const double a = static_cast<double>(p) * inv;
+      table[static_cast<int64_t>(p) * rlk::kHeadDim + i] = static_cast<float>(std::cos(a));
+      table[static_cast<int64_t>(p) * rlk::kHeadDim + kHalf + i] = static_cast<float>(std::sin(a));
+    }
+  }
+  return ok();
+}
+
+rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads,
+                         const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table, int32_t max_pos,
+                         rlk_stream_t stream) {
+  rlk_status st = check_params(params);
+  if (st) return st;
+  if (!x || !y || !table || !cu_seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(table))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  if (num_heads < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "num_heads %d < 1", num_heads);
+  if (cu_seqlens[0] != 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0");
+  for (int s = 0; s < params->num_seqs; ++s) {
+    const int64_t len = static_cast<int64_t>(cu_seqlens[s + 1]) - cu_seqlens[s];
+    if (len < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens not monotone at sequence %d", s);
+    const int64_t p0 = pos_offset ? pos_offset[s] : 0;
+    if (p0 < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: negative position offset", s);
+    if (len > 0 && p0 + len > max_pos)
+      return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: positions up to %lld are past the table (%d positions)", s,
+                  static_cast<long long>(p0 + len - 1), max_pos);
+  }
+  const int64_t rows = static_cast<int64_t>(cu_seqlens[params->num_seqs]) * num_heads;
+  if (rows == 0) return ok();
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
+  auto rp = std::make_unique<rlk::RopeParams>();
+  std::memset(rp.get(), 0, sizeof(*rp));
+  rp->x = static_cast<const uint16_t*>(x);
+  rp->y = static_cast<uint16_t*>(y);
+  rp->table = table;
+  rp->rows = rows;
+  rp->heads = num_heads;
+  rp->num_seqs = params->num_seqs;
+  for (int s = 0; s <= params->num_seqs; ++s) rp->cu[s] = cu_seqlens[s];
+  for (int s = 0; s < params->num_seqs; ++s) rp->pos0[s] = pos_offset ? pos_offset[s] : 0;
+  cudaError_t e = rlk::launch_rope(*rp, dev->num_sms, stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

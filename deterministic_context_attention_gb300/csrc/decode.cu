@@ -69,7 +69,8 @@ struct DecLayout {
                        kVEmpty = kVFull + kSV, kSFull = kVEmpty + kSV, kSEmpty = kSFull + kSS,
                        kPFull = kSEmpty + kSS, kPEmpty = kPFull + kPS, kOFull = kPEmpty + kPS,
                        kOEmpty = kOFull + kOS, kStatsFull = kOEmpty + kOS, kSyncMax = kStatsFull + kSR,
-                       kSyncPart = kSyncMax + 4, kNumBars = kSyncPart + 4;  // sync: [group][parity]
+                       kSyncPart = kSyncMax + 4, kQRope = kSyncPart + 4,  // sync: [group][parity]
+                       kNumBars = kQRope + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kPageWin = 512;                     // page ids cached per window (one per producer)
   static constexpr int kPageOff = (kMiscOff + 16 + 15) / 16 * 16;
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(&bars[L::kSyncMax + s], 128);
       mbar_init(&bars[L::kSyncPart + s], 128);
     }
+    mbar_init(&bars[L::kQRope], 128);
     *abort = 0;
     fence_mbar_init();
   }
@@ -285,7 +287,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (item >= p.num_items) continue;
       const DecItem di = dec_item(p, item);
       const int kv_len = di.kv_len, nb = di.nb;
-      bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x601);
+      // with RoPE the correction warps hand over the rotated rows
+      bool ok = mbar_wait(&bars[p.rope_table ? L::kQRope : L::kQFull], q_it & 1, abort, p.err, 0x601);
       if (!__all_sync(0xffffffffu, ok)) break;
       ++q_it;
       const uint32_t kb = k_it, vb = v_it, sb = s_it, ob = o_it;
@@ -468,13 +471,51 @@ __global__ void __launch_bounds__(kDThreads, 1)
     // ------------------------------------------------------------ correction / epilogue
     const int d = tid;  // head dimension lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t o_it = 0;
+    uint32_t o_it = 0, rq_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
       const DecItem di = dec_item(p, item);
       const int seq = di.seq, g = di.g, nb = di.nb;
       const bool split = p.state_o != nullptr;
+      if (p.rope_table) {
+        // RoPE of the query rows at position kv_len - 1, in place: thread t
+        // takes pairs 4u .. 4u+3 (u = t mod 16) of row t / 16; the pair's
+        // second element sits at the same offset of the second half
+        bool ok = mbar_wait(&bars[L::kQFull], rq_it & 1, abort, p.err, 0x803);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        ++rq_it;
+        const int i = tid >> 4, u = tid & 15;
+        if (i < G) {
+          const float* trow = p.rope_table + static_cast<int64_t>(di.kv_len - 1) * kHeadDim;
+          const float4 c = __ldg(reinterpret_cast<const float4*>(trow) + u);
+          const float4 s = __ldg(reinterpret_cast<const float4*>(trow + 64) + u);
+          uint2* pa = reinterpret_cast<uint2*>(q_tile + tile16_off(i, 4 * u));
+          uint2* pb = reinterpret_cast<uint2*>(q_tile + tile16_off(i, 64 + 4 * u));
+          const uint2 a = *pa, b = *pb;
+          const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+          const uint32_t wa[2] = {a.x, a.y}, wb[2] = {b.x, b.y};
+          uint32_t ra[2], rb[2];
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            float ya[2], yb[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * w + h;
+              const float x0 = bf16_bits_as_f32(static_cast<uint16_t>(h ? (wa[w] >> 16) : wa[w]));
+              const float x1 = bf16_bits_as_f32(static_cast<uint16_t>(h ? (wb[w] >> 16) : wb[w]));
+              ya[h] = __fmaf_rn(x0, cc[e], -__fmul_rn(x1, ss[e]));
+              yb[h] = __fmaf_rn(x1, cc[e], __fmul_rn(x0, ss[e]));
+            }
+            ra[w] = pack_bf16x2(ya[0], ya[1]);
+            rb[w] = pack_bf16x2(yb[0], yb[1]);
+          }
+          *pa = make_uint2(ra[0], ra[1]);
+          *pb = make_uint2(rb[0], rb[1]);
+        }
+        fence_proxy_async_smem();  // the tensor core reads the rows through the async proxy
+        mbar_arrive(&bars[L::kQRope]);
+      }
       float O[MG];
 #pragma unroll
       for (int q = 0; q < MG; ++q) O[q] = 0.0f;

@@ -58,6 +58,9 @@ struct FwdParams {
   // decode
   const int32_t* page_table;
   int32_t max_pages, page_size, n_pages, pad0;
+  // transposed decode: RoPE table [positions][cos 64, sin 64] (FP32); when
+  // set, the query rows are rotated at position kv_len - 1 after they land
+  const float* rope_table;
   // sequences: fused/states use cu_q / cu_k (packed offsets); decode uses
   // cu_k[s] as the context length of sequence s.
   int32_t cu_q[kMaxSeqs + 1];
@@ -86,6 +89,18 @@ struct MergeParams {
   float* lse;
   int32_t cu_q[kMaxSeqs + 1];
   int32_t cu_k[kMaxSeqs + 1];
+};
+
+// RoPE pass over packed BF16 rows [T, heads, 128]; row i of sequence s sits
+// at position pos0[s] + i.
+struct RopeParams {
+  const uint16_t* x;
+  uint16_t* y;          // may equal x
+  const float* table;   // [positions][cos 64, sin 64]
+  int64_t rows;         // T * heads
+  int32_t heads, num_seqs;
+  int32_t cu[kMaxSeqs + 1];
+  int32_t pos0[kMaxSeqs];
 };
 
 }  // namespace rlk

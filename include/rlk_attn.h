@@ -201,6 +201,60 @@ rlk_status rlk_attn_decode_paged(const rlk_attn_params* params, const void* q, c
                                  rlk_stream_t stream);
 
 /*
+ * RoPE table for rlk_attn_rope and rlk_attn_decode_paged_rope (host only):
+ * table[p * 128 + i] = (float)cos(p * theta^(-2i/128)) and
+ * table[p * 128 + 64 + i] = (float)sin(...) for p < max_pos, i < 64, the
+ * angle in double and rounded once.  The caller copies it to the device.
+ *   theta: base, finite and > 1 (Qwen3: 1e6); table: HOST, max_pos * 128 floats.
+ * RLK_ERR_INVALID_ARGUMENT for theta <= 1, max_pos < 1 or a NULL table.
+ * [P1] Scope: optional RoPE composition before Attention.
+ */
+rlk_status rlk_attn_rope_table(double theta, int32_t max_pos, float* table);
+
+/*
+ * Rotary position embedding of packed BF16 rows, rotate-half convention
+ * (pairs (i, i + 64) of the 128 dimensions), in the one FP32 form every
+ * RoPE path of the library uses:
+ *   y_i      = bf16_rn(fmaf(x_i, c, -(x_{i+64} * s)))
+ *   y_{i+64} = bf16_rn(fmaf(x_{i+64}, c, x_i * s))     (products rounded to FP32)
+ * with c, s the table's entries at the row's position -- so a row's result
+ * depends only on its values and its position (cache / position / RoPE
+ * identity between prefill, chunked replay and decode).
+ *   x, y: device BF16 [T, num_heads, 128], T = cu_seqlens[num_seqs]; y may
+ *     equal x (in place) but must not otherwise overlap it;
+ *   cu_seqlens: HOST [num_seqs + 1]; pos_offset: HOST [num_seqs] or NULL
+ *     (0): row i of sequence s is at position pos_offset[s] + i (a chunk of
+ *     q_len queries over a cache of kv_len keys: kv_len - q_len);
+ *   table: device, from rlk_attn_rope_table, max_pos positions.
+ * Only params->num_seqs and head_dim are read.  Every position must be
+ * < max_pos (RLK_ERR_INVALID_ARGUMENT otherwise, before any launch).
+ * [P1] Scope: RoPE before Attention, Attention consuming post-RoPE Q/K.
+ */
+rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads,
+                         const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table,
+                         int32_t max_pos, rlk_stream_t stream);
+
+/*
+ * rlk_attn_decode_paged with the query's RoPE applied inside the decode
+ * kernel: q holds the pre-RoPE query of each sequence, rotated at position
+ * seqlens[s] - 1 right after it lands in shared memory (the form of
+ * rlk_attn_rope, so the result equals rlk_attn_rope + rlk_attn_decode_paged
+ * bit for bit); the pools hold post-RoPE K (rotated once, when the token
+ * entered the cache) and V.
+ *   rope_table: device, from rlk_attn_rope_table, rope_max_pos positions
+ *     (every seqlens[s] <= rope_max_pos).
+ * Needs kv_block_size 128 and at most 8 query heads per KV head
+ * (RLK_ERR_UNSUPPORTED otherwise).
+ * [P3] PR stack: decode KV-cache replay and cache/position/RoPE identity.
+ */
+rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                      const void* v_pool, int32_t n_pages, int32_t page_size,
+                                      const int32_t* page_table, int32_t max_pages,
+                                      const int32_t* seqlens, const float* rope_table,
+                                      int32_t rope_max_pos, float* out_f32, void* out_bf16,
+                                      float* lse, rlk_stream_t stream);
+
+/*
  * Paged-KV decode with each sequence's KV blocks split into split_k fixed,
  * contiguous ranges of global blocks (range r: blocks floor(r*nb/k) up to
  * floor((r+1)*nb/k), nb = the sequence's blocks) that different SMs process:

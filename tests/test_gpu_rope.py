@@ -1,0 +1,132 @@
+"""GPU parity of RoPE: the streaming pass equals the oracle's canonical FP32
+RoPE bit for bit (BF16 results are byte-exact work), and the decode kernel's
+in-kernel query RoPE equals the pass followed by plain decode, which in turn
+equals the last row of the prefill over rotated inputs ("WS2 Attention PR5
+Drift Benchmark", Scope: RoPE composed before Attention, Attention consuming
+post-RoPE Q/K; "[WS2][Attention] H100 validation and reproduction guide", PR
+stack: decode KV-cache replay and cache/position/RoPE identity)."""
+import numpy as np
+import pytest
+
+import oracle
+from deterministic_context_attention_gb300 import synth
+from tests.gpu_helpers import assert_bitwise, assert_forward_parity, empty_outputs, lib, run_fused, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+THETA = 1.0e6
+
+
+def table_dev(max_pos):
+    torch = torch_cuda()
+    return torch.from_numpy(lib().rlk_attn_rope_table(THETA, max_pos)).cuda()
+
+
+def gpu_rope(x, cu, pos_offset, max_pos, inplace=False):
+    """x [T, H, 128] BF16 values (float32) through rlk_attn_rope."""
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    xd = dv.bf16_to_device(x)
+    yd = xd if inplace else torch.full_like(xd, float("nan"))
+    p = rlk.make_params(len(cu) - 1)
+    rlk.rlk_attn_rope(p, xd, yd, x.shape[1], cu, pos_offset, table_dev(max_pos), max_pos)
+    rlk.rlk_attn_check_device_error()
+    return yd.float().cpu().numpy()
+
+
+def positions(cu, pos_offset):
+    return np.concatenate([np.arange(cu[s + 1] - cu[s], dtype=np.int64) + (0 if pos_offset is None else pos_offset[s])
+                           for s in range(len(cu) - 1)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("heads,inplace", [(32, False), (8, True), (3, False)])
+def test_rope_pass_equals_oracle_bitwise(heads, inplace):
+    # ragged lengths with an empty sequence, offsets from 0 to 40,000
+    lens = [300, 0, 129, 1, 1000]
+    offs = np.array([0, 7, 100, 40000, 3], np.int32)
+    cu = synth.cu_seqlens(lens)
+    x = synth.normal_bf16(41, synth.T_Q, (int(cu[-1]), heads, 128))
+    y = gpu_rope(x, cu, offs, 41001, inplace)
+    ref = oracle.rope_f32(x, positions(cu, offs), THETA)
+    np.testing.assert_array_equal(y, ref)
+
+
+def test_rope_pass_prefill_workload_bitwise():
+    # the query tensor of the varlen prefill workload, positions 0..len-1
+    cfg = synth.CFG_PREFILL
+    cu = synth.cu_seqlens(cfg["lens"])
+    x = synth.normal_bf16(cfg["seed"], synth.T_Q, (int(cu[-1]), cfg["hq"], 128))
+    y = gpu_rope(x, cu, None, 4096)
+    np.testing.assert_array_equal(y, oracle.rope_f32(x, positions(cu, None), THETA))
+
+
+def test_rope_chunked_positions_equal_full_rows():
+    # a chunk of q_len rows at offset kv_len - q_len gives the full rows' bits
+    cu_full = synth.cu_seqlens([700])
+    x = synth.normal_bf16(43, synth.T_K, (700, 8, 128))
+    full = gpu_rope(x, cu_full, None, 700)
+    chunk = gpu_rope(x[500:], synth.cu_seqlens([200]), np.array([500], np.int32), 700)
+    assert_bitwise((chunk,), (full[500:],), "chunk rows")
+
+
+def run_decode_q(dec, q, rope_max_pos=None):
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    qd = dv.bf16_to_device(q)
+    kp = torch.from_numpy(dec.k_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    vp = torch.from_numpy(dec.v_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    ptd = dv.i32_to_device(dec.page_table)
+    n = len(dec.seqlens)
+    out, outb, lse = empty_outputs(torch, n, dec.hq)
+    p = rlk.make_params(n, dec.hq, dec.hkv, 128, softmax_scale=dec.scale)
+    if rope_max_pos is None:
+        rlk.rlk_attn_decode_paged(p, qd, kp, vp, dec.k_bits.shape[0], dec.page_size, ptd, dec.page_table.shape[1],
+                                  dec.seqlens, out, outb, lse)
+    else:
+        rlk.rlk_attn_decode_paged_rope(p, qd, kp, vp, dec.k_bits.shape[0], dec.page_size, ptd,
+                                       dec.page_table.shape[1], dec.seqlens, table_dev(rope_max_pos), rope_max_pos,
+                                       out, outb, lse)
+    rlk.rlk_attn_check_device_error()
+    return out.cpu().numpy(), outb.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (32, 4), (24, 8)])
+def test_decode_rope_equals_pass_then_decode(hq, hkv):
+    dec = synth.paged_decode_problem(ctx=[1, 17, 128, 129, 1000, 2049], hq=hq, hkv=hkv, seed=44, spare_pages=3)
+    n = len(dec.seqlens)
+    fused = run_decode_q(dec, dec.q, rope_max_pos=4096)
+    q_rot = gpu_rope(dec.q, np.arange(n + 1, dtype=np.int32), dec.seqlens - 1, 4096)
+    plain = run_decode_q(dec, q_rot)
+    assert_bitwise(fused, plain, "in-kernel RoPE vs pass + decode")
+    q_ref = oracle.rope_f32(dec.q, dec.seqlens - 1, THETA)
+    ref_out, ref_lse = oracle.decode_paged_f64(q_ref, dec.k_pool, dec.v_pool, dec.page_table, dec.seqlens, dec.scale)
+    assert_forward_parity(*fused, ref_out, ref_lse, "decode with RoPE")
+
+
+def test_rope_cache_position_identity():
+    # prefill over RoPE'd q and k; decode of the last token (pre-RoPE query,
+    # cache filled with the RoPE'd keys through a permuted page table) gives
+    # the prefill's last row bit for bit
+    torch = torch_cuda()
+    hq, hkv, ctx, ps = 32, 8, 1000, 16
+    q = synth.normal_bf16(45, synth.T_Q, (ctx, hq, 128))
+    k = synth.normal_bf16(45, synth.T_K, (ctx, hkv, 128))
+    v = synth.normal_bf16(45, synth.T_V, (ctx, hkv, 128))
+    cu = np.array([0, ctx], np.int32)
+    q_rot = gpu_rope(q, cu, None, ctx)
+    k_rot = gpu_rope(k, cu, None, ctx)
+    prob = synth.Prefill(q_rot, k_rot, v, cu, cu, hq, hkv, 128, 1.0 / np.sqrt(128), 128)
+    po, pb, pl = run_fused(prob)
+    npg = (ctx + ps - 1) // ps
+    perm = np.random.default_rng(46).permutation(npg).astype(np.int32)
+    kb = np.zeros((npg, ps, hkv, 128), np.uint16)
+    vb = np.zeros((npg, ps, hkv, 128), np.uint16)
+    pad = npg * ps - ctx
+    kb[perm] = np.concatenate([synth.bf16_bits(k_rot), np.zeros((pad, hkv, 128), np.uint16)]).reshape(npg, ps, hkv, 128)
+    vb[perm] = np.concatenate([synth.bf16_bits(v), np.zeros((pad, hkv, 128), np.uint16)]).reshape(npg, ps, hkv, 128)
+    dec = synth.PagedDecode(q[-1:], kb, vb, perm[None, :], np.array([ctx], np.int32), ps, hq, hkv, 128,
+                            1.0 / np.sqrt(128), 46)
+    d = run_decode_q(dec, q[-1:], rope_max_pos=ctx)
+    assert_bitwise(d, (po[-1:], pb[-1:], pl[-1:]), "decode with RoPE vs prefill last row")

@@ -6,6 +6,8 @@ import ctypes
 import os
 import re
 
+import math
+
 import numpy as np
 import pytest
 
@@ -197,3 +199,53 @@ def test_decode_auto_split_choice(lib):
     assert rlk.rlk_attn_decode_auto_split(p1, [131072], 1) == 1  # a single SM gains nothing from splitting
     assert rlk.rlk_attn_decode_auto_split(p4, [32768, 0, 5, 5], 152) == -1
     assert rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 0) == -1
+
+
+def test_rope_table_values_and_validation(lib):
+    t = rlk.rlk_attn_rope_table(1e6, 3)
+    assert t.shape == (3, 128) and t.dtype == np.float32
+    np.testing.assert_array_equal(t[0, :64], np.ones(64, np.float32))   # position 0: cos 0, sin 0
+    np.testing.assert_array_equal(t[0, 64:], np.zeros(64, np.float32))
+    assert t[1, 0] == np.float32(math.cos(1.0)) and t[1, 64] == np.float32(math.sin(1.0))
+    f1 = 1e6 ** (-2.0 / 128)
+    assert t[2, 1] == np.float32(math.cos(2 * f1)) and t[2, 65] == np.float32(math.sin(2 * f1))
+    for theta, max_pos in ((1.0, 4), (float("inf"), 4), (1e6, 0)):
+        with pytest.raises(rlk.RlkError) as e:
+            rlk.rlk_attn_rope_table(theta, max_pos)
+        assert e.value.status == 1
+
+
+def test_rope_rejects_before_any_launch(lib):
+    # every case fails host validation before the library touches the
+    # device, so the placeholder pointers never reach a kernel
+    p = rlk.make_params(2)
+    cu = [0, 10, 20]
+    bad = [
+        dict(offs=[0, 95], max_pos=100),          # sequence 1 reaches position 104
+        dict(offs=[-1, 0], max_pos=100),          # negative offset
+        dict(x=17),                               # unaligned
+        dict(heads=0),
+        dict(cu=[1, 10, 20]),                     # does not start at 0
+        dict(cu=[0, 10, 5]),                      # not monotone
+        dict(table=None),
+    ]
+    for b in bad:
+        with pytest.raises(rlk.RlkError) as e:
+            rlk.rlk_attn_rope(p, b.get("x", 16), 16, b.get("heads", 8), b.get("cu", cu), b.get("offs", None),
+                              b.get("table", 16), b.get("max_pos", 100), stream=0)
+        assert e.value.status == 1, b
+
+
+def test_decode_rope_rejects_before_any_launch(lib):
+    def call(p, seqlens=(50,), table=16, max_pos=4096):
+        rlk.rlk_attn_decode_paged_rope(p, 16, 16, 16, 4, 16, 16, 4, list(seqlens), table, max_pos, 16, None, 16,
+                                       stream=0)
+    p = rlk.make_params(1)
+    for kw, status in ((dict(table=None), 1), (dict(max_pos=40), 1)):  # no table; position 49 past 40
+        with pytest.raises(rlk.RlkError) as e:
+            call(p, **kw)
+        assert e.value.status == status
+    for prm in (rlk.make_params(1, kv_block_size=64), rlk.make_params(1, num_q_heads=32, num_kv_heads=2)):
+        with pytest.raises(rlk.RlkError) as e:  # the in-kernel RoPE lives in the transposed decode kernel only
+            call(prm)
+        assert e.value.status == 2
