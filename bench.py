@@ -593,7 +593,7 @@ def run_reference(args):
 
 def run_profile(args):
     """Run one entry point a few times without timing, for ncu captures:
-    --profile prefill|states|merge|decode|decode-small|backward."""
+    --profile prefill|states|merge|decode|decode-small|decode-long|rope|backward."""
     import torch
     import deterministic_context_attention_gb300 as rlk
     from deterministic_context_attention_gb300 import build as rbuild
@@ -602,7 +602,40 @@ def run_profile(args):
     rlk.load()
     stream = torch.cuda.current_stream()
     n = args.profile_iters
-    if args.profile == "backward":
+    if args.profile == "rope":
+        # RoPE in place on the varlen prefill workload's Q and K
+        cfg = synth.CFG_PREFILL
+        cu = synth.cu_seqlens(cfg["lens"])
+        t = int(cu[-1])
+        q = dv.bf16_to_device(synth.normal_bf16(cfg["seed"], synth.T_Q, (t, cfg["hq"], 128)))
+        k = dv.bf16_to_device(synth.normal_bf16(cfg["seed"], synth.T_K, (t, cfg["hkv"], 128)))
+        max_pos = max(cfg["lens"])
+        table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
+        pr = rlk.make_params(len(cfg["lens"]))
+        for _ in range(n):
+            rlk.rlk_attn_rope(pr, q, q, cfg["hq"], cu, None, table, max_pos, stream=stream)
+            rlk.rlk_attn_rope(pr, k, k, cfg["hkv"], cu, None, table, max_pos, stream=stream)
+    elif args.profile == "decode-long":
+        # few long sequences: 4 x 32768 tokens, split decode with split_k 4
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        ctx = np.full(4, 32768, np.int32)
+        n_pages = int(((ctx + 15) // 16).sum())
+        pt = synth.rng(5, synth.T_PAGES).permutation(n_pages).astype(np.int32).reshape(4, -1).copy()
+        kp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+        vp = torch.randn((n_pages, 16, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+        qd = torch.randn((4, 32, 128), generator=g, device="cuda").to(torch.bfloat16)
+        ptd = dv.i32_to_device(pt)
+        pd = rlk.make_params(4, 32, 8, 128)
+        o = torch.empty((4, 32, 128), dtype=torch.float32, device="cuda")
+        ob = torch.empty((4, 32, 128), dtype=torch.bfloat16, device="cuda")
+        l = torch.empty((4, 32), dtype=torch.float32, device="cuda")
+        ws = torch.empty(rlk.rlk_attn_workspace_size(pd, rlk.RLK_OP_DECODE_SPLIT, None, ctx), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(n):
+            rlk.rlk_attn_decode_paged_splitk(pd, qd, kp, vp, n_pages, 16, ptd, pt.shape[1], ctx, 4, o, ob, l, ws,
+                                             stream=stream)
+    elif args.profile == "backward":
         prob, p, (q, k, v, out, do, lse, dq, dk, dvv, ws), _ = backward_workload(torch, rlk, dv)
         for _ in range(n):
             rlk.rlk_attn_backward(p, q, k, v, out, do, lse, prob.cu_q, -1, dq, dk, dvv, ws, stream=stream)
@@ -670,7 +703,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-rows", type=int, default=512)
     ap.add_argument("--profile", default=None,
-                    choices=["prefill", "states", "merge", "decode", "decode-small", "backward"])
+                    choices=["prefill", "states", "merge", "decode", "decode-small", "decode-long", "rope",
+                             "backward"])
     ap.add_argument("--profile-iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile:
