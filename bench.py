@@ -438,12 +438,31 @@ def measure_rope(torch, rlk, dv, peaks, flush, stream, args):
         rlk.rlk_attn_rope(pr, q, q, cfg["hq"], cu, None, table, max_pos, stream=stream)
         rlk.rlk_attn_rope(pr, k, k, cfg["hkv"], cu, None, table, max_pos, stream=stream)
     ts = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+    # the same after a flush that leaves L2 clean: the 512 MB write leaves up
+    # to 129 MB of dirty lines whose write-back a 182 MB pass otherwise pays
+    reader = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        reader.sum()
+        torch.cuda._sleep(400000)
+        if i >= args.warmup:
+            starts[i - args.warmup].record(stream)
+        step()
+        if i >= args.warmup:
+            ends[i - args.warmup].record(stream)
+    torch.cuda.synchronize()
+    tc = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    del reader
     rlk.rlk_attn_check_device_error(stream)
     nbytes = t * (cfg["hq"] + cfg["hkv"]) * 512
-    ms = float(np.mean(ts))
-    gbs = nbytes / (ms * 1e-3) / 1e9
+    ms, msc = float(np.mean(ts)), float(np.mean(tc))
+    gbs, gbsc = nbytes / (ms * 1e-3) / 1e9, nbytes / (msc * 1e-3) / 1e9
     return {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": nbytes, "launches_per_step": 2,
             "frac": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
+            "clean_l2": {"ms": round(msc, 4), "gbs": round(gbsc, 1), "frac": round(gbsc / peaks["hbm_gbs"], 4),
+                         "flush": "512 MB write, then a 256 MB read (L2 left holding clean lines)"},
             "workload": "RoPE in place on the varlen prefill Q [8897,32,128] and K [8897,8,128] (BF16)"}
 
 
