@@ -45,11 +45,15 @@ struct alignas(16) BwdItem {
   int32_t rows;   // dQ: rows of the tile written; dK/dV: unused
 };
 
-constexpr int kMaxBwdItems = 1800;
+constexpr int kMaxBwdTiles = 1800;
 
+// The item list holds tiles; item i is head i mod item_heads of tile
+// i / item_heads (the heads of a tile are adjacent in the longest-first
+// order), so a launch takes kMaxBwdTiles * heads items.
 struct BwdParams {
   ErrWord* err;
   int32_t hq, hkv, group, num_items;
+  int32_t item_heads, pad0;
   int64_t t_pad;        // row stride of the transposed lse / Delta
   float scale, scale_log2;
   const float* lse_t;   // [hq][t_pad]
@@ -58,8 +62,15 @@ struct BwdParams {
   float* dk;
   float* dv;
   int32_t cu[kMaxSeqs + 1];
-  BwdItem items[kMaxBwdItems];
+  BwdItem items[kMaxBwdTiles];
 };
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int item) {
+  const int t = item / p.item_heads;
+  BwdItem it = p.items[t];
+  it.head = item - t * p.item_heads;
+  return it;
+}
 
 // ------------------------------------------------------------------ preprocess
 struct PrepParams {
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(384, 1)
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
       const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
       if (item >= p.num_items) continue;
-      const BwdItem it = p.items[item];
+      const BwdItem it = bwd_item(p, item);
       int len, nsteps;
       item_steps(it, len, nsteps);
       const int tok0 = p.cu[it.seq];
@@ -245,7 +256,7 @@ __global__ void __launch_bounds__(384, 1)
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
       const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
       if (item >= p.num_items) continue;
-      const BwdItem it = p.items[item];
+      const BwdItem it = bwd_item(p, item);
       int len, nsteps;
       item_steps(it, len, nsteps);
       bool ok = mbar_wait(&bars[L::kResFull], res_it & 1, abort, p.err, 0x611);
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(384, 1)
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
       const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
       if (item >= p.num_items) continue;
-      const BwdItem it = p.items[item];
+      const BwdItem it = bwd_item(p, item);
       int len, nsteps;
       item_steps(it, len, nsteps);
       const int tok0 = p.cu[it.seq];
@@ -547,17 +558,18 @@ int owner_of(int pos, int n, int cp, int layout) {
 }
 
 template <int KIND>
-cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& items, const CUtensorMap& mq,
+cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& tiles, int heads, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int num_sms,
                        cudaStream_t stream) {
   auto kern = rlk_bwd_kernel<KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kAlloc);
   if (e != cudaSuccess) return e;
-  for (size_t i0 = 0; i0 < items.size(); i0 += kMaxBwdItems) {
-    const size_t n = std::min(items.size() - i0, static_cast<size_t>(kMaxBwdItems));
-    std::copy(items.begin() + i0, items.begin() + i0 + n, bp->items);
-    bp->num_items = static_cast<int32_t>(n);
-    const int grid = std::min(static_cast<int>(n), num_sms);
+  bp->item_heads = heads;
+  for (size_t i0 = 0; i0 < tiles.size(); i0 += kMaxBwdTiles) {
+    const size_t n = std::min(tiles.size() - i0, static_cast<size_t>(kMaxBwdTiles));
+    std::copy(tiles.begin() + i0, tiles.begin() + i0 + n, bp->items);
+    bp->num_items = static_cast<int32_t>(n) * heads;
+    const int grid = std::min(bp->num_items, num_sms);
     kern<<<grid, 384, BwdLayout::kAlloc, stream>>>(*bp, mq, mk, mv, mdo);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -629,7 +641,9 @@ rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k
   bp->dv = dv;
   for (int s = 0; s <= prm->num_seqs; ++s) bp->cu[s] = cu[s];
 
-  // dK/dV items: (seq, KV head, KV block), most query blocks first
+  // dK/dV tiles: (seq, KV block), most query blocks first, each taken by
+  // every KV head; dQ tiles: (seq, query tile), most KV blocks first, each
+  // taken by every query head
   std::vector<std::pair<int, BwdItem>> kv;
   std::vector<std::pair<int, BwdItem>> qi;
   for (int s = 0; s < prm->num_seqs; ++s) {
@@ -637,7 +651,7 @@ rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k
     const int nb = (len + 127) / 128;
     for (int j = 0; j < nb; ++j) {
       if (cp_rank >= 0 && owner_of(j * 128, len, prm->cp_size, prm->cp_layout) != cp_rank) continue;
-      for (int g = 0; g < prm->num_kv_heads; ++g) kv.push_back({nb - j, BwdItem{s, g, j, 128}});
+      kv.push_back({nb - j, BwdItem{s, 0, j, 128}});
     }
     std::vector<std::pair<int, int>> ranges;
     if (cp_rank < 0) ranges.push_back({0, len});
@@ -646,19 +660,21 @@ rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k
       for (int r0 = rg.first; r0 < rg.second; r0 += 128) {
         const int rows = std::min(128, rg.second - r0);
         const int cost = (r0 + rows - 1) / 128 + 1;
-        for (int h = 0; h < prm->num_q_heads; ++h) qi.push_back({cost, BwdItem{s, h, r0, rows}});
+        qi.push_back({cost, BwdItem{s, 0, r0, rows}});
       }
   }
   auto by_cost = [](const std::pair<int, BwdItem>& a, const std::pair<int, BwdItem>& b) { return a.first > b.first; };
   std::stable_sort(kv.begin(), kv.end(), by_cost);
   std::stable_sort(qi.begin(), qi.end(), by_cost);
-  std::vector<BwdItem> items;
-  for (auto& x : kv) items.push_back(x.second);
-  if (!items.empty() && launch_bwd<0>(bp.get(), items, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
+  std::vector<BwdItem> tiles;
+  for (auto& x : kv) tiles.push_back(x.second);
+  if (!tiles.empty() &&
+      launch_bwd<0>(bp.get(), tiles, prm->num_kv_heads, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
     return RLK_ERR_CUDA;
-  items.clear();
-  for (auto& x : qi) items.push_back(x.second);
-  if (!items.empty() && launch_bwd<1>(bp.get(), items, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
+  tiles.clear();
+  for (auto& x : qi) tiles.push_back(x.second);
+  if (!tiles.empty() &&
+      launch_bwd<1>(bp.get(), tiles, prm->num_q_heads, mq, mk, mv, mdo, num_sms, stream) != cudaSuccess)
     return RLK_ERR_CUDA;
   return RLK_OK;
 }
