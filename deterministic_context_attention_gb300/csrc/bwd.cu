@@ -117,8 +117,9 @@ struct BwdLayout {
   static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;
   static constexpr int kBarOff = kVecOff + 2 * 8 * 2 * 64 * 4;
   // barriers
-  static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 7,
-                       kAccFull = 8, kAccEmpty = 9, kNumBars = 10;
+  // S/dP and P/dS barriers come in pairs: one per 64-column half of a step
+  static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 8,
+                       kAccFull = 10, kAccEmpty = 11, kNumBars = 12;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kTotal = kMiscOff + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -157,8 +158,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars[L::kStFull + s], 1);
       mbar_init(&bars[L::kStEmpty + s], 1);
     }
-    mbar_init(&bars[L::kSFull], 1);
-    mbar_init(&bars[L::kPFull], 256);  // both column halves
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bars[L::kSFull + h], 1);
+      mbar_init(&bars[L::kPFull + h], 128);  // the four warps of the half
+    }
     mbar_init(&bars[L::kAccFull], 1);
     mbar_init(&bars[L::kAccEmpty], 128);
     *abort = 0;
@@ -249,7 +252,14 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdK = idesc_bf16(128, 128, false, false);  // both operands K-major
+    // Each step's S/dP is issued as two N = 64 halves (columns 0-63, 64-127
+    // of TMEM and of the step's query rows or keys), so the elementwise step
+    // of one half runs while the tensor core works on the other:
+    //   S/dP_0(t) S/dP_1(t) | acc_0(t) S/dP_0(t+1) | acc_1(t) S/dP_1(t+1) | ...
+    // where acc_c takes K-steps 4c..4c+3 (hi, then lo) of dV/dK or dQ.  The
+    // tensor core runs them in issue order, so S/dP_c(t+1) overwrites the
+    // half only after acc_c(t) has read it.
+    constexpr uint32_t kIdK = idesc_bf16(128, 64, false, false);   // both operands K-major, N = 64
     constexpr uint32_t kIdMN = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
     uint32_t res_it = 0, st_it = 0, s_it = 0, acc_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
@@ -260,59 +270,88 @@ __global__ void __launch_bounds__(384, 1)
       int len, nsteps;
       item_steps(it, len, nsteps);
       bool ok = mbar_wait(&bars[L::kResFull], res_it & 1, abort, p.err, 0x611);
-      ok = ok && mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
       if (!__all_sync(0xffffffffu, ok)) break;
       ++res_it;
-      bool fail = false;
-      for (int t = 0; t < nsteps; ++t) {
-        const uint32_t stage = st_it % L::kStages;
-        bool w = mbar_wait(&bars[L::kStFull + stage], (st_it / L::kStages) & 1, abort, p.err, 0x613);
-        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-        tc_fence_after();
-        const uint32_t st_addr = smem_u32(st_base + stage * 2 * L::kTile);
-        // resident A = (K_j, V_j) [dK/dV] or (Q_i, dO_i) [dQ]; streamed B = the other pair
+      // S^T|S and dP^T|dP of half c of step t (stream stage of step t)
+      auto issue_sdp = [&](uint32_t st_addr, int c) {
         if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK, k > 0);
+          const uint32_t boff = static_cast<uint32_t>(c) * 64 * 128;  // rows 64c.. of the streamed tiles
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK, k > 0);
-          umma_commit(&bars[L::kSFull]);
+            umma_ss(tm_s + 64 * c, kdesc(res_addr, k), kdesc(st_addr + boff, k), kIdK, k > 0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tm_dp + 64 * c, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile + boff, k), kIdK, k > 0);
+          umma_commit(&bars[L::kSFull + c]);
         }
         __syncwarp();
-        w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
-        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-        ++s_it;
-        tc_fence_after();
+      };
+      // K-steps 4c..4c+3 of the accumulators (first: the item's first product)
+      auto issue_acc = [&](uint32_t st_addr, int c, bool first) {
         if (lane == 0) {
-          const uint32_t first = (t == 0) ? 0u : 1u;
+          const int k0 = 4 * c;
           if (KIND == 0) {
             // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: N = D, K = query rows)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma_ts(tm_acc0, tm_s + 16 * k, mndesc(st_addr + L::kTile, k), kIdMN, (k > 0) ? 1u : first);
+            for (int k = k0; k < k0 + 4; ++k)
+              umma_ts(tm_acc0, tm_s + 16 * k, mndesc(st_addr + L::kTile, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) umma_ts(tm_acc0, tm_s + 16 * k + 8, mndesc(st_addr + L::kTile, k), kIdMN, 1u);
+            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc0, tm_s + 16 * k + 8, mndesc(st_addr + L::kTile, k), kIdMN, 1u);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma_ts(tm_acc1, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (k > 0) ? 1u : first);
+            for (int k = k0; k < k0 + 4; ++k)
+              umma_ts(tm_acc1, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
+            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
           } else {
             // dQ += dS K_j  (B = K_j MN-major: N = D, K = keys)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (k > 0) ? 1u : first);
+            for (int k = k0; k < k0 + 4; ++k)
+              umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
-          }
-          umma_commit(&bars[L::kStEmpty + stage]);
-          if (t + 1 == nsteps) {
-            umma_commit(&bars[L::kAccFull]);
-            umma_commit(&bars[L::kResEmpty]);
+            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
           }
         }
         __syncwarp();
+      };
+      auto stage_addr = [&](uint32_t si) { return smem_u32(st_base + (si % L::kStages) * 2 * L::kTile); };
+      bool fail = false;
+      {
+        bool w = mbar_wait(&bars[L::kStFull + st_it % L::kStages], (st_it / L::kStages) & 1, abort, p.err, 0x613);
+        if (!__all_sync(0xffffffffu, w)) break;
+        tc_fence_after();
+        issue_sdp(stage_addr(st_it), 0);
+        issue_sdp(stage_addr(st_it), 1);
+      }
+      // the accumulators are free once the previous item's epilogue read them
+      ok = mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      for (int t = 0; t < nsteps; ++t) {
+        const uint32_t cur = st_it, nxt = st_it + 1;
+        const bool more = t + 1 < nsteps;
+        for (int c = 0; c < 2; ++c) {
+          bool w = mbar_wait(&bars[L::kPFull + c], s_it & 1, abort, p.err, 0x614);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          tc_fence_after();
+          issue_acc(stage_addr(cur), c, t == 0 && c == 0);
+          if (c == 1 && lane == 0) {
+            umma_commit(&bars[L::kStEmpty + cur % L::kStages]);  // step t's stage is no longer read
+            if (!more) {
+              umma_commit(&bars[L::kAccFull]);
+              umma_commit(&bars[L::kResEmpty]);
+            }
+          }
+          __syncwarp();
+          if (more) {
+            if (c == 0) {
+              w = mbar_wait(&bars[L::kStFull + nxt % L::kStages], (nxt / L::kStages) & 1, abort, p.err, 0x615);
+              if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+              tc_fence_after();
+            }
+            issue_sdp(stage_addr(nxt), c);
+          }
+        }
+        if (fail) break;
+        ++s_it;
         ++st_it;
       }
       if (fail) break;
@@ -372,7 +411,7 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           col0 = t * 128;
         }
-        bool w = mbar_wait(&bars[L::kSFull], s_it & 1, abort, p.err, 0x621);
+        bool w = mbar_wait(&bars[L::kSFull + half], s_it & 1, abort, p.err, 0x621);
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
         // every element of this warp's half is visible: no per-element mask
@@ -438,7 +477,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[L::kPFull]);
+        mbar_arrive(&bars[L::kPFull + half]);
         ++s_it;
       }
       if (fail) break;
