@@ -464,15 +464,17 @@ __global__ void __launch_bounds__(384, 1)
                                                 make_float2(da[u], da[u + 1])));
               const int slot = ((e + u) >> 4) * 16 + (((e + u) & 15) >> 1);
               uint32_t hi, lo;
-              split_pair2(pp, hi, lo);
-              pw[slot] = hi;
-              pw[slot + 8] = lo;
+              if (KIND == 0) {  // dQ reads only dS
+                split_pair2(pp, hi, lo);
+                pw[slot] = hi;
+                pw[slot + 8] = lo;
+              }
               split_pair2(ds, hi, lo);
               dw[slot] = hi;
               dw[slot + 8] = lo;
             }
           }
-          tmem_st32(tm_s + lane_off + colc, pw);
+          if (KIND == 0) tmem_st32(tm_s + lane_off + colc, pw);
           tmem_st32(tm_dp + lane_off + colc, dw);
         }
         tmem_st_wait();
