@@ -587,19 +587,37 @@ __global__ void __launch_bounds__(512, 1)
         } else if (MODE == kModeStates) {
           tmem_ld32(ta, x0);
           tmem_ld32(ta + 32, x1);
+          // the warp's 32 rows are consecutive pairs of the slab: their
+          // state rows are one contiguous 16 KB span
           const int64_t pair = it.slab_off + static_cast<int64_t>(it.head) * it.slab_rc +
                                (it.row_begin + r - it.slab_rb);
-          float4* dst = reinterpret_cast<float4*>(p.state_o + pair * kHeadDim);
+          const int64_t pair0 = pair - lane;
+          const uint32_t has_mask = __ballot_sync(0xffffffffu, has);
+          // each 32-column chunk goes through shared memory (chunk j of a
+          // row in slot j ^ (row & 7)) and leaves as whole 128-byte lines,
+          // four rows per store instruction
+          float4* stg = reinterpret_cast<float4*>(smem + L::kEpiOff + (warp & 3) * (32 * 128));
+          auto put_chunk = [&](const uint32_t (&xa)[32], int c) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              stg[lane * 8 + (j ^ (lane & 7))] =
+                  make_float4(state_elem(__uint_as_float(xa[4 * j]), rcp), state_elem(__uint_as_float(xa[4 * j + 1]), rcp),
+                              state_elem(__uint_as_float(xa[4 * j + 2]), rcp), state_elem(__uint_as_float(xa[4 * j + 3]), rcp));
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int rr = 4 * k + (lane >> 3), jj = lane & 7;
+              const float4 v = stg[rr * 8 + (jj ^ (rr & 7))];
+              if ((has_mask >> rr) & 1u)
+                reinterpret_cast<float4*>(p.state_o + (pair0 + rr) * kHeadDim + 32 * c)[jj] = v;
+            }
+            __syncwarp();
+          };
           tmem_ld_wait(x0);
           tmem_ld_wait(x1);
-          if (has) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              dst[e / 4] = make_float4(state_elem(__uint_as_float(x0[e]), rcp), state_elem(__uint_as_float(x0[e + 1]), rcp),
-                                       state_elem(__uint_as_float(x0[e + 2]), rcp), state_elem(__uint_as_float(x0[e + 3]), rcp));
-              dst[8 + e / 4] = make_float4(state_elem(__uint_as_float(x1[e]), rcp), state_elem(__uint_as_float(x1[e + 1]), rcp),
-                                           state_elem(__uint_as_float(x1[e + 2]), rcp), state_elem(__uint_as_float(x1[e + 3]), rcp));
-            }
+          if (has_mask) {
+            put_chunk(x0, 0);
+            put_chunk(x1, 1);
           }
           tmem_ld32(ta + 64, x0);
           tmem_ld32(ta + 96, x1);
@@ -607,16 +625,11 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld_wait(x1);
           tc_fence_before();
           mbar_arrive(&bars[L::kPVEmpty + buf]);  // PV read: the buffer is free
-          if (has) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              dst[16 + e / 4] = make_float4(state_elem(__uint_as_float(x0[e]), rcp), state_elem(__uint_as_float(x0[e + 1]), rcp),
-                                            state_elem(__uint_as_float(x0[e + 2]), rcp), state_elem(__uint_as_float(x0[e + 3]), rcp));
-              dst[24 + e / 4] = make_float4(state_elem(__uint_as_float(x1[e]), rcp), state_elem(__uint_as_float(x1[e + 1]), rcp),
-                                            state_elem(__uint_as_float(x1[e + 2]), rcp), state_elem(__uint_as_float(x1[e + 3]), rcp));
-            }
-            p.state_lse[pair] = lse_b;
+          if (has_mask) {
+            put_chunk(x0, 2);
+            put_chunk(x1, 3);
           }
+          if (has) p.state_lse[pair] = lse_b;
         } else {
           tmem_ld32(ta, x0);
           float Lp = 0.f, alpha = 0.f, beta = 0.f;
