@@ -26,6 +26,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -90,8 +91,11 @@ class Clocks:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            # raw samples go to RLK_BENCH_CLOCKS_DIR (default: the temp directory);
+            # the JSON line carries their summary
+            d = os.environ.get("RLK_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+            os.makedirs(d, exist_ok=True)
+            self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
