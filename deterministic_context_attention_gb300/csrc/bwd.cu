@@ -315,6 +315,63 @@ __global__ void __launch_bounds__(384, 1)
       };
       auto stage_addr = [&](uint32_t si) { return smem_u32(st_base + (si % L::kStages) * 2 * L::kTile); };
       bool fail = false;
+      if constexpr (KIND == 1) {
+        // dQ: one N = 128 S/dP per step and the accumulation after both
+        // halves' elementwise steps.  Its single accumulator makes S/dP the
+        // larger part of its tensor work, so the N = 64 halves' lower MMA
+        // rate costs more than their overlap gains (measured 1.6 % slower
+        // for the whole backward); the accumulation order is the halves'.
+        constexpr uint32_t kIdK128 = idesc_bf16(128, 128, false, false);
+        auto issue_sdp128 = [&](uint32_t st_addr) {
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK128, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK128, k > 0);
+            umma_commit(&bars[L::kSFull]);
+            umma_commit(&bars[L::kSFull + 1]);
+          }
+          __syncwarp();
+        };
+        {
+          bool w = mbar_wait(&bars[L::kStFull + st_it % L::kStages], (st_it / L::kStages) & 1, abort, p.err, 0x613);
+          if (!__all_sync(0xffffffffu, w)) break;
+          tc_fence_after();
+          issue_sdp128(stage_addr(st_it));
+        }
+        ok = mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        for (int t = 0; t < nsteps; ++t) {
+          const uint32_t cur = st_it, nxt = st_it + 1;
+          const bool more = t + 1 < nsteps;
+          bool w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
+          w = w && mbar_wait(&bars[L::kPFull + 1], s_it & 1, abort, p.err, 0x614);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          tc_fence_after();
+          issue_acc(stage_addr(cur), 0, t == 0);
+          issue_acc(stage_addr(cur), 1, false);
+          if (lane == 0) {
+            umma_commit(&bars[L::kStEmpty + cur % L::kStages]);
+            if (!more) {
+              umma_commit(&bars[L::kAccFull]);
+              umma_commit(&bars[L::kResEmpty]);
+            }
+          }
+          __syncwarp();
+          if (more) {
+            w = mbar_wait(&bars[L::kStFull + nxt % L::kStages], (nxt / L::kStages) & 1, abort, p.err, 0x615);
+            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+            tc_fence_after();
+            issue_sdp128(stage_addr(nxt));
+          }
+          ++s_it;
+          ++st_it;
+        }
+        if (fail) break;
+        ++acc_it;
+        continue;
+      }
       {
         bool w = mbar_wait(&bars[L::kStFull + st_it % L::kStages], (st_it / L::kStages) & 1, abort, p.err, 0x613);
         if (!__all_sync(0xffffffffu, w)) break;
