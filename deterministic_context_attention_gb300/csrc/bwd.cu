@@ -252,13 +252,13 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Each step's S/dP is issued as two N = 64 halves (columns 0-63, 64-127
-    // of TMEM and of the step's query rows or keys), so the elementwise step
+    // dK/dV: each step's S/dP is issued as two N = 64 halves (columns 0-63,
+    // 64-127 of TMEM and of the step's query rows), so the elementwise step
     // of one half runs while the tensor core works on the other:
     //   S/dP_0(t) S/dP_1(t) | acc_0(t) S/dP_0(t+1) | acc_1(t) S/dP_1(t+1) | ...
-    // where acc_c takes K-steps 4c..4c+3 (hi, then lo) of dV/dK or dQ.  The
+    // where acc_c takes K-steps 4c..4c+3 (hi, then lo) of dV and dK.  The
     // tensor core runs them in issue order, so S/dP_c(t+1) overwrites the
-    // half only after acc_c(t) has read it.
+    // half only after acc_c(t) has read it.  dQ issues S/dP whole (below).
     constexpr uint32_t kIdK = idesc_bf16(128, 64, false, false);   // both operands K-major, N = 64
     constexpr uint32_t kIdMN = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
     uint32_t res_it = 0, st_it = 0, s_it = 0, acc_it = 0;
