@@ -16,6 +16,16 @@ three streams with double-buffered device tensors, as a serving loop would
 run them.  Under torchrun every rank runs the same batch
 on its own GPU (weak scaling, no collective on the data path).
 
+Rank 0 adds, outside the timed region of the headline, one object per other
+path (each with its own CUDA-event timing and L2 flush): "merge" (the
+canonical fold of the prefill's CP=1 state table), "states" (the state
+producer), "decode" (64 sequences, contexts U[512, 32768], 16-token pages),
+"decode_long" (4 x 32768 tokens: single pass against the split decode),
+"rope" (the RoPE pass over the prefill's Q and K, also after a flush that
+leaves L2 clean), "backward" (2 x 4096) and "chunked" (2 x 8192 in chunks of
+2048); --no-extras skips them.  --profile NAME runs one path a few times,
+untimed, for ncu.
+
 --impl reference times the CPU oracle (FP64 definition) on the host cores on
 a bounded sample of the same workload's rows, in the same metric.
 """
