@@ -349,20 +349,49 @@ rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q,
   if ((st = make_map(&mq, q, params->num_q_heads, tq, 1, rlk::kTileRows))) return st;
   if ((st = make_map(&mk, k, params->num_kv_heads, tk, 1, params->kv_block_size))) return st;
   if ((st = make_map(&mv, v, params->num_kv_heads, tk, 1, params->kv_block_size))) return st;
-  std::vector<rlk::FwdTile> tiles;
-  for (const rlk_attn_slab& sl : plan.slabs) {
-    for (int r = 0; r < sl.row_count; r += rlk::kTileRows) {
-      rlk::FwdTile t;
-      t.seq = sl.seq;
-      t.row_begin = sl.row_begin + r;
-      t.row_count = std::min(rlk::kTileRows, sl.row_count - r);
-      t.block = sl.block;
-      t.slab_offset = sl.offset;
-      t.slab_row_begin = sl.row_begin;
-      t.slab_row_count = sl.row_count;
-      tiles.push_back(t);
+  // Items: a 128-row tile of a sequence's query rows and a run of
+  // consecutive blocks this rank produces (the slabs of a run follow each
+  // other in the plan, so the kernel derives each block's slab from the
+  // first); longest runs first.  Rows of a tile that precede a block's slab
+  // see none of its keys and write nothing for it.
+  const int B = params->kv_block_size;
+  std::vector<std::vector<int64_t>> slab_of(params->num_seqs);  // slab offset per (seq, block), -1 if not produced
+  for (int s = 0; s < params->num_seqs; ++s)
+    slab_of[s].assign((cu_seqlens_k[s + 1] - cu_seqlens_k[s] + B - 1) / B, -1);
+  for (const rlk_attn_slab& sl : plan.slabs) slab_of[sl.seq][sl.block] = sl.offset;
+  std::vector<std::pair<int, rlk::FwdTile>> costed;
+  for (int s = 0; s < params->num_seqs; ++s) {
+    const int ql = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+    const int kl = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+    for (int r0 = 0; r0 < ql; r0 += rlk::kTileRows) {
+      const int rows = std::min(rlk::kTileRows, ql - r0);
+      const int nbt = (kl - ql + r0 + rows - 1) / B + 1;  // blocks the tile's last row sees
+      for (int b = 0; b < nbt;) {
+        if (slab_of[s][b] < 0) {
+          ++b;
+          continue;
+        }
+        int e = b;
+        while (e < nbt && slab_of[s][e] >= 0) ++e;
+        rlk::FwdTile t;
+        std::memset(&t, 0, sizeof(t));
+        t.seq = s;
+        t.row_begin = r0;
+        t.row_count = rows;
+        t.block = b;
+        t.slab_offset = slab_of[s][b];
+        t.slab_row_count = e - b;
+        costed.push_back({e - b, t});
+        b = e;
+      }
     }
   }
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
+                     return a.first > b.first;
+                   });
+  std::vector<rlk::FwdTile> tiles;
+  for (auto& c : costed) tiles.push_back(c.second);
   auto fp = std::make_unique<rlk::FwdParams>();
   base_fwd(fp.get(), params, dev, rlk::kModeStates);
   fill_seqs(fp.get(), params, cu_seqlens_q, cu_seqlens_k);

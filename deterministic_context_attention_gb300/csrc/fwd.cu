@@ -84,7 +84,6 @@ struct FwdLayout {
 
 struct ItemInfo {
   int seq, head, row_begin, row_count, nb, blk0, q_len, kv_len, q_tok0, k_tok0;
-  int slab_rb, slab_rc;
   int64_t slab_off;
 };
 
@@ -103,7 +102,6 @@ __device__ __forceinline__ ItemInfo item_info(const FwdParams& p, int item) {
     it.k_tok0 = 0;
     it.blk0 = 0;
     it.nb = (it.kv_len + p.block - 1) / p.block;
-    it.slab_rb = it.slab_rc = 0;
     it.slab_off = 0;
   } else {
     const int tile = item / p.hq;
@@ -118,15 +116,13 @@ __device__ __forceinline__ ItemInfo item_info(const FwdParams& p, int item) {
     it.kv_len = p.cu_k[t.seq + 1] - it.k_tok0;
     if (MODE == kModeStates) {
       it.blk0 = t.block;
-      it.nb = 1;
+      it.nb = t.slab_row_count;  // a run of consecutive blocks of the rank
     } else {
       const int pmax = it.kv_len - it.q_len + t.row_begin + t.row_count - 1;
       it.blk0 = 0;
       it.nb = pmax / p.block + 1;
     }
     it.slab_off = t.slab_offset;
-    it.slab_rb = t.slab_row_begin;
-    it.slab_rc = t.slab_row_count;
   }
   return it;
 }
@@ -569,6 +565,7 @@ __global__ void __launch_bounds__(512, 1)
       const bool valid = row_of_lane<MODE>(r) < it.row_count;
       const bool warp_rows = __any_sync(0xffffffffu, valid);
       float Lrun = -INFINITY;
+      int64_t slab_off = it.slab_off;  // states: the slab of block blk0 + j
       bool fail = false;
       for (int j = 0; j < it.nb; ++j) {
         const uint32_t buf = pv_it & 1;
@@ -589,8 +586,10 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(ta + 32, x1);
           // the warp's 32 rows are consecutive pairs of the slab: their
           // state rows are one contiguous 16 KB span
-          const int64_t pair = it.slab_off + static_cast<int64_t>(it.head) * it.slab_rc +
-                               (it.row_begin + r - it.slab_rb);
+          const int slab_rb = max(0, (it.blk0 + j) * B - (it.kv_len - it.q_len));
+          const int slab_rc = it.q_len - slab_rb;
+          const int64_t pair = slab_off + static_cast<int64_t>(it.head) * slab_rc + (it.row_begin + r - slab_rb);
+          slab_off += static_cast<int64_t>(slab_rc) * p.hq;
           const int64_t pair0 = pair - lane;
           const uint32_t has_mask = __ballot_sync(0xffffffffu, has);
           // each 32-column chunk goes through shared memory (chunk j of a

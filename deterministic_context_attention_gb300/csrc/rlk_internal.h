@@ -34,11 +34,15 @@ struct alignas(16) FwdTile {
   int32_t seq;
   int32_t row_begin;       // first query row, relative to the sequence's first query row
   int32_t row_count;       // rows of the tile that are written (<= 128)
-  int32_t block;           // states mode: the global block; otherwise -1
-  int64_t slab_offset;     // states mode: first (row, head) pair of the slab
-  int32_t slab_row_begin;  // states mode: first row the slab covers
-  int32_t slab_row_count;  // states mode: rows the slab covers
+  int32_t block;           // states mode, split decode: the first global block; otherwise -1
+  int64_t slab_offset;     // states mode: first (row, head) pair of that block's slab
+  int32_t slab_row_begin;  // unused (0)
+  int32_t slab_row_count;  // states mode, split decode: consecutive blocks from `block`
 };
+// States mode: the slabs of consecutive blocks follow each other in the
+// state table, and block b's slab covers rows max(0, b*B - (kv_len - q_len))
+// .. q_len - 1 with (row, head) pair offset + head * rows + (row - first row),
+// so an item derives every block's slab from the first one.
 
 struct FwdParams {
   ErrWord* err;
