@@ -94,6 +94,7 @@ def load():
             "rlk_attn_rope_table": [ctypes.c_double, i32, P],
             "rlk_attn_rope": [PP, P, P, i32, P, P, P, i32, P],
             "rlk_attn_decode_paged_rope": [PP, P, P, P, i32, i32, P, i32, P, P, i32, P, P, P, P],
+            "rlk_attn_decode_paged_splitk_rope": [PP, P, P, P, i32, i32, P, i32, P, i32, P, i32, P, P, P, P, sz, P],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
             "rlk_attn_workspace_size": [PP, i32, P, P],
             "rlk_attn_check_device_error": [P],
@@ -269,6 +270,20 @@ def rlk_attn_decode_paged_rope(params, q, k_pool, v_pool, n_pages, page_size, pa
                                              _ptr(sl), _ptr(rope_table), int(rope_max_pos), _ptr(out_f32),
                                              _ptr(out_bf16), _ptr(lse), _stream(stream)),
            "rlk_attn_decode_paged_rope")
+
+
+def rlk_attn_decode_paged_splitk_rope(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                                      split_k, rope_table, rope_max_pos, out_f32, out_bf16, lse, workspace,
+                                      workspace_bytes=None, stream=None):
+    sl = _i32_host(seqlens)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().rlk_attn_decode_paged_splitk_rope(ctypes.byref(params), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                                    int(n_pages), int(page_size), _ptr(page_table), int(max_pages),
+                                                    _ptr(sl), int(split_k), _ptr(rope_table), int(rope_max_pos),
+                                                    _ptr(out_f32), _ptr(out_bf16), _ptr(lse), _ptr(workspace),
+                                                    int(workspace_bytes), _stream(stream)),
+           "rlk_attn_decode_paged_splitk_rope")
 
 
 def rlk_attn_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,

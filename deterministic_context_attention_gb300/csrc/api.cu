@@ -685,12 +685,13 @@ int32_t rlk_attn_decode_auto_split(const rlk_attn_params* params, const int32_t*
   return choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, num_sms);
 }
 
-rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const void* q, const void* k_pool,
-                                        const void* v_pool, int32_t n_pages, int32_t page_size,
-                                        const int32_t* page_table, int32_t max_pages,
-                                        const int32_t* seqlens, int32_t split_k, float* out_f32,
-                                        void* out_bf16, float* lse, void* workspace,
-                                        size_t workspace_bytes, rlk_stream_t stream) {
+namespace {
+
+rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, const void* k_pool, const void* v_pool,
+                              int32_t n_pages, int32_t page_size, const int32_t* page_table, int32_t max_pages,
+                              const int32_t* seqlens, int32_t split_k, const float* rope_table,
+                              int32_t rope_max_pos, float* out_f32, void* out_bf16, float* lse, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
@@ -713,6 +714,13 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
     if (seqlens[s] < 1 || static_cast<int64_t>(seqlens[s]) > static_cast<int64_t>(max_pages) * page_size)
       return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: context length %d not in 1..max_pages*page_size", s,
                   seqlens[s]);
+  if (rope_table) {
+    if (!aligned16(rope_table)) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table must be 16-byte aligned");
+    for (int s = 0; s < params->num_seqs; ++s)
+      if (seqlens[s] > rope_max_pos)
+        return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: position %d is past the RoPE table (%d positions)", s,
+                    seqlens[s] - 1, rope_max_pos);
+  }
   const size_t need = rlk_attn_workspace_size(params, RLK_OP_DECODE_SPLIT, nullptr, seqlens);
   if (!workspace || workspace_bytes < need)
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", workspace_bytes, need);
@@ -722,8 +730,8 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
     split_k = choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, dev->num_sms);
     // one range per sequence is the single-pass decode, which needs no state table
     if (split_k == 1)
-      return rlk_attn_decode_paged(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
-                                   out_f32, out_bf16, lse, stream);
+      return decode_paged_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
+                               rope_table, rope_max_pos, out_f32, out_bf16, lse, stream);
   }
   // state table: pair (block_base[s] + b) * Hq + head; o_b FP32 [pair][128], then lse_b [pair]
   std::vector<int32_t> block_base(params->num_seqs + 1, 0);
@@ -766,6 +774,7 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
   }
   fp->state_o = static_cast<float*>(workspace);
   fp->state_lse = static_cast<float*>(workspace) + pairs * rlk::kHeadDim;
+  fp->rope_table = rope_table;
   fp->page_table = page_table;
   fp->max_pages = max_pages;
   fp->page_size = page_size;
@@ -787,6 +796,29 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
   cudaError_t e = rlk::launch_decode_merge(*fp, dev->num_sms, stream);
   if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "split decode merge launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+
+rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                        const void* v_pool, int32_t n_pages, int32_t page_size,
+                                        const int32_t* page_table, int32_t max_pages,
+                                        const int32_t* seqlens, int32_t split_k, float* out_f32,
+                                        void* out_bf16, float* lse, void* workspace,
+                                        size_t workspace_bytes, rlk_stream_t stream) {
+  return decode_splitk_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens, split_k,
+                            nullptr, 0, out_f32, out_bf16, lse, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_attn_decode_paged_splitk_rope(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                             const void* v_pool, int32_t n_pages, int32_t page_size,
+                                             const int32_t* page_table, int32_t max_pages,
+                                             const int32_t* seqlens, int32_t split_k, const float* rope_table,
+                                             int32_t rope_max_pos, float* out_f32, void* out_bf16, float* lse,
+                                             void* workspace, size_t workspace_bytes, rlk_stream_t stream) {
+  if (!rope_table) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table is NULL");
+  return decode_splitk_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens, split_k,
+                            rope_table, rope_max_pos, out_f32, out_bf16, lse, workspace, workspace_bytes, stream);
 }
 
 size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const int32_t* cu_seqlens_q,

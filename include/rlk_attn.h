@@ -285,6 +285,25 @@ rlk_status rlk_attn_decode_paged_splitk(const rlk_attn_params* params, const voi
                                         size_t workspace_bytes, rlk_stream_t stream);
 
 /*
+ * rlk_attn_decode_paged_splitk with the query's RoPE applied inside the
+ * decode kernel, as in rlk_attn_decode_paged_rope (q pre-RoPE, rotated at
+ * position seqlens[s] - 1; the pools hold post-RoPE K): the result equals
+ * rlk_attn_decode_paged_rope bit for bit whatever split_k.
+ *   rope_table, rope_max_pos: as for rlk_attn_decode_paged_rope (NULL table:
+ *     RLK_ERR_INVALID_ARGUMENT); the other arguments as for
+ *     rlk_attn_decode_paged_splitk.
+ * [P3] PR stack: decode KV-cache replay and cache/position/RoPE identity;
+ * [P4] split-KV policy as an explicit, fixed knob.
+ */
+rlk_status rlk_attn_decode_paged_splitk_rope(const rlk_attn_params* params, const void* q, const void* k_pool,
+                                             const void* v_pool, int32_t n_pages, int32_t page_size,
+                                             const int32_t* page_table, int32_t max_pages,
+                                             const int32_t* seqlens, int32_t split_k, const float* rope_table,
+                                             int32_t rope_max_pos, float* out_f32, void* out_bf16,
+                                             float* lse, void* workspace, size_t workspace_bytes,
+                                             rlk_stream_t stream);
+
+/*
  * The split factor rlk_attn_decode_paged_splitk uses for split_k == 0 on a
  * device with num_sms SMs (host only, no device work): 1 .. 64, or -1 for
  * invalid params, a NULL seqlens, a context length < 1 or num_sms < 1.

@@ -105,6 +105,29 @@ def test_decode_rope_equals_pass_then_decode(hq, hkv):
     assert_forward_parity(*fused, ref_out, ref_lse, "decode with RoPE")
 
 
+@pytest.mark.parametrize("split_k", [0, 3])
+def test_split_decode_rope_equals_single_pass(split_k):
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    dec = synth.paged_decode_problem(ctx=[1, 129, 1000, 3000], hq=32, hkv=8, seed=47, spare_pages=2)
+    n = len(dec.seqlens)
+    single = run_decode_q(dec, dec.q, rope_max_pos=4096)
+    qd = dv.bf16_to_device(dec.q)
+    kp = torch.from_numpy(dec.k_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    vp = torch.from_numpy(dec.v_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    p = rlk.make_params(n, dec.hq, dec.hkv, 128, softmax_scale=dec.scale)
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, dec.seqlens), dtype=torch.uint8,
+                     device="cuda")
+    out, outb, lse = empty_outputs(torch, n, dec.hq)
+    rlk.rlk_attn_decode_paged_splitk_rope(p, qd, kp, vp, dec.k_bits.shape[0], dec.page_size,
+                                          dv.i32_to_device(dec.page_table), dec.page_table.shape[1], dec.seqlens,
+                                          split_k, table_dev(4096), 4096, out, outb, lse, ws)
+    rlk.rlk_attn_check_device_error()
+    assert_bitwise((out.cpu().numpy(), outb.float().cpu().numpy(), lse.cpu().numpy()), single,
+                   f"split {split_k} with RoPE")
+
+
 def test_rope_cache_position_identity():
     # prefill over RoPE'd q and k; decode of the last token (pre-RoPE query,
     # cache filled with the RoPE'd keys through a permuted page table) gives

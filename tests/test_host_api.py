@@ -249,3 +249,15 @@ def test_decode_rope_rejects_before_any_launch(lib):
         with pytest.raises(rlk.RlkError) as e:  # the in-kernel RoPE lives in the transposed decode kernel only
             call(prm)
         assert e.value.status == 2
+
+
+def test_split_decode_rope_rejects_before_any_launch(lib):
+    p = rlk.make_params(1)
+
+    def call(table=16, max_pos=4096, seqlens=(50,)):
+        rlk.rlk_attn_decode_paged_splitk_rope(p, 16, 16, 16, 4, 16, 16, 4, list(seqlens), 2, table, max_pos, 16,
+                                              None, 16, 16, 1 << 20, stream=0)
+    for kw in (dict(table=None), dict(max_pos=40)):  # no table; position 49 past 40
+        with pytest.raises(rlk.RlkError) as e:
+            call(**kw)
+        assert e.value.status == 1
