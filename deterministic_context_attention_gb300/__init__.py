@@ -98,6 +98,7 @@ def load():
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
             "rlk_attn_workspace_size": [PP, i32, P, P],
             "rlk_attn_check_device_error": [P],
+            "rlk_attn_selftest_wait_timeout": [P],
             "rlk_attn_last_error": [],
             "rlk_attn_core_id": [],
         }
@@ -246,6 +247,11 @@ def rlk_attn_decode_auto_split(params, seqlens, num_sms) -> int:
     """Split factor rlk_attn_decode_paged_splitk picks for split_k=0 (-1: invalid input)."""
     sl = _i32_host(seqlens)
     return int(load().rlk_attn_decode_auto_split(ctypes.byref(params), _ptr(sl), int(num_sms)))
+
+
+def rlk_attn_selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (reports a device timeout)."""
+    _check(load().rlk_attn_selftest_wait_timeout(_stream(stream)), "rlk_attn_selftest_wait_timeout")
 
 
 def rlk_attn_rope_table(theta, max_pos):

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "../../include/rlk_attn.h"
+#include "ptx.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
@@ -976,6 +977,35 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
   st = rlk::run_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,
                          workspace_bytes, stream);
   if (st) return st;
+  return ok();
+}
+
+namespace {
+
+// One warp waits on a barrier that nothing completes, through the same
+// bounded wait every kernel uses: after the wait's limit it reports a
+// timeout (site 0x7e1) in the error word and returns.
+__global__ void rlk_wait_selftest_kernel(rlk::ErrWord* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    rlk::mbar_init(&bar, 1);
+    abort_flag = 0;
+    rlk::fence_mbar_init();
+  }
+  __syncthreads();
+  (void)rlk::mbar_wait(&bar, 0, &abort_flag, err, 0x7e1);
+}
+
+}  // namespace
+
+rlk_status rlk_attn_selftest_wait_timeout(rlk_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  rlk_status st = device_info(&dev);
+  if (st) return st;
+  rlk_wait_selftest_kernel<<<1, 32, 0, stream>>>(dev->err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

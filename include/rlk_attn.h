@@ -369,6 +369,16 @@ size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op,
  * current device; returns RLK_OK or the status of the first fault class. */
 rlk_status rlk_attn_check_device_error(rlk_stream_t stream);
 
+/*
+ * Diagnostic of the failure-detection path: launches one warp that waits on
+ * a barrier nothing completes, through the bounded wait every kernel uses
+ * (limit 1 s); the kernel then records a device timeout (site 0x7e1) in the
+ * error word and returns, so the next rlk_attn_check_device_error on the
+ * stream reports RLK_ERR_DEVICE_TIMEOUT and clears the word.  No fault, no
+ * trap: the context stays usable.  Returns the launch status.
+ */
+rlk_status rlk_attn_selftest_wait_timeout(rlk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* rlk_attn_last_error(void);
 
