@@ -20,6 +20,10 @@
  *        order, full-KV arithmetic retained), PR stack (decode KV-cache replay,
  *        paged-KV adapter, dQ/dK/dV backward), Acceptance (Out/LSE/dQ/dK/dV
  *        max abs 0.0 across 2/4/8 ranks; fallback=false).
+ *   [P4] "[WS2][Cross-config][Attention] Integrate the Qwen3-8B TP=2 CP=2
+ *        BF16 Attention setting ..." (PR #263): the attention-contract knobs
+ *        (reduction order, split-KV policy with its supported k values, batch
+ *        size, dtype).
  *
  * Conventions (every entry point):
  *   - Tensors are packed varlen ("THD"), row-major, contiguous:
