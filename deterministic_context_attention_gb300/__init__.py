@@ -85,8 +85,8 @@ def load():
             "rlk_attn_plan_states": [PP, P, P, i32, i64, P, i64, P, P],
             "rlk_attn_block_manifest_hash": [PP, P, P, P],
             "rlk_attn_prefill_states": [PP, P, P, P, P, P, i32, i64, P, P, P],
-            "rlk_attn_merge_states": [PP, P, P, P, i64, P, P, P, P, P, P, sz, P],
-            "rlk_attn_merge_states_noalloc": [PP, P, P, P, i64, P, P, P, P, P, P],
+            "rlk_attn_merge_states": [PP, P, P, P, i64, P, P, i64, P, P, P, P, sz, P],
+            "rlk_attn_merge_states_noalloc": [PP, P, P, P, i64, P, P, i64, P, P, P, P],
             "rlk_attn_prefill": [PP, P, P, P, P, P, i32, P, P, P, P],
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
             "rlk_attn_decode_paged_splitk": [PP, P, P, P, i32, i32, P, i32, P, i32, P, P, P, P, sz, P],
@@ -191,25 +191,37 @@ def rlk_attn_prefill_states(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank
                                           _stream(stream)), "rlk_attn_prefill_states")
 
 
+def _state_pairs(state_lse, n_state_pairs):
+    """The state table's (row, head) pair count: given, or the length of the
+    state_lse tensor."""
+    if n_state_pairs is not None:
+        return int(n_state_pairs)
+    if not hasattr(state_lse, "numel"):
+        raise ValueError("n_state_pairs is required when state_lse is not a tensor")
+    return int(state_lse.numel())
+
+
 def rlk_attn_merge_states(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, state_o, state_lse, out_f32,
-                          out_bf16, lse, workspace, workspace_bytes=None, stream=None):
+                          out_bf16, lse, workspace, workspace_bytes=None, stream=None, n_state_pairs=None):
     cq, ck = _i32_host(cu_seqlens_q), _i32_host(cu_seqlens_k)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(load().rlk_attn_merge_states(ctypes.byref(params), _ptr(cq), _ptr(ck), _ptr(slabs), int(n_slabs),
-                                        _ptr(state_o), _ptr(state_lse), _ptr(out_f32), _ptr(out_bf16),
-                                        _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+                                        _ptr(state_o), _ptr(state_lse), _state_pairs(state_lse, n_state_pairs),
+                                        _ptr(out_f32), _ptr(out_bf16), _ptr(lse), _ptr(workspace),
+                                        int(workspace_bytes), _stream(stream)),
            "rlk_attn_merge_states")
 
 
 def rlk_attn_merge_states_noalloc(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, state_o, state_lse,
-                                  out_f32, out_bf16, lse, stream=None):
+                                  out_f32, out_bf16, lse, stream=None, n_state_pairs=None):
     """rlk_attn_merge_states for callers that cannot allocate: the index
     scratch is the library's own device array (see the C header for its
     limit and for the rule that overlapping calls race)."""
     cq, ck = _i32_host(cu_seqlens_q), _i32_host(cu_seqlens_k)
     _check(load().rlk_attn_merge_states_noalloc(ctypes.byref(params), _ptr(cq), _ptr(ck), _ptr(slabs),
-                                                int(n_slabs), _ptr(state_o), _ptr(state_lse), _ptr(out_f32),
+                                                int(n_slabs), _ptr(state_o), _ptr(state_lse),
+                                                _state_pairs(state_lse, n_state_pairs), _ptr(out_f32),
                                                 _ptr(out_bf16), _ptr(lse), _stream(stream)),
            "rlk_attn_merge_states_noalloc")
 

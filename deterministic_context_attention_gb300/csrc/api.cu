@@ -28,11 +28,11 @@ cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t st
 cudaError_t launch_rope(const RopeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t stream);
-cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
 rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
                         const float* out_f32, const void* dout, const float* lse,
                         const int32_t* cu, int32_t cp_rank, float* dq, float* dk, float* dv,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                        void* workspace, size_t workspace_bytes, ErrWord* err, int num_sms,
+                        cudaStream_t stream);
 size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu);
 }  // namespace rlk
 
@@ -64,10 +64,17 @@ rlk_status ok() {
   return RLK_OK;
 }
 
+// What the library keeps per device, set up once with that device current
+// (under g_dev_mutex, so concurrent first calls from several host threads are
+// safe): the SM count, the device addresses of the error word and of the
+// no-alloc merge scratch, and the kernels' function attributes (which are
+// per device).
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   rlk::ErrWord* err = nullptr;
+  int32_t* merge_scratch = nullptr;
+  int64_t merge_scratch_entries = 0;
 };
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[64];
@@ -90,6 +97,11 @@ rlk_status device_info(DeviceInfo** out) {
     e = cudaGetSymbolAddress(&addr, g_rlk_err);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
     d.err = static_cast<rlk::ErrWord*>(addr);
+    e = rlk::merge_noalloc_scratch(&d.merge_scratch, &d.merge_scratch_entries);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "cudaGetSymbolAddress(merge scratch): %s", cudaGetErrorString(e));
+    if ((e = rlk::configure_fwd_kernels()) != cudaSuccess || (e = rlk::configure_decode_kernels()) != cudaSuccess ||
+        (e = rlk::configure_merge_kernels()) != cudaSuccess || (e = rlk::configure_bwd_kernels()) != cudaSuccess)
+      return fail(RLK_ERR_CUDA, "kernel set-up on device %d: %s", dev, cudaGetErrorString(e));
     d.ready = true;
   }
   *out = &d;
@@ -261,15 +273,6 @@ void base_fwd(rlk::FwdParams* fp, const rlk_attn_params* p, const DeviceInfo* de
 
 }  // namespace
 
-namespace rlk {
-// Device address of the error word on the current device (nullptr if the
-// device is unusable).
-ErrWord* device_error_word() {
-  DeviceInfo* d = nullptr;
-  if (device_info(&d) != RLK_OK) return nullptr;
-  return d->err;
-}
-}  // namespace rlk
 
 extern "C" {
 
@@ -853,12 +856,13 @@ size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const 
 
 rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                  const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs, int64_t n_slabs,
-                                 const float* state_o, const float* state_lse, float* out_f32, void* out_bf16,
-                                 float* lse, void* workspace, size_t workspace_bytes, rlk_stream_t stream) {
+                                 const float* state_o, const float* state_lse, int64_t n_state_pairs,
+                                 float* out_f32, void* out_bf16, float* lse, void* workspace,
+                                 size_t workspace_bytes, rlk_stream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
-  if (n_slabs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
+  if (n_slabs < 0 || n_state_pairs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
     return fail(RLK_ERR_INVALID_ARGUMENT, "bad state table");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
   if ((out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) || (state_o && !aligned16(state_o)) ||
@@ -887,6 +891,7 @@ rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* c
   mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
   mp->state_o = state_o;
   mp->state_lse = state_lse;
+  mp->n_pairs = n_state_pairs;
   mp->index = static_cast<int32_t*>(workspace);
   mp->out_f32 = out_f32;
   mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
@@ -905,11 +910,12 @@ rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* c
 rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                          const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
                                          int64_t n_slabs, const float* state_o, const float* state_lse,
-                                         float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+                                         int64_t n_state_pairs, float* out_f32, void* out_bf16, float* lse,
+                                         rlk_stream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
-  if (n_slabs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
+  if (n_slabs < 0 || n_state_pairs < 0 || (n_slabs > 0 && (!slabs || !state_o || !state_lse)))
     return fail(RLK_ERR_INVALID_ARGUMENT, "bad state table");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
   if ((out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) || (state_o && !aligned16(state_o)) ||
@@ -927,10 +933,6 @@ rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const in
                 static_cast<long long>(rlk::kNoAllocIndexEntries));
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
-  int32_t* scratch = nullptr;
-  int64_t entries = 0;
-  cudaError_t e = rlk::merge_noalloc_scratch(&scratch, &entries);
-  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "scratch address: %s", cudaGetErrorString(e));
   const int64_t total_rows = cu_seqlens_q[params->num_seqs];
   if (total_rows == 0) return ok();
   auto mp = std::make_unique<rlk::MergeParams>();
@@ -945,7 +947,8 @@ rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const in
   mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
   mp->state_o = state_o;
   mp->state_lse = state_lse;
-  mp->index = scratch;
+  mp->n_pairs = n_state_pairs;
+  mp->index = dev->merge_scratch;
   mp->out_f32 = out_f32;
   mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
   mp->lse = lse;
@@ -953,7 +956,7 @@ rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const in
     mp->cu_q[s] = cu_seqlens_q[s];
     mp->cu_k[s] = cu_seqlens_k[s];
   }
-  e = rlk::launch_merge(*mp, dev->num_sms, stream);
+  const cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
   if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -974,8 +977,10 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
   const size_t need = rlk::backward_workspace_bytes(params, cu_seqlens);
   if (!workspace || workspace_bytes < need)
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev))) return st;
   st = rlk::run_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,
-                         workspace_bytes, stream);
+                         workspace_bytes, dev->err, dev->num_sms, stream);
   if (st) return st;
   return ok();
 }
@@ -1022,9 +1027,10 @@ rlk_status rlk_attn_check_device_error(rlk_stream_t stream) {
   const rlk::ErrWord zero{0, 0};
   cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
   if (w.bits & rlk::kErrDeviceTimeout) return fail(RLK_ERR_DEVICE_TIMEOUT, "device wait timed out (site 0x%x)", w.site);
+  // a slab that was not read also leaves its block missing: report the cause
+  if (w.bits & rlk::kErrBadSlab) return fail(RLK_ERR_BAD_STATE_TABLE, "state table slab out of range");
   if (w.bits & rlk::kErrDuplicateBlock) return fail(RLK_ERR_DUPLICATE_BLOCK, "duplicate global block in state table");
   if (w.bits & rlk::kErrMissingBlock) return fail(RLK_ERR_MISSING_BLOCK, "missing global block in state table");
-  if (w.bits & rlk::kErrBadSlab) return fail(RLK_ERR_BAD_STATE_TABLE, "state table slab out of range");
   if (w.bits & rlk::kErrBadPage) return fail(RLK_ERR_BAD_PAGE, "page id outside the pool");
   return fail(RLK_ERR_CUDA, "device error bits 0x%x", w.bits);
 }

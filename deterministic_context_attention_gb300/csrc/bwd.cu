@@ -34,7 +34,6 @@
 
 namespace rlk {
 
-ErrWord* device_error_word();  // api.cu
 
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -660,8 +659,7 @@ cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& tiles, int hea
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo, int num_sms,
                        cudaStream_t stream) {
   auto kern = rlk_bwd_kernel<KIND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kAlloc);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   bp->item_heads = heads;
   for (size_t i0 = 0; i0 < tiles.size(); i0 += kMaxBwdTiles) {
     const size_t n = std::min(tiles.size() - i0, static_cast<size_t>(kMaxBwdTiles));
@@ -679,6 +677,13 @@ cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& tiles, int hea
 
 static_assert(sizeof(BwdParams) + 4 * sizeof(CUtensorMap) + 256 <= 32764, "backward parameters");
 
+cudaError_t configure_bwd_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(rlk_bwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BwdLayout::kAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(rlk_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kAlloc);
+}
+
 size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu) {
   const size_t t_pad = static_cast<size_t>(cu[prm->num_seqs]) + 128;
   return (2 * t_pad * prm->num_q_heads * sizeof(float) + 255) / 256 * 256;
@@ -687,12 +692,8 @@ size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu) {
 rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
                         const float* out_f32, const void* dout, const float* lse, const int32_t* cu,
                         int32_t cp_rank, float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream) {
+                        ErrWord* err, int num_sms, cudaStream_t stream) {
   (void)workspace_bytes;
-  int dev = 0, num_sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return RLK_ERR_CUDA;
   const int T = cu[prm->num_seqs];
   if (T == 0) return RLK_OK;
   if (prm->kv_block_size != 128) return RLK_ERR_UNSUPPORTED;
@@ -724,8 +725,7 @@ rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k
 
   auto bp = std::make_unique<BwdParams>();
   std::memset(bp.get(), 0, sizeof(BwdParams));
-  bp->err = device_error_word();
-  if (!bp->err) return RLK_ERR_CUDA;
+  bp->err = err;
   bp->hq = prm->num_q_heads;
   bp->hkv = prm->num_kv_heads;
   bp->group = prm->num_q_heads / prm->num_kv_heads;

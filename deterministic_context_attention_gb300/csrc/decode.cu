@@ -11,8 +11,8 @@
 // Benchmark", Transformer Engine Reuse: state_b = (o_b, lse_b, b)) and every
 // floating-point step is the one numerics.cuh defines, in the same order:
 // the block maximum (exact), p = 2^fma(S, scale_log2, -m scale_log2), the
-// canonical row sum (key c to partial c mod 32 in ascending key order, then
-// the fixed 16-8-4-2-1 tree), P = P_hi + P_lo, PV accumulated over the hi
+// canonical row sum (per 64-key half, key c to partial c mod 32 in
+// ascending key order and the fixed 16-8-4-2-1 tree; then half 0 + half 1), P = P_hi + P_lo, PV accumulated over the hi
 // K-steps then the lo K-steps, o_b = PV / l and the canonical fold in
 // ascending global_block_index order.  The tensor core gives the same bits
 // for a product and for its transposed formulation, so a decode row equals
@@ -437,9 +437,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[L::kPFull + grp]);
-        // canonical row sums: key c goes to partial c mod 32 (this lane); the
-        // partial adds the four warps' keys of the lane in ascending order,
-        // then the 16-8-4-2-1 tree runs as a butterfly (lane 0 holds the sum)
+        // canonical row sums: per 64-key half of the block, key c goes to
+        // partial c mod 32 (this lane), the partial adding the half's two
+        // warps' keys of the lane in ascending order; the 16-8-4-2-1 tree of
+        // each half runs as a butterfly, and the block sum is half 0 + half 1
+        // (lane 0 holds it)
 #pragma unroll
         for (int q = 0; q < MG; ++q) part[((rb * 4 + w) * MG + q) * 32 + lane] = pr[q];
         mbar_arrive(&bars[L::kSyncPart + grp * 2 + rb]);
@@ -450,12 +452,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
         for (int q = 0; q < MG; ++q) {
           if (q >= G || (q & 3) != w) continue;  // warp w sums query heads w, w + 4
           const float* pq = part + (rb * 4 * MG + q) * 32 + lane;
-          float a = pq[0];
-          a = __fadd_rn(a, pq[MG * 32]);
-          a = __fadd_rn(a, pq[2 * MG * 32]);
-          a = __fadd_rn(a, pq[3 * MG * 32]);
+          float a = __fadd_rn(pq[0], pq[MG * 32]);
+          float a1 = __fadd_rn(pq[2 * MG * 32], pq[3 * MG * 32]);
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
+          for (int off = 16; off >= 1; off >>= 1) {
+            a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
+            a1 = __fadd_rn(a1, __shfl_xor_sync(0xffffffffu, a1, off));
+          }
+          a = __fadd_rn(a, a1);
           if (lane == 0) {
             float lse_b, rcp;
             block_stats(mc[q], a, lse_b, rcp);
@@ -594,13 +598,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
 template <int MG>
 cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rlk_decode_kernel<MG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DecLayout::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   rlk_decode_kernel<MG><<<grid, kDThreads, DecLayout::kAlloc, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
@@ -714,13 +711,20 @@ bool decode_transposed_supported(const FwdParams& p) {
          DecLayout::kPageWin % (DecLayout::B / p.page_size) == 0;
 }
 
+cudaError_t configure_decode_kernels() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
+    return e;
+  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
+    return e;
+  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
+    return e;
+  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
+    return e;
+  return cudaFuncSetAttribute(rlk_decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDmSmem);
+}
+
 cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rlk_decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDmSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   DecFoldParams f;
   f.state_o = p.state_o;
   f.state_lse = p.state_lse;

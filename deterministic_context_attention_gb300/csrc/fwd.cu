@@ -21,14 +21,18 @@
 // Warp roles (512 threads, four warpgroups):
 //   warps 0-3  correction / epilogue: thread r owns TMEM lane r (row r) and
 //              keeps the running O of its row in registers
-//   warps 4-7  softmax (even global blocks): thread r owns TMEM lane r; reads S, writes P_hi/P_lo
-//              over it (per 16-key MMA step: 8 columns hi, then 8 lo)
+//   warps 4-7  softmax, keys [0, B/2) of every block; warps 12-15 softmax,
+//              keys [B/2, B): thread r of either group owns TMEM lane r and
+//              reads its half of the row's S once into registers (the half's
+//              maximum comes with the load); the two warps of a TMEM lane
+//              quadrant exchange the half maxima and half sums through shared
+//              memory, then write P_hi/P_lo over their half of S (per 16-key
+//              MMA step: 8 columns hi, then 8 lo)
 //   warp  8    TMA producer (Q tile; K and V blocks or pages, separate rings)
 //   warp  9    TMEM allocator and MMA issuer (also zeroes V rows past the
 //              valid length of a partial block)
 //   warps 10-11 idle (registers are granted per warpgroup: warps 8-11 run
-//              with 48, warps 0-3 with 208)
-//   warps 12-15 second softmax group: groups alternate global blocks
+//              with 48, warps 0-3 with 208, the softmax groups with 128)
 // TMEM (512 columns): S/P double buffer [0,256), PV double buffer [256,512).
 // Per block the tensor core runs S_{b+1} then PV_b, so the softmax of block
 // b+1 overlaps PV_b and the correction of block b overlaps both.
@@ -44,7 +48,7 @@
 namespace rlk {
 
 // Four warpgroups (512 threads, 128 registers per thread at launch),
-// re-split per warpgroup: correction 208, two softmax groups 128 each,
+// re-split per warpgroup: correction 208, the two softmax groups 128 each,
 // producer / MMA 48.
 constexpr int kThreads = 512;
 constexpr int kRegsLaunch = 128;
@@ -68,11 +72,14 @@ struct FwdLayout {
   static constexpr int kBarOff = kVOff + kSV * kKVBytes;
   static constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kSK, kVFull = kKEmpty + kSK,
                        kVEmpty = kVFull + kSV, kSFull = kVEmpty + kSV, kPFull = kSFull + 2, kPVFull = kPFull + 2,
-                       kPVEmpty = kPVFull + 2, kStatsFull = kPVEmpty + 2, kNumBars = kStatsFull + kStatsRing;
+                       kPVEmpty = kPVFull + 2, kStatsFull = kPVEmpty + 2, kXch = kStatsFull + kStatsRing,
+                       kNumBars = kXch + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;
-  static constexpr int kPageWin = 1024;  // decode: page ids cached per window
-  static constexpr int kPageOff = kStatsOff + kStatsRing * kTileRows * 8;
+  // softmax exchange: the half maxima and half sums of every row, [2][128] each
+  static constexpr int kXchOff = kStatsOff + kStatsRing * kTileRows * 8;
+  static constexpr int kPageWin = 512;  // decode: page ids cached per window
+  static constexpr int kPageOff = kXchOff + 2 * 2 * kTileRows * 4;
   // epilogue staging: per correction warp 32 rows x 128 B (one column chunk)
   static constexpr int kEpiOff = kPageOff + 2 * kPageWin * 4;
   static constexpr int kEpiBytes = 4 * 32 * 128;
@@ -158,49 +165,72 @@ __device__ __forceinline__ void setmaxnreg_dec48() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
 }
 
-// Probabilities of 32 keys (chunk c of the block) for one row: writes the
-// packed hi/lo words in MMA-step order and adds the keys to the canonical
-// partial sums (which start at +0).  MASKED: keys at or past nvis are set to
-// -inf first, so their probability is exactly 0.
-template <bool MASKED>
-__device__ __forceinline__ void softmax_chunk(const uint32_t (&raw)[32], int c, int nvis, float scale_log2,
-                                              float neg_mc, float (&part)[32], uint32_t (&w)[32]) {
-  const float2 sc = make_float2(scale_log2, scale_log2);
-  const float2 nm = make_float2(neg_mc, neg_mc);
+// Softmax of one row's half block (the H = B/2 keys [h H, (h+1) H) of global
+// block b), from a single read of the half's S.  The H/32 column chunks are
+// loaded together (each load also returns its chunk's maximum) into s; with
+// masking, keys at or past hv (the visible keys of this half) are set to
+// -inf first, so their probability is exactly 0.  The half's maximum is
+// returned; after the maxima of both halves are exchanged, half_probs forms
+// the probabilities in place and their canonical half sum.
+template <int NC>
+__device__ __forceinline__ float half_load(uint32_t ta, bool full, int hv, uint32_t (&s)[NC][32]) {
+  float mx[NC];
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    float2 s = make_float2(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1]));
-    if (MASKED) {
-      const int key = 32 * c + e;
-      s.x = key < nvis ? s.x : -INFINITY;
-      s.y = key + 1 < nvis ? s.y : -INFINITY;
+  for (int c = 0; c < NC; ++c) tmem_ld32_max(ta + 32 * c, s[c], mx[c]);
+  tmem_ld_wait_only();
+#pragma unroll
+  for (int c = 0; c < NC; ++c) tmem_tie(s[c], mx[c]);
+  float m = -INFINITY;
+  if (full) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) m = fmaxf(m, mx[c]);
+  } else {
+    const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        s[c][e] = 32 * c + e < hv ? s[c][e] : ninf;
+        s[c][e + 1] = 32 * c + e + 1 < hv ? s[c][e + 1] : ninf;
+        m = fmax3(m, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+      }
     }
-    const float2 x = ffma2(s, sc, nm);
-    const float2 pr = make_float2(ex2_hw(x.x), ex2_hw(x.y));
-    const float2 acc = fadd2(make_float2(part[e], part[e + 1]), pr);
-    part[e] = acc.x;
-    part[e + 1] = acc.y;
-    uint32_t hi, lo;
-    split_pair2(pr, hi, lo);
-    const int slot = (e >> 4) * 16 + ((e & 15) >> 1);  // K-step e/16, word within it
-    w[slot] = hi;
-    w[slot + 8] = lo;
   }
+  return m;
 }
 
-// Pass 2 over the block's keys, one 32-key chunk at a time (a rolled loop
-// keeps the code small).
-template <int B, bool MASKED>
-__device__ __forceinline__ void softmax_pass2(uint32_t ta, int nvis, float scale_log2, float neg_mc,
-                                              float (&part)[32]) {
-  uint32_t cur[32], wv[32];
-#pragma unroll 1
-  for (int c = 0; c < B / 32; ++c) {
-    tmem_ld32(ta + 32 * c, cur);
-    tmem_ld_wait(cur);
-    softmax_chunk<MASKED>(cur, c, nvis, scale_log2, neg_mc, part, wv);
-    tmem_st32(ta + 32 * c, wv);
+// p = 2^fma(S, scale_log2, -mc) for the half's keys, chunk by chunk: each
+// chunk's words become (hi, lo) = split(p_2i, p_2i+1) in key-pair order and
+// are stored over its S columns in MMA-step order; returns the canonical half
+// sum: partial j (j < 32) adds the half's keys j, j + 32, ... in ascending
+// order, and the 32 partials combine by the 16-8-4-2-1 tree.
+template <int NC>
+__device__ __forceinline__ float half_probs(uint32_t ta, uint32_t (&s)[NC][32], float scale_log2, float mc) {
+  const float2 sc = make_float2(scale_log2, scale_log2);
+  const float2 nm = make_float2(-mc, -mc);
+  float part[32];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 x = ffma2(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sc, nm);
+      const float2 pr = make_float2(ex2_hw(x.x), ex2_hw(x.y));
+      if (c == 0) {
+        part[e] = pr.x;
+        part[e + 1] = pr.y;
+      } else {
+        const float2 acc = fadd2(make_float2(part[e], part[e + 1]), pr);
+        part[e] = acc.x;
+        part[e + 1] = acc.y;
+      }
+      uint32_t hi, lo;
+      split_pair2(pr, hi, lo);
+      s[c][e] = hi;
+      s[c][e + 1] = lo;
+    }
+    tmem_st32_hilo(ta + 32 * c, s[c]);
   }
+  return partial_tree(part);
 }
 
 template <int B, int MODE>
@@ -233,11 +263,12 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[L::kSFull + s], 1);
-      mbar_init(&bars[L::kPFull + s], 128);
+      mbar_init(&bars[L::kPFull + s], 256);
       mbar_init(&bars[L::kPVFull + s], 1);
       mbar_init(&bars[L::kPVEmpty + s], 128);
     }
     for (int s = 0; s < SR; ++s) mbar_init(&bars[L::kStatsFull + s], 128);
+    for (int s = 0; s < 4; ++s) mbar_init(&bars[L::kXch + s], 64);
     *abort = 0;
     fence_mbar_init();
   }
@@ -266,7 +297,7 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tm_v);
       }
       uint32_t k_it = 0, v_it = 0, q_it = 0;
-      // decode: the page ids of the current sequence, cached in two 1024-entry
+      // decode: the page ids of the current sequence, cached in two 512-entry
       // windows (V trails K by one block, so both may be live at a boundary)
       int32_t* page_cache = reinterpret_cast<int32_t*>(smem + L::kPageOff);
       int cached_win0 = -1, cached_win1 = -1;
@@ -360,6 +391,7 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t kIdescS = idesc_bf16(128, B, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, false, true);
       const Desc qd0 = make_desc(q_addr, 16, 1024);
+      const uint32_t leader = elect_one_sync();
       uint32_t k_it = 0, v_it = 0, s_it = 0, pv_it = 0, q_it = 0;
       for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
         const int item = snake_item(round);
@@ -375,18 +407,18 @@ __global__ void __launch_bounds__(512, 1)
           bool w = mbar_wait(&bars[L::kKFull + stage], (ki / SK) & 1, abort, p.err, 0x202);
           if (!__all_sync(0xffffffffu, w)) return false;
           tc_fence_after();
-          if (lane == 0) {
-            const Desc kd0 = make_desc(smem_u32(k_base + stage * L::kKVBytes), 16, 1024);
-            const uint32_t d = tm_s + ((sb + j) & 1) * 128;
-            // S = Q K^T: K-steps 0-3 in the first 64-column half, 4-7 in the second
-            mma_ss<0>(d, qd0, 0, kd0, 0, kIdescS);
+          // the whole warp walks the K-steps (warp-uniform descriptors); the
+          // elected lane issues
+          const Desc kd0 = make_desc(smem_u32(k_base + stage * L::kKVBytes), 16, 1024);
+          const uint32_t d = tm_s + ((sb + j) & 1) * 128;
+          // S = Q K^T: K-steps 0-3 in the first 64-column half, 4-7 in the second
+          if (leader) mma_ss<0>(d, qd0, 0, kd0, 0, kIdescS);
 #pragma unroll
-            for (int k = 1; k < kHeadDim / 16; ++k)
-              mma_ss<1>(d, qd0, (k >> 2) * (L::kQHalf >> 4) + (k & 3) * 2, kd0, (k >> 2) * (L::kKVHalf >> 4) + (k & 3) * 2,
-                        kIdescS);
-            umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
-            umma_commit(&bars[L::kKEmpty + stage]);
-          }
+          for (int k = 1; k < kHeadDim / 16; ++k)
+            if (leader) mma_ss<1>(d, qd0, (k >> 2) * (L::kQHalf >> 4) + (k & 3) * 2, kd0,
+                         (k >> 2) * (L::kKVHalf >> 4) + (k & 3) * 2, kIdescS);
+          if (leader) { umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
+          umma_commit(&bars[L::kKEmpty + stage]); }
           __syncwarp();
           return true;
         };
@@ -396,7 +428,7 @@ __global__ void __launch_bounds__(512, 1)
           if (j + 1 < it.nb) {
             if (!issue_s(j + 1)) { fail = true; break; }
           } else {
-            if (lane == 0) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
+            if (leader) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
             __syncwarp();
           }
           const uint32_t sidx = sb + j, buf = sidx & 1;
@@ -423,18 +455,18 @@ __global__ void __launch_bounds__(512, 1)
             __syncwarp();
           }
           tc_fence_after();
-          if (lane == 0) {
+          {
             const Desc vdd = make_desc(smem_u32(vd), L::kKVHalf, 1024);
             const uint32_t a0 = tm_s + buf * 128;
             const uint32_t d = tm_pv + pvbuf * 128;
             // PV = P_hi V + P_lo V; K-step k reads V rows 16k..16k+15 (2048 B)
-            mma_ts<0>(d, a0, vdd, 0, kIdescPV);
+            if (leader) mma_ts<0>(d, a0, vdd, 0, kIdescPV);
 #pragma unroll
-            for (int k = 1; k < B / 16; ++k) mma_ts<1>(d, a0 + 16 * k, vdd, k * 128, kIdescPV);
+            for (int k = 1; k < B / 16; ++k) if (leader) mma_ts<1>(d, a0 + 16 * k, vdd, k * 128, kIdescPV);
 #pragma unroll
-            for (int k = 0; k < B / 16; ++k) mma_ts<1>(d, a0 + 16 * k + 8, vdd, k * 128, kIdescPV);
-            umma_commit(&bars[L::kPVFull + pvbuf]);
-            umma_commit(&bars[L::kVEmpty + vstage]);
+            for (int k = 0; k < B / 16; ++k) if (leader) mma_ts<1>(d, a0 + 16 * k + 8, vdd, k * 128, kIdescPV);
+            if (leader) { umma_commit(&bars[L::kPVFull + pvbuf]);
+            umma_commit(&bars[L::kVEmpty + vstage]); }
           }
           __syncwarp();
         }
@@ -447,12 +479,17 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    // two warpgroups take alternate global blocks: group 0 (warps 4-7) the
-    // even ones, group 1 (warps 12-15) the odd ones, so each has two blocks'
-    // time for one block's softmax; row r is TMEM lane r in both
-    const int swg = warp >= 12 ? 1 : 0;
-    const int r = tid - (swg ? 384 : 128);
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // group h (warps 4-7: h = 0, warps 12-15: h = 1) takes keys
+    // [h B/2, (h+1) B/2) of every global block; row r is TMEM lane r in both
+    constexpr int HB = B / 2, NC = HB / 32;
+    const int h = warp >= 12 ? 1 : 0;
+    const int r = tid - (h ? 384 : 128);
+    const int quad = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    uint64_t* xbar = &bars[L::kXch + quad];  // the quadrant's two warps meet here
+    uint32_t x_par = 0;
+    float* xmax = reinterpret_cast<float*>(smem + L::kXchOff);  // [2][128]
+    float* xsum = xmax + 2 * kTileRows;                          // [2][128]
     uint32_t s_it = 0, st_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = snake_item(round);
@@ -466,84 +503,42 @@ __global__ void __launch_bounds__(512, 1)
       bool fail = false;
       for (int j = 0; j < it.nb; ++j) {
         const int b = it.blk0 + j;
-        const uint32_t buf = s_it & 1;  // == the group that owns this block
-        if (static_cast<int>(buf) != swg) {
-          ++s_it;
-          ++st_it;
-          continue;
-        }
+        const uint32_t buf = s_it & 1;
         bool w = mbar_wait(&bars[L::kSFull + buf], (s_it >> 1) & 1, abort, p.err, 0x301);
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         tc_fence_after();
-        const uint32_t ta = tm_s + lane_off + buf * 128;
+        const uint32_t ta = tm_s + lane_off + buf * 128 + h * HB;
         const int nvis = valid ? visible_keys(pos, it.kv_len, b, B) : 0;
         const bool has = nvis > 0;
-        // every row of the warp that is written sees all B keys: no masking
-        // on this block (a row that is not written may hold anything: MMA
-        // rows are independent and its state is never stored)
-        const bool full = __all_sync(0xffffffffu, !valid || nvis == B);
-        float lse_b = -INFINITY, rcp = 0.0f;
+        const int hv = min(max(nvis - h * HB, 0), HB);  // visible keys of this half
+        // every row of the warp that is written sees all keys of the half: no
+        // masking (a row that is not written may hold anything: MMA rows are
+        // independent and its state is never stored)
+        const bool full = __all_sync(0xffffffffu, !valid || hv == HB);
+        uint32_t sv[NC][32];
+        float lse_b = -INFINITY, rcp = 0.0f, mc = 0.0f;
+        if (warp_rows) xmax[h * kTileRows + r] = half_load<NC>(ta, full, hv, sv);
+        mbar_arrive(xbar);
+        w = mbar_wait(xbar, x_par, abort, p.err, 0x302);
+        x_par ^= 1;
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         if (warp_rows) {
-          // pass 1: maximum raw score over the visible keys (all chunks in
-          // flight, one wait)
-          float m = -INFINITY;
-          {
-            // four independent partial maxima (the maximum is exact, so the
-            // grouping does not matter); two 32-column chunks in flight at a time
-            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-            for (int h = 0; h < B / 64; ++h) {
-              uint32_t r0[32], r1[32];
-              tmem_ld32(ta + 64 * h, r0);
-              tmem_ld32(ta + 64 * h + 32, r1);
-              tmem_ld_wait(r0);
-              tmem_ld_wait(r1);
-              if (full) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  if (h == 0) {
-                    m0 = fmax3(m0, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
-                    m1 = fmax3(m1, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
-                  } else {
-                    m2 = fmax3(m2, __uint_as_float(r0[e]), __uint_as_float(r0[e + 1]));
-                    m3 = fmax3(m3, __uint_as_float(r1[e]), __uint_as_float(r1[e + 1]));
-                  }
-                }
-              } else {
-                const int k0 = 64 * h;
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  const float a0 = k0 + e < nvis ? __uint_as_float(r0[e]) : -INFINITY;
-                  const float a1 = k0 + e + 1 < nvis ? __uint_as_float(r0[e + 1]) : -INFINITY;
-                  const float b0 = k0 + 32 + e < nvis ? __uint_as_float(r1[e]) : -INFINITY;
-                  const float b1 = k0 + 33 + e < nvis ? __uint_as_float(r1[e + 1]) : -INFINITY;
-                  if (h == 0) {
-                    m0 = fmax3(m0, a0, a1);
-                    m1 = fmax3(m1, b0, b1);
-                  } else {
-                    m2 = fmax3(m2, a0, a1);
-                    m3 = fmax3(m3, b0, b1);
-                  }
-                }
-              }
-            }
-            m = fmax3(fmaxf(m0, m1), m2, m3);
-          }
-          const float mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
-          const float neg_mc = -mc;
-          // pass 2: probabilities, canonical partial sums, P = P_hi + P_lo over S
-          float part[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) part[e] = 0.0f;  // +0 + p == p: same sums as starting from key c
-          if (full) softmax_pass2<B, false>(ta, nvis, p.scale_log2, neg_mc, part);
-          else softmax_pass2<B, true>(ta, nvis, p.scale_log2, neg_mc, part);
-          if (has) block_stats(mc, partial_tree(part), lse_b, rcp);
-        }  // warp_rows
+          const float m = fmaxf(xmax[r], xmax[kTileRows + r]);  // exact
+          mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
+          xsum[h * kTileRows + r] = half_probs<NC>(ta, sv, p.scale_log2, mc);
+        }
+        mbar_arrive(xbar);
+        w = mbar_wait(xbar, x_par, abort, p.err, 0x303);
+        x_par ^= 1;
+        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+        if (h == 0 && warp_rows && has) block_stats(mc, __fadd_rn(xsum[r], xsum[kTileRows + r]), lse_b, rcp);
         tmem_st_wait();
         tc_fence_before();
-        stats[(st_it % SR) * kTileRows + r] = make_float2(lse_b, rcp);
+        if (h == 0) {
+          stats[(st_it % SR) * kTileRows + r] = make_float2(lse_b, rcp);
+          mbar_arrive(&bars[L::kStatsFull + (st_it % SR)]);
+        }
         mbar_arrive(&bars[L::kPFull + buf]);
-        mbar_arrive(&bars[L::kStatsFull + (st_it % SR)]);
         ++s_it;
         ++st_it;
       }
@@ -755,28 +750,37 @@ __global__ void __launch_bounds__(512, 1)
 
 // ---------------------------------------------------------------- launchers
 template <int B, int MODE>
-static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, int grid, cudaStream_t stream) {
+static cudaError_t configure_fwd_t() {
   using L = FwdLayout<B>;
   auto kern = rlk_fwd_kernel<B, MODE>;
-  static bool checked = false;
-  if (!checked) {
-    // The warpgroup register split (208 / 128 / 128 / 48) needs the launch to
-    // grant 128 registers per thread; with fewer, setmaxnreg.inc would wait
-    // forever.
-    cudaFuncAttributes a;
-    cudaError_t e = cudaFuncGetAttributes(&a, kern);
-    if (e != cudaSuccess) return e;
-    if (a.numRegs < kRegsLaunch) {
-      fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers at launch, the warpgroup split needs %d\n", B, MODE,
-              a.numRegs, kRegsLaunch);
-      return cudaErrorInvalidConfiguration;
-    }
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    checked = true;
+  // The warpgroup register split (208 / 128 / 128 / 48) needs the launch to
+  // grant 128 registers per thread; with fewer, setmaxnreg.inc would wait
+  // forever.
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, kern);
+  if (e != cudaSuccess) return e;
+  if (a.numRegs < kRegsLaunch) {
+    fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers at launch, the warpgroup split needs %d\n", B, MODE,
+            a.numRegs, kRegsLaunch);
+    return cudaErrorInvalidConfiguration;
   }
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(p, tq, tk, tv);
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+}
+
+cudaError_t configure_fwd_kernels() {
+  cudaError_t e;
+  if ((e = configure_fwd_t<128, kModeFused>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<128, kModeStates>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<128, kModeDecode>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<64, kModeFused>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<64, kModeStates>()) != cudaSuccess) return e;
+  return configure_fwd_t<64, kModeDecode>();
+}
+
+template <int B, int MODE>
+static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  rlk_fwd_kernel<B, MODE><<<grid, kThreads, FwdLayout<B>::kAlloc, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 

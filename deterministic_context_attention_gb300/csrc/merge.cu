@@ -23,29 +23,33 @@ __device__ __forceinline__ int first_row_of_block(int b, int B, int q_len, int k
   return max(0, b * B - (kv_len - q_len));
 }
 
-// One CTA: index[s][b] = slab id, then check every slab owns its slot.
+// A slab the merge may read: its sequence, block and row range agree with
+// the problem, and its hq * row_count state rows lie inside the table.
+__device__ __forceinline__ bool slab_ok(const MergeParams& p, const Slab& sl) {
+  if (sl.seq < 0 || sl.seq >= p.num_seqs || sl.block < 0 || sl.block >= p.max_blocks) return false;
+  const int q_len = p.cu_q[sl.seq + 1] - p.cu_q[sl.seq];
+  const int kv_len = p.cu_k[sl.seq + 1] - p.cu_k[sl.seq];
+  return sl.block * p.block < kv_len && sl.row_begin == first_row_of_block(sl.block, p.block, q_len, kv_len) &&
+         sl.row_count == q_len - sl.row_begin && sl.offset >= 0 &&
+         sl.offset <= p.n_pairs - static_cast<int64_t>(p.hq) * sl.row_count;
+}
+
+// One CTA: index[s][b] = slab id, then check every valid slab owns its slot
+// (a slab that fails slab_ok is reported and never indexed, so its block
+// counts as missing unless another slab supplies it).
 __global__ void __launch_bounds__(1024) rlk_merge_index_kernel(const __grid_constant__ MergeParams p) {
   const int n_idx = p.num_seqs * p.max_blocks;
   for (int i = threadIdx.x; i < n_idx; i += blockDim.x) p.index[i] = -1;
   __syncthreads();
   for (int64_t sid = threadIdx.x; sid < p.n_slabs; sid += blockDim.x) {
     const Slab sl = p.slabs[sid];
-    bool ok = sl.seq >= 0 && sl.seq < p.num_seqs && sl.block >= 0 && sl.block < p.max_blocks;
-    if (ok) {
-      const int q_len = p.cu_q[sl.seq + 1] - p.cu_q[sl.seq];
-      const int kv_len = p.cu_k[sl.seq + 1] - p.cu_k[sl.seq];
-      ok = sl.block * p.block < kv_len &&
-           sl.row_begin == first_row_of_block(sl.block, p.block, q_len, kv_len) &&
-           sl.row_count == q_len - sl.row_begin && sl.offset >= 0;
-    }
-    if (ok) p.index[sl.seq * p.max_blocks + sl.block] = static_cast<int32_t>(sid);
+    if (slab_ok(p, sl)) p.index[sl.seq * p.max_blocks + sl.block] = static_cast<int32_t>(sid);
     else report_error(p.err, kErrBadSlab, 0x501);
   }
   __syncthreads();
   for (int64_t sid = threadIdx.x; sid < p.n_slabs; sid += blockDim.x) {
     const Slab sl = p.slabs[sid];
-    if (sl.seq >= 0 && sl.seq < p.num_seqs && sl.block >= 0 && sl.block < p.max_blocks &&
-        p.index[sl.seq * p.max_blocks + sl.block] != static_cast<int32_t>(sid))
+    if (slab_ok(p, sl) && p.index[sl.seq * p.max_blocks + sl.block] != static_cast<int32_t>(sid))
       report_error(p.err, kErrDuplicateBlock, 0x502);
   }
 }
@@ -196,16 +200,14 @@ __global__ void __launch_bounds__(kMergeThreads, 2) rlk_merge_fold_kernel(const 
   }
 }
 
+cudaError_t configure_merge_kernels() {
+  return cudaFuncSetAttribute(rlk_merge_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+}
+
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream) {
   rlk_merge_index_kernel<<<1, 1024, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(rlk_merge_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   const int64_t warps = p.total_rows * ((p.hq + kMergeHeadsPerWarp - 1) / kMergeHeadsPerWarp);
   int64_t blocks = (warps + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms) * 2;  // 2 CTAs of 256 threads per SM
@@ -226,22 +228,15 @@ namespace rlk {
 
 static __device__ __align__(256) int32_t g_merge_index_scratch[kNoAllocIndexEntries];
 
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.  (In host code the array's name is
-// only a host-side stand-in; the kernels must receive this address.)
+// Device address of the scratch array on the current device.  (In host code
+// the array's name is only a host-side stand-in; the kernels must receive
+// this address.)  The library looks it up once per device, with that device
+// current, in its per-device set-up.
 cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries) {
-  static int32_t* addr[64] = {nullptr};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* a = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&a, g_merge_index_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
-    void* a = nullptr;
-    e = cudaGetSymbolAddress(&a, g_merge_index_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<int32_t*>(a);
-  }
-  *ptr = addr[dev];
+  *ptr = static_cast<int32_t*>(a);
   *entries = kNoAllocIndexEntries;
   return cudaSuccess;
 }

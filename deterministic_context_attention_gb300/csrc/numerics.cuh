@@ -46,17 +46,15 @@ __device__ __forceinline__ float bf16_hi_as_f32(uint32_t w) { return __uint_as_f
 // (scale_log2 > 0, so the maximum of the raw scores scaled once is also the
 // maximum of the scaled scores.)
 //
-// Canonical row sum: key c goes to partial c mod 32, the keys of a partial
-// added in ascending order; the 32 partials are then combined by the fixed
-// tree a[t] <- a[t] + a[t + off] for off = 16, 8, 4, 2, 1 -- the association a
-// 32-lane xor butterfly produces, so a warp-per-row kernel reproduces it.
+// Canonical row sum: the block's keys are split into two halves of B/2; in
+// each half, key c goes to partial c mod 32 (the keys of a partial added in
+// ascending order) and the 32 partials are combined by the fixed tree
+// a[t] <- a[t] + a[t + off] for off = 16, 8, 4, 2, 1 -- the association a
+// 32-lane xor butterfly produces, so a warp-per-row kernel reproduces it; the
+// block sum is half 0 + half 1.  (The halves let two warps share a row, each
+// reading its half of S once.)
 __device__ __forceinline__ float prob(float s, float scale_log2, float neg_mc) {
   return ex2_hw(__fmaf_rn(s, scale_log2, neg_mc));
-}
-// add probability p of key c (keys visited in ascending order) to partials a
-__device__ __forceinline__ void partial_add(float (&a)[32], int c, float p) {
-  if (c < 32) a[c & 31] = p;
-  else a[c & 31] = __fadd_rn(a[c & 31], p);
 }
 __device__ __forceinline__ float partial_tree(float (&a)[32]) {
 #pragma unroll
@@ -123,12 +121,20 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // Split a pair of probabilities into packed BF16 hi and lo words (the same
-// values as split_pair, with packed subtraction).
+// values as split_pair).  The residual p - hi is exact in FP32 and is formed
+// by one mixed-precision fma per element (hi * -1 + p, hi read as BF16
+// straight from its half of the packed word), so lo = bf16_rn(p - hi) without
+// widening hi first; an exact zero residual is +0, as __fsub_rn gives.
 __device__ __forceinline__ void split_pair2(float2 p, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(p.x, p.y);
-  const float2 h = make_float2(bf16_lo_as_f32(hi), bf16_hi_as_f32(hi));
-  const float2 r = fsub2(p, h);
-  lo = pack_bf16x2(r.x, r.y);
+  asm("{\n\t.reg .b16 h0, h1, m1;\n\t.reg .f32 r0, r1;\n\t"
+      "cvt.rn.bf16x2.f32 %0, %3, %2;\n\t"
+      "mov.b32 {h0, h1}, %0;\n\t"
+      "mov.b16 m1, 0xBF80;\n\t"  // BF16 -1.0
+      "fma.rn.f32.bf16 r0, h0, m1, %2;\n\t"
+      "fma.rn.f32.bf16 r1, h1, m1, %3;\n\t"
+      "cvt.rn.bf16x2.f32 %1, r1, r0;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "f"(p.x), "f"(p.y));
 }
 
 // Block output element: o = PV * (1/l).

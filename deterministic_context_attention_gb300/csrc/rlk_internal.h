@@ -1,6 +1,8 @@
 // rlk_internal.h -- launch parameter blocks and limits shared by the host
 // side of the C ABI and the kernels.  Not part of the public interface.
 #pragma once
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 namespace rlk {
@@ -87,6 +89,7 @@ struct MergeParams {
   const Slab* slabs;       // device, arrival order
   const float* state_o;
   const float* state_lse;
+  int64_t n_pairs;         // (row, head) pairs the state table holds
   int32_t* index;          // [num_seqs * max_blocks] slab id per (seq, block)
   float* out_f32;
   uint16_t* out_bf16;
@@ -106,5 +109,17 @@ struct RopeParams {
   int32_t cu[kMaxSeqs + 1];
   int32_t pos0[kMaxSeqs];
 };
+
+// Per-device set-up, run once per device (with it current) before the first
+// launch there: the kernels' dynamic shared memory limits and launch checks.
+// Function attributes are per device, so every device a process uses needs
+// its own call.
+cudaError_t configure_fwd_kernels();
+cudaError_t configure_decode_kernels();
+cudaError_t configure_merge_kernels();
+cudaError_t configure_bwd_kernels();
+// Device address of the no-alloc merge's file-scope scratch on the current
+// device, and its size in int32 entries.
+cudaError_t merge_noalloc_scratch(int32_t** ptr, int64_t* entries);
 
 }  // namespace rlk

@@ -154,18 +154,24 @@ rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q,
  * [Tq,Hq,128], nullable), out_bf16 (device BF16, nullable; not both NULL)
  * and lse (device FP32 [Tq,Hq]).  slabs: DEVICE array of n_slabs entries
  * (e.g. several ranks' plans concatenated in any order), offsets into
- * state_o / state_lse.  workspace: device, >= rlk_attn_workspace_size(...,
+ * state_o / state_lse.  n_state_pairs: the number of (row, head) pairs the
+ * table holds (state_o: device FP32 [n_state_pairs, 128], state_lse: device
+ * FP32 [n_state_pairs]).  workspace: device, >= rlk_attn_workspace_size(...,
  * RLK_OP_MERGE, ...) bytes.  Every block of every row must be present exactly
  * once: a duplicate sets RLK_ERR_DUPLICATE_BLOCK, a missing one
- * RLK_ERR_MISSING_BLOCK (and NaN rows) on the device error word.
+ * RLK_ERR_MISSING_BLOCK (and NaN rows) on the device error word.  A slab
+ * whose rows do not fit the table (offset + Hq * row_count > n_state_pairs),
+ * or whose sequence, block or row range disagrees with cu_seqlens, is not
+ * read: it sets RLK_ERR_BAD_STATE_TABLE, and its block then counts as
+ * missing.
  * [P1] Transformer Engine Reuse; the drift-class table (merge_order_probe:
  * reversed arrival equals the sorted merge).
  */
 rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                  const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
                                  int64_t n_slabs, const float* state_o, const float* state_lse,
-                                 float* out_f32, void* out_bf16, float* lse, void* workspace,
-                                 size_t workspace_bytes, rlk_stream_t stream);
+                                 int64_t n_state_pairs, float* out_f32, void* out_bf16, float* lse,
+                                 void* workspace, size_t workspace_bytes, rlk_stream_t stream);
 
 /*
  * Fused causal prefill (full or chunked replay): for each query row, the
@@ -350,8 +356,9 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
  *   holds until the process exits.  num_seqs times the largest number of KV
  *   blocks of a sequence must not exceed 65,536; larger problems return
  *   RLK_ERR_UNSUPPORTED with a message.  Nothing is allocated or freed.
- *   The first call on a device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   The first call of any entry point on a device sets the library up
+ *   there (with that device current), which includes looking up the array's
+ *   device address; make that first call before any stream capture.
  *   Every call reuses the same array and initialises it itself, so calls in
  *   sequence are independent, but calls that overlap on the GPU (different
  *   streams, or different host threads on one device) race on it.
@@ -359,7 +366,8 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
 rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                          const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
                                          int64_t n_slabs, const float* state_o, const float* state_lse,
-                                         float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream);
+                                         int64_t n_state_pairs, float* out_f32, void* out_bf16, float* lse,
+                                         rlk_stream_t stream);
 
 enum { RLK_OP_MERGE = 1, RLK_OP_BACKWARD = 2, RLK_OP_DECODE_SPLIT = 3 };
 

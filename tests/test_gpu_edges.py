@@ -97,3 +97,39 @@ def test_decode_one_long_context():
         assert abs(float(single[2][0, h]) - l32) <= 4e-6, f"head {h}: GPU lse vs canonical FP32 fold"
         worst_fold = max(worst_fold, abs(l32 - float(ref_lse[0, h])))
     assert float(np.abs(single[2] - ref_lse).max()) <= worst_fold + 4e-6
+
+
+def test_merge_rejects_slab_past_the_state_table():
+    # a slab whose offset is valid in itself but whose rows reach past the
+    # table (offset + Hq * row_count > n_state_pairs) must not be read: the
+    # merge reports a bad state table, leaves that block missing, and the
+    # context stays usable for the next call
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    from tests.gpu_helpers import device_inputs, params_of, to_np
+    prob = synth.prefill_problem(lens=[300, 129], hq=32, hkv=8, block=128, seed=57)
+    q, k, v = device_inputs(prob)
+    p = params_of(prob)
+    slabs, npairs = rlk.rlk_attn_plan_states(p, prob.cu_q, prob.cu_k, -1, 0)
+    so = torch.empty((npairs, 128), dtype=torch.float32, device="cuda")
+    sl = torch.empty((npairs,), dtype=torch.float32, device="cuda")
+    rlk.rlk_attn_prefill_states(p, q, k, v, prob.cu_q, prob.cu_k, -1, 0, so, sl)
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, prob.cu_q, prob.cu_k), dtype=torch.uint8,
+                     device="cuda")
+    bad = slabs.copy()
+    last = int(np.argmax(bad["offset"]))
+    bad["offset"][last] = npairs - prob.hq * int(bad["row_count"][last]) + 1  # one pair past the end
+    out, outb, lse = empty_outputs(torch, q.shape[0], prob.hq)
+    rlk.rlk_attn_merge_states(p, prob.cu_q, prob.cu_k, dv.slabs_to_device(bad), len(bad), so, sl, out, outb, lse, ws)
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_check_device_error()
+    assert e.value.status == 9  # RLK_ERR_BAD_STATE_TABLE
+    # the rows needing that block are NaN (missing), the others are merged
+    got = to_np(out, outb, lse)
+    assert np.isnan(got[2]).any() and not np.isnan(got[2]).all()
+    # the same table with the right offset merges cleanly afterwards
+    good = empty_outputs(torch, q.shape[0], prob.hq)
+    rlk.rlk_attn_merge_states(p, prob.cu_q, prob.cu_k, dv.slabs_to_device(slabs), len(slabs), so, sl, *good, ws)
+    rlk.rlk_attn_check_device_error()
+    assert_bitwise(to_np(*good), run_fused(prob), "merge after a rejected table")

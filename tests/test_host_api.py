@@ -137,7 +137,7 @@ def test_workspace_sizes(lib):
     assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_BACKWARD, cu) >= int(cu[-1]) * 32 * 4
     assert rlk.rlk_attn_workspace_size(p, 99, cu, cu) == 0
     with pytest.raises(rlk.RlkError) as e:
-        rlk.rlk_attn_merge_states(p, cu, cu, 16, 1, 16, 16, 16, None, 16, 16, 8, stream=0)
+        rlk.rlk_attn_merge_states(p, cu, cu, 16, 1, 16, 16, 16, None, 16, 16, 8, stream=0, n_state_pairs=1)
     assert e.value.status == 3
 
 
@@ -148,7 +148,7 @@ def test_noalloc_merge_rejects_oversized_problem_before_any_device_work(lib):
     cu = synth.cu_seqlens([262144] * 128)
     p = rlk.make_params(128)
     with pytest.raises(rlk.RlkError) as e:
-        rlk.rlk_attn_merge_states_noalloc(p, cu, cu, 16, 1, 16, 16, 16, None, 16, stream=0)
+        rlk.rlk_attn_merge_states_noalloc(p, cu, cu, 16, 1, 16, 16, 16, None, 16, stream=0, n_state_pairs=1)
     assert e.value.status == 2
     assert "scratch" in rlk.rlk_attn_last_error()
 

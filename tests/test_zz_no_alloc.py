@@ -60,3 +60,47 @@ def test_noalloc_merge_matches_workspace_merge_twice():
             assert np.array_equal(got[0].view(np.uint32), ref[0].view(np.uint32))
             assert np.array_equal(got[1].view(np.uint32), ref[1].view(np.uint32))
             assert np.array_equal(got[2].view(np.uint32), ref[2].view(np.uint32))
+
+
+def test_noalloc_merge_at_the_scratch_limit():
+    # num_seqs * max blocks == the 65,536-entry scratch exactly: 16 one-token
+    # queries over 262,144 keys each, KV block 64 (4,096 blocks per
+    # sequence), Hq = Hkv = 1.  The states are filled on the host (the merge
+    # only reads the table), the slabs arrive permuted, and the no-alloc
+    # merge must give the workspace merge's bits on two calls in a row.
+    from tests.gpu_helpers import empty_outputs, lib, to_np, torch_cuda
+    import deterministic_context_attention_gb300 as rlk_mod
+    from deterministic_context_attention_gb300 import device as dv
+    torch = torch_cuda()
+    rlk = lib()
+    n_seq, kv_len, block = 16, 262144, 64
+    nb = kv_len // block
+    assert n_seq * nb == 65536
+    cu_q = np.arange(n_seq + 1, dtype=np.int32)
+    cu_k = (np.arange(n_seq + 1, dtype=np.int64) * kv_len).astype(np.int32)
+    p = rlk.make_params(n_seq, 1, 1, block)
+    n_pairs = n_seq * nb
+    rng = np.random.default_rng(61)
+    so = torch.from_numpy(rng.standard_normal((n_pairs, 128), dtype=np.float32)).cuda()
+    sl = torch.from_numpy((3.0 * rng.standard_normal(n_pairs)).astype(np.float32)).cuda()
+    slabs = np.zeros(n_pairs, dtype=rlk_mod.SLAB_DTYPE)
+    slabs["seq"] = np.repeat(np.arange(n_seq), nb)
+    slabs["block"] = np.tile(np.arange(nb), n_seq)
+    slabs["row_begin"] = 0
+    slabs["row_count"] = 1
+    slabs["offset"] = np.arange(n_pairs)
+    slabs = slabs[rng.permutation(n_pairs)]
+    dslabs = dv.slabs_to_device(slabs)
+    ws = torch.empty(rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, cu_q, cu_k), dtype=torch.uint8, device="cuda")
+    ref = empty_outputs(torch, n_seq, 1)
+    rlk.rlk_attn_merge_states(p, cu_q, cu_k, dslabs, n_pairs, so, sl, *ref, ws)
+    rlk.rlk_attn_check_device_error()
+    ref = to_np(*ref)
+    assert np.isfinite(ref[0]).all() and np.isfinite(ref[2]).all()
+    for _ in range(2):
+        got = empty_outputs(torch, n_seq, 1)
+        rlk.rlk_attn_merge_states_noalloc(p, cu_q, cu_k, dslabs, n_pairs, so, sl, *got)
+        rlk.rlk_attn_check_device_error()
+        got = to_np(*got)
+        for a, b in zip(got, ref):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
