@@ -11,8 +11,8 @@
 // Benchmark", Transformer Engine Reuse: state_b = (o_b, lse_b, b)) and every
 // floating-point step is the one numerics.cuh defines, in the same order:
 // the block maximum (exact), p = 2^fma(S, scale_log2, -m scale_log2), the
-// canonical row sum (per 64-key half, key c to partial c mod 32 in
-// ascending key order and the fixed 16-8-4-2-1 tree; then half 0 + half 1), P = P_hi + P_lo, PV accumulated over the hi
+// canonical row sum (per 64-key half, key c to partial c mod 16 in
+// ascending key order and the fixed 8-4-2-1 tree; then half 0 + half 1), P = P_hi + P_lo, PV accumulated over the hi
 // K-steps then the lo K-steps, o_b = PV / l and the canonical fold in
 // ascending global_block_index order.  The tensor core gives the same bits
 // for a product and for its transposed formulation, so a decode row equals
@@ -437,11 +437,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[L::kPFull + grp]);
-        // canonical row sums: per 64-key half of the block, key c goes to
-        // partial c mod 32 (this lane), the partial adding the half's two
-        // warps' keys of the lane in ascending order; the 16-8-4-2-1 tree of
-        // each half runs as a butterfly, and the block sum is half 0 + half 1
-        // (lane 0 holds it)
+        // canonical row sums: per 64-key half of the block (warps 2h and
+        // 2h + 1), key c goes to partial c mod 16, the partial adding keys j,
+        // j + 16 (first warp's lanes j, j + 16), j + 32, j + 48 (second
+        // warp's) in ascending order; the 8-4-2-1 tree of each half runs as a
+        // butterfly over 16 lanes, and the block sum is half 0 + half 1 (lane
+        // 0 holds it)
 #pragma unroll
         for (int q = 0; q < MG; ++q) part[((rb * 4 + w) * MG + q) * 32 + lane] = pr[q];
         mbar_arrive(&bars[L::kSyncPart + grp * 2 + rb]);
@@ -452,10 +453,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         for (int q = 0; q < MG; ++q) {
           if (q >= G || (q & 3) != w) continue;  // warp w sums query heads w, w + 4
           const float* pq = part + (rb * 4 * MG + q) * 32 + lane;
-          float a = __fadd_rn(pq[0], pq[MG * 32]);
-          float a1 = __fadd_rn(pq[2 * MG * 32], pq[3 * MG * 32]);
+          const float* pw = pq - lane + (lane & 15);  // key (lane mod 16) of each warp's 32
+          float a = __fadd_rn(__fadd_rn(__fadd_rn(pw[0], pw[16]), pw[MG * 32]), pw[MG * 32 + 16]);
+          float a1 = __fadd_rn(__fadd_rn(__fadd_rn(pw[2 * MG * 32], pw[2 * MG * 32 + 16]), pw[3 * MG * 32]),
+                               pw[3 * MG * 32 + 16]);
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
+          for (int off = 8; off >= 1; off >>= 1) {
             a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, off));
             a1 = __fadd_rn(a1, __shfl_xor_sync(0xffffffffu, a1, off));
           }

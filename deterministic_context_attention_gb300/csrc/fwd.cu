@@ -199,36 +199,38 @@ __device__ __forceinline__ float half_load(uint32_t ta, bool full, int hv, uint3
   return m;
 }
 
-// p = 2^fma(S, scale_log2, -mc) for the half's keys, chunk by chunk: each
-// chunk's words become (hi, lo) = split(p_2i, p_2i+1) in key-pair order and
-// are stored over its S columns in MMA-step order; returns the canonical half
-// sum: partial j (j < 32) adds the half's keys j, j + 32, ... in ascending
-// order, and the 32 partials combine by the 16-8-4-2-1 tree.
+// p = 2^fma(S, scale_log2, -mc) for the half's keys, chunk by chunk: the
+// words become (hi, lo) = split(p_2i, p_2i+1) in key-pair order and each
+// 16-key MMA step is stored over its S columns; returns the canonical half
+// sum: partial j (j < 16) adds the half's keys j, j + 16, j + 32, ... in
+// ascending order, and the 16 partials combine by the 8-4-2-1 tree.
 template <int NC>
 __device__ __forceinline__ float half_probs(uint32_t ta, uint32_t (&s)[NC][32], float scale_log2, float mc) {
   const float2 sc = make_float2(scale_log2, scale_log2);
   const float2 nm = make_float2(-mc, -mc);
-  float part[32];
+  float part[16];
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
       const float2 x = ffma2(make_float2(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sc, nm);
       const float2 pr = make_float2(ex2_hw(x.x), ex2_hw(x.y));
-      if (c == 0) {
-        part[e] = pr.x;
-        part[e + 1] = pr.y;
+      const int j = e & 15;
+      if (c == 0 && e < 16) {
+        part[j] = pr.x;
+        part[j + 1] = pr.y;
       } else {
-        const float2 acc = fadd2(make_float2(part[e], part[e + 1]), pr);
-        part[e] = acc.x;
-        part[e + 1] = acc.y;
+        const float2 acc = fadd2(make_float2(part[j], part[j + 1]), pr);
+        part[j] = acc.x;
+        part[j + 1] = acc.y;
       }
       uint32_t hi, lo;
       split_pair2(pr, hi, lo);
       s[c][e] = hi;
       s[c][e + 1] = lo;
+      // each 16-key MMA step's words go out as soon as they exist
+      if ((e & 15) == 14) tmem_st16_hilo(ta + 32 * c + (e & 16), &s[c][e & 16]);
     }
-    tmem_st32_hilo(ta + 32 * c, s[c]);
   }
   return partial_tree(part);
 }
@@ -415,10 +417,13 @@ __global__ void __launch_bounds__(512, 1)
           if (leader) mma_ss<0>(d, qd0, 0, kd0, 0, kIdescS);
 #pragma unroll
           for (int k = 1; k < kHeadDim / 16; ++k)
-            if (leader) mma_ss<1>(d, qd0, (k >> 2) * (L::kQHalf >> 4) + (k & 3) * 2, kd0,
-                         (k >> 2) * (L::kKVHalf >> 4) + (k & 3) * 2, kIdescS);
-          if (leader) { umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
-          umma_commit(&bars[L::kKEmpty + stage]); }
+            if (leader)
+              mma_ss<1>(d, qd0, (k >> 2) * (L::kQHalf >> 4) + (k & 3) * 2, kd0, (k >> 2) * (L::kKVHalf >> 4) + (k & 3) * 2,
+                        kIdescS);
+          if (leader) {
+            umma_commit(&bars[L::kSFull + ((sb + j) & 1)]);
+            umma_commit(&bars[L::kKEmpty + stage]);
+          }
           __syncwarp();
           return true;
         };
@@ -462,11 +467,15 @@ __global__ void __launch_bounds__(512, 1)
             // PV = P_hi V + P_lo V; K-step k reads V rows 16k..16k+15 (2048 B)
             if (leader) mma_ts<0>(d, a0, vdd, 0, kIdescPV);
 #pragma unroll
-            for (int k = 1; k < B / 16; ++k) if (leader) mma_ts<1>(d, a0 + 16 * k, vdd, k * 128, kIdescPV);
+            for (int k = 1; k < B / 16; ++k)
+              if (leader) mma_ts<1>(d, a0 + 16 * k, vdd, k * 128, kIdescPV);
 #pragma unroll
-            for (int k = 0; k < B / 16; ++k) if (leader) mma_ts<1>(d, a0 + 16 * k + 8, vdd, k * 128, kIdescPV);
-            if (leader) { umma_commit(&bars[L::kPVFull + pvbuf]);
-            umma_commit(&bars[L::kVEmpty + vstage]); }
+            for (int k = 0; k < B / 16; ++k)
+              if (leader) mma_ts<1>(d, a0 + 16 * k + 8, vdd, k * 128, kIdescPV);
+            if (leader) {
+              umma_commit(&bars[L::kPVFull + pvbuf]);
+              umma_commit(&bars[L::kVEmpty + vstage]);
+            }
           }
           __syncwarp();
         }

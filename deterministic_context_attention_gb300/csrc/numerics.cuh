@@ -47,18 +47,19 @@ __device__ __forceinline__ float bf16_hi_as_f32(uint32_t w) { return __uint_as_f
 // maximum of the scaled scores.)
 //
 // Canonical row sum: the block's keys are split into two halves of B/2; in
-// each half, key c goes to partial c mod 32 (the keys of a partial added in
-// ascending order) and the 32 partials are combined by the fixed tree
-// a[t] <- a[t] + a[t + off] for off = 16, 8, 4, 2, 1 -- the association a
-// 32-lane xor butterfly produces, so a warp-per-row kernel reproduces it; the
-// block sum is half 0 + half 1.  (The halves let two warps share a row, each
-// reading its half of S once.)
+// each half, key c goes to partial c mod 16 (the keys of a partial added in
+// ascending order) and the 16 partials are combined by the fixed tree
+// a[t] <- a[t] + a[t + off] for off = 8, 4, 2, 1 -- the association an xor
+// butterfly over 16 lanes produces, so a kernel with keys on lanes
+// reproduces it; the block sum is half 0 + half 1.  (The halves let two
+// warps share a row, each reading its half of S once; 16 partials keep a
+// half row's softmax within 128 registers.)
 __device__ __forceinline__ float prob(float s, float scale_log2, float neg_mc) {
   return ex2_hw(__fmaf_rn(s, scale_log2, neg_mc));
 }
-__device__ __forceinline__ float partial_tree(float (&a)[32]) {
+__device__ __forceinline__ float partial_tree(float (&a)[16]) {
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
+  for (int off = 8; off >= 1; off >>= 1) {
 #pragma unroll
     for (int t = 0; t < off; ++t) a[t] = __fadd_rn(a[t], a[t + off]);
   }
