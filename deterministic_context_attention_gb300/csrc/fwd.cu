@@ -536,18 +536,21 @@ __global__ void __launch_bounds__(512, 1)
           mc = has ? __fmul_rn(m, p.scale_log2) : 0.0f;
           xsum[h * kTileRows + r] = half_probs<NC>(ta, sv, p.scale_log2, mc);
         }
+        // P is in TMEM: the PV product may start while the half sums are
+        // exchanged and the block statistics formed (only the correction
+        // warps read those)
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[L::kPFull + buf]);
         mbar_arrive(xbar);
         w = mbar_wait(xbar, x_par, abort, p.err, 0x303);
         x_par ^= 1;
         if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
         if (h == 0 && warp_rows && has) block_stats(mc, __fadd_rn(xsum[r], xsum[kTileRows + r]), lse_b, rcp);
-        tmem_st_wait();
-        tc_fence_before();
         if (h == 0) {
           stats[(st_it % SR) * kTileRows + r] = make_float2(lse_b, rcp);
           mbar_arrive(&bars[L::kStatsFull + (st_it % SR)]);
         }
-        mbar_arrive(&bars[L::kPFull + buf]);
         ++s_it;
         ++st_it;
       }
