@@ -13,6 +13,7 @@
 #include <memory>
 #include <mutex>
 #include <string>
+#include <type_traits>
 #include <vector>
 
 #include "../../include/rlk_attn.h"
@@ -48,6 +49,11 @@ static __device__ rlk::ErrWord g_rlk_err;
 namespace {
 
 thread_local std::string g_last_error;
+
+// Set while an entry point validates the sequence ranges of a batch larger
+// than one launch's tables (over_ranges): each range's call then checks its
+// arguments on the host and returns before it touches the device.
+thread_local bool g_dry_run = false;
 
 rlk_status fail(rlk_status st, const char* fmt, ...) {
   char buf[512];
@@ -155,8 +161,8 @@ rlk_status check_params(const rlk_attn_params* p) {
     return fail(RLK_ERR_UNSUPPORTED, "kv_block_size %d: must be 64 or 128", p->kv_block_size);
   if (p->cp_size < 1 || p->cp_size > 8) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_size %d not in 1..8", p->cp_size);
   if (p->cp_layout != 0 && p->cp_layout != 1) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_layout %d", p->cp_layout);
-  if (p->num_seqs < 1 || p->num_seqs > rlk::kMaxSeqs)
-    return fail(RLK_ERR_UNSUPPORTED, "num_seqs %d not in 1..%d", p->num_seqs, rlk::kMaxSeqs);
+  if (p->num_seqs < 1 || p->num_seqs > rlk::kMaxSeqsPerCall)
+    return fail(RLK_ERR_UNSUPPORTED, "num_seqs %d not in 1..%d", p->num_seqs, rlk::kMaxSeqsPerCall);
   if (!(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale))
     return fail(RLK_ERR_INVALID_ARGUMENT, "softmax_scale must be finite and > 0");
   return RLK_OK;
@@ -173,6 +179,48 @@ rlk_status check_cu(const rlk_attn_params* p, const int32_t* cu_q, const int32_t
                              static_cast<long long>(ql), static_cast<long long>(kl));
   }
   return RLK_OK;
+}
+
+// Batches of more sequences than one launch's tables hold (kMaxSeqs) run as
+// consecutive ranges of at most kMaxSeqs sequences, each a complete call on
+// rebased cu_seqlens and offset tensor pointers (per-sequence arithmetic does
+// not depend on the other sequences of a batch, so the results are the
+// same).  Every range is validated first (a dry run that stops before any
+// device work), then the ranges launch in order on the caller's stream, so a
+// bad argument anywhere still fails the call before its first launch.
+template <class Fn>
+rlk_status over_ranges(int num_seqs, Fn&& range_call) {
+  g_dry_run = true;
+  for (int s0 = 0; s0 < num_seqs; s0 += rlk::kMaxSeqs) {
+    const rlk_status st = range_call(s0, std::min(num_seqs, s0 + rlk::kMaxSeqs));
+    if (st) {
+      g_dry_run = false;
+      return st;
+    }
+  }
+  g_dry_run = false;
+  for (int s0 = 0; s0 < num_seqs; s0 += rlk::kMaxSeqs) {
+    const rlk_status st = range_call(s0, std::min(num_seqs, s0 + rlk::kMaxSeqs));
+    if (st) return st;
+  }
+  return ok();
+}
+// cu[s0..s1] - cu[s0]: the cumulative lengths of a sequence range
+std::vector<int32_t> rebase(const int32_t* cu, int s0, int s1) {
+  std::vector<int32_t> r(s1 - s0 + 1);
+  for (int s = s0; s <= s1; ++s) r[s - s0] = cu[s] - cu[s0];
+  return r;
+}
+// p advanced by n elements of `bytes` bytes (NULL stays NULL)
+template <class T>
+T* adv(T* p, int64_t n, int bytes) {
+  using C = typename std::conditional<std::is_const<T>::value, const char, char>::type;
+  return p ? reinterpret_cast<T*>(reinterpret_cast<C*>(p) + n * bytes) : nullptr;
+}
+rlk_attn_params range_params(const rlk_attn_params* p, int s0, int s1) {
+  rlk_attn_params r = *p;
+  r.num_seqs = s1 - s0;
+  return r;
 }
 
 float scale_log2(const rlk_attn_params* p) {
@@ -341,8 +389,25 @@ rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q,
   if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
   if (pair_base < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "pair_base < 0");
   if (!q || !k || !v || !state_o || !state_lse) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
+  if (params->num_seqs > rlk::kMaxSeqs) {
+    // the plan is sequence-major, so a range's slabs start where the plan of
+    // the sequences before it ends
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      SlabPlan before;
+      const rlk_attn_params head = range_params(params, 0, s0);
+      if (s0 > 0) plan_slabs(&head, cu_seqlens_q, cu_seqlens_k, cp_rank, pair_base, &before);
+      const auto cq = rebase(cu_seqlens_q, s0, s1), ck = rebase(cu_seqlens_k, s0, s1);
+      const int64_t tq = cu_seqlens_q[s0], tk = cu_seqlens_k[s0];
+      return rlk_attn_prefill_states(&rp, adv(q, tq * params->num_q_heads * 128, 2),
+                                     adv(k, tk * params->num_kv_heads * 128, 2), adv(v, tk * params->num_kv_heads * 128, 2),
+                                     cq.data(), ck.data(), cp_rank, pair_base + before.n_pairs, state_o, state_lse,
+                                     stream);
+    });
+  }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state_o))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   SlabPlan plan;
@@ -414,9 +479,20 @@ rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const 
   if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
   if (!q || !k || !v) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if (params->num_seqs > rlk::kMaxSeqs)
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      const auto cq = rebase(cu_seqlens_q, s0, s1), ck = rebase(cu_seqlens_k, s0, s1);
+      const int64_t tq = cu_seqlens_q[s0], tk = cu_seqlens_k[s0];
+      const int64_t oq = tq * params->num_q_heads, ok_ = tk * params->num_kv_heads;
+      return rlk_attn_prefill(&rp, adv(q, oq * 128, 2), adv(k, ok_ * 128, 2), adv(v, ok_ * 128, 2), cq.data(),
+                              ck.data(), cp_rank, adv(out_f32, oq * 128, 4), adv(out_bf16, oq * 128, 2),
+                              adv(lse, oq, 4), stream);
+    });
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && !aligned16(out_bf16)))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   const int B = params->kv_block_size;
@@ -479,6 +555,15 @@ rlk_status decode_paged_impl(const rlk_attn_params* params, const void* q, const
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && !aligned16(out_bf16)))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  if (params->num_seqs > rlk::kMaxSeqs)
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      const int64_t o = static_cast<int64_t>(s0) * params->num_q_heads;
+      return decode_paged_impl(&rp, adv(q, o * 128, 2), k_pool, v_pool, n_pages, page_size,
+                               page_table + static_cast<int64_t>(s0) * max_pages, max_pages, seqlens + s0, rope_table,
+                               rope_max_pos, adv(out_f32, o * 128, 4), adv(out_bf16, o * 128, 2), adv(lse, o, 4),
+                               stream);
+    });
   const int B = params->kv_block_size;
   if (page_size < 8 || page_size > B || B % page_size)
     return fail(RLK_ERR_UNSUPPORTED, "page_size %d must be >= 8 and divide kv_block_size %d", page_size, B);
@@ -499,6 +584,7 @@ rlk_status decode_paged_impl(const rlk_attn_params* params, const void* q, const
         return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: position %d is past the RoPE table (%d positions)", s,
                     seqlens[s] - 1, rope_max_pos);
   }
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   const int group = params->num_q_heads / params->num_kv_heads;
@@ -602,6 +688,14 @@ rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, 
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
   if (num_heads < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "num_heads %d < 1", num_heads);
   if (cu_seqlens[0] != 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0");
+  if (params->num_seqs > rlk::kMaxSeqs)
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      const auto cu = rebase(cu_seqlens, s0, s1);
+      const int64_t o = static_cast<int64_t>(cu_seqlens[s0]) * num_heads * 128;
+      return rlk_attn_rope(&rp, adv(x, o, 2), adv(y, o, 2), num_heads, cu.data(),
+                           pos_offset ? pos_offset + s0 : nullptr, table, max_pos, stream);
+    });
   for (int s = 0; s < params->num_seqs; ++s) {
     const int64_t len = static_cast<int64_t>(cu_seqlens[s + 1]) - cu_seqlens[s];
     if (len < 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens not monotone at sequence %d", s);
@@ -613,6 +707,7 @@ rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, 
   }
   const int64_t rows = static_cast<int64_t>(cu_seqlens[params->num_seqs]) * num_heads;
   if (rows == 0) return ok();
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   auto rp = std::make_unique<rlk::RopeParams>();
@@ -701,6 +796,18 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   if (!q || !k_pool || !v_pool || !page_table || !seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
   if (split_k < 0 || split_k > 64) return fail(RLK_ERR_INVALID_ARGUMENT, "split_k %d not in 0..64", split_k);
+  if (params->num_seqs > rlk::kMaxSeqs)
+    // each range reuses the workspace from its start (the ranges run in
+    // order on the stream, and a range's state table is no larger than the
+    // whole call's)
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      const int64_t o = static_cast<int64_t>(s0) * params->num_q_heads;
+      return decode_splitk_impl(&rp, adv(q, o * 128, 2), k_pool, v_pool, n_pages, page_size,
+                                page_table + static_cast<int64_t>(s0) * max_pages, max_pages, seqlens + s0, split_k,
+                                rope_table, rope_max_pos, adv(out_f32, o * 128, 4), adv(out_bf16, o * 128, 2),
+                                adv(lse, o, 4), workspace, workspace_bytes, stream);
+    });
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && !aligned16(out_bf16)) || !aligned16(workspace))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
@@ -728,6 +835,7 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   const size_t need = rlk_attn_workspace_size(params, RLK_OP_DECODE_SPLIT, nullptr, seqlens);
   if (!workspace || workspace_bytes < need)
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   if (split_k == 0) {
@@ -854,6 +962,78 @@ size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const 
   return 0;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The merge of one launch's sequence range [seq_base, seq_base + num_seqs)
+// of a call over total_seqs sequences: cu_q / cu_k are the range's (rebased),
+// out / lse point at the range's first row, and the slab table, state table
+// and index scratch are the whole call's.
+rlk_status merge_range(const rlk_attn_params* params, const int32_t* cu_q, const int32_t* cu_k, int seq_base,
+                       int total_seqs, const rlk_attn_slab* slabs, int64_t n_slabs, const float* state_o,
+                       const float* state_lse, int64_t n_state_pairs, float* out_f32, void* out_bf16, float* lse,
+                       int32_t* index, const DeviceInfo* dev, cudaStream_t stream) {
+  const int64_t total_rows = cu_q[params->num_seqs];
+  if (total_rows == 0) return ok();
+  auto mp = std::make_unique<rlk::MergeParams>();
+  std::memset(mp.get(), 0, sizeof(*mp));
+  mp->err = dev->err;
+  mp->num_seqs = params->num_seqs;
+  mp->hq = params->num_q_heads;
+  mp->block = params->kv_block_size;
+  int max_blocks = 1;
+  for (int s = 0; s < params->num_seqs; ++s)
+    max_blocks = std::max(max_blocks, (cu_k[s + 1] - cu_k[s] + params->kv_block_size - 1) / params->kv_block_size);
+  mp->max_blocks = max_blocks;
+  mp->seq_base = seq_base;
+  mp->total_seqs = total_seqs;
+  mp->total_rows = total_rows;
+  mp->n_slabs = n_slabs;
+  mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
+  mp->state_o = state_o;
+  mp->state_lse = state_lse;
+  mp->n_pairs = n_state_pairs;
+  mp->index = index;
+  mp->out_f32 = out_f32;
+  mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+  mp->lse = lse;
+  for (int s = 0; s <= params->num_seqs; ++s) {
+    mp->cu_q[s] = cu_q[s];
+    mp->cu_k[s] = cu_k[s];
+  }
+  const cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
+  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// Both merge entry points after their own checks: the whole call, or its
+// kMaxSeqs-sequence ranges in order (each range indexes only its own
+// sequences' slabs, so the index scratch is reused range after range).
+rlk_status merge_call(const rlk_attn_params* params, const int32_t* cu_q, const int32_t* cu_k,
+                      const rlk_attn_slab* slabs, int64_t n_slabs, const float* state_o, const float* state_lse,
+                      int64_t n_state_pairs, float* out_f32, void* out_bf16, float* lse, int32_t* index,
+                      const DeviceInfo* dev, cudaStream_t stream) {
+  if (params->num_seqs <= rlk::kMaxSeqs)
+    return merge_range(params, cu_q, cu_k, 0, params->num_seqs, slabs, n_slabs, state_o, state_lse, n_state_pairs,
+                       out_f32, out_bf16, lse, index, dev, stream);
+  for (int s0 = 0; s0 < params->num_seqs; s0 += rlk::kMaxSeqs) {
+    const int s1 = std::min(params->num_seqs, s0 + rlk::kMaxSeqs);
+    const rlk_attn_params rp = range_params(params, s0, s1);
+    const auto cq = rebase(cu_q, s0, s1), ck = rebase(cu_k, s0, s1);
+    const int64_t o = static_cast<int64_t>(cu_q[s0]) * params->num_q_heads;
+    const rlk_status st = merge_range(&rp, cq.data(), ck.data(), s0, params->num_seqs, slabs, n_slabs, state_o,
+                                      state_lse, n_state_pairs, adv(out_f32, o * 128, 4), adv(out_bf16, o * 128, 2),
+                                      adv(lse, o, 4), index, dev, stream);
+    if (st) return st;
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
 rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                  const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs, int64_t n_slabs,
                                  const float* state_o, const float* state_lse, int64_t n_state_pairs,
@@ -873,40 +1053,10 @@ rlk_status rlk_attn_merge_states(const rlk_attn_params* params, const int32_t* c
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
-  const int64_t total_rows = cu_seqlens_q[params->num_seqs];
-  if (total_rows == 0) return ok();
-  auto mp = std::make_unique<rlk::MergeParams>();
-  std::memset(mp.get(), 0, sizeof(*mp));
-  mp->err = dev->err;
-  mp->num_seqs = params->num_seqs;
-  mp->hq = params->num_q_heads;
-  mp->block = params->kv_block_size;
-  int max_blocks = 1;
-  for (int s = 0; s < params->num_seqs; ++s)
-    max_blocks = std::max(max_blocks, (cu_seqlens_k[s + 1] - cu_seqlens_k[s] + params->kv_block_size - 1) /
-                                          params->kv_block_size);
-  mp->max_blocks = max_blocks;
-  mp->total_rows = total_rows;
-  mp->n_slabs = n_slabs;
-  mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
-  mp->state_o = state_o;
-  mp->state_lse = state_lse;
-  mp->n_pairs = n_state_pairs;
-  mp->index = static_cast<int32_t*>(workspace);
-  mp->out_f32 = out_f32;
-  mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
-  mp->lse = lse;
-  for (int s = 0; s <= params->num_seqs; ++s) {
-    mp->cu_q[s] = cu_seqlens_q[s];
-    mp->cu_k[s] = cu_seqlens_k[s];
-  }
-  cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
-  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
-  return ok();
+  return merge_call(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, state_o, state_lse, n_state_pairs, out_f32,
+                    out_bf16, lse, static_cast<int32_t*>(workspace), dev, stream);
 }
 
-// Same merge as rlk_attn_merge_states, for callers that cannot allocate:
-// the index scratch is the library's own file-scope device array.
 rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const int32_t* cu_seqlens_q,
                                          const int32_t* cu_seqlens_k, const rlk_attn_slab* slabs,
                                          int64_t n_slabs, const float* state_o, const float* state_lse,
@@ -933,32 +1083,8 @@ rlk_status rlk_attn_merge_states_noalloc(const rlk_attn_params* params, const in
                 static_cast<long long>(rlk::kNoAllocIndexEntries));
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
-  const int64_t total_rows = cu_seqlens_q[params->num_seqs];
-  if (total_rows == 0) return ok();
-  auto mp = std::make_unique<rlk::MergeParams>();
-  std::memset(mp.get(), 0, sizeof(*mp));
-  mp->err = dev->err;
-  mp->num_seqs = params->num_seqs;
-  mp->hq = params->num_q_heads;
-  mp->block = params->kv_block_size;
-  mp->max_blocks = max_blocks;
-  mp->total_rows = total_rows;
-  mp->n_slabs = n_slabs;
-  mp->slabs = reinterpret_cast<const rlk::Slab*>(slabs);
-  mp->state_o = state_o;
-  mp->state_lse = state_lse;
-  mp->n_pairs = n_state_pairs;
-  mp->index = dev->merge_scratch;
-  mp->out_f32 = out_f32;
-  mp->out_bf16 = static_cast<uint16_t*>(out_bf16);
-  mp->lse = lse;
-  for (int s = 0; s <= params->num_seqs; ++s) {
-    mp->cu_q[s] = cu_seqlens_q[s];
-    mp->cu_k[s] = cu_seqlens_k[s];
-  }
-  const cudaError_t e = rlk::launch_merge(*mp, dev->num_sms, stream);
-  if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
-  return ok();
+  return merge_call(params, cu_seqlens_q, cu_seqlens_k, slabs, n_slabs, state_o, state_lse, n_state_pairs, out_f32,
+                    out_bf16, lse, dev->merge_scratch, dev, stream);
 }
 
 rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const void* k, const void* v,
@@ -971,12 +1097,25 @@ rlk_status rlk_attn_backward(const rlk_attn_params* params, const void* q, const
   if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
   if (!q || !k || !v || !out_f32 || !dout || !lse || !dq || !dk || !dv)
     return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
+  if (params->kv_block_size != 128) return fail(RLK_ERR_UNSUPPORTED, "the backward takes KV block 128");
+  if (params->num_seqs > rlk::kMaxSeqs)
+    return over_ranges(params->num_seqs, [&](int s0, int s1) {
+      const rlk_attn_params rp = range_params(params, s0, s1);
+      const auto cu = rebase(cu_seqlens, s0, s1);
+      const int64_t t = cu_seqlens[s0];
+      const int64_t oq = t * params->num_q_heads, ok_ = t * params->num_kv_heads;
+      return rlk_attn_backward(&rp, adv(q, oq * 128, 2), adv(k, ok_ * 128, 2), adv(v, ok_ * 128, 2),
+                               adv(out_f32, oq * 128, 4), adv(dout, oq * 128, 2), adv(lse, oq, 4), cu.data(), cp_rank,
+                               adv(dq, oq * 128, 4), adv(dk, ok_ * 128, 4), adv(dv, ok_ * 128, 4), workspace,
+                               workspace_bytes, stream);
+    });
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_f32) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
   const size_t need = rlk::backward_workspace_bytes(params, cu_seqlens);
   if (!workspace || workspace_bytes < need)
     return fail(RLK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  if (g_dry_run) return ok();
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   st = rlk::run_backward(params, q, k, v, out_f32, dout, lse, cu_seqlens, cp_rank, dq, dk, dv, workspace,

@@ -23,33 +23,40 @@ __device__ __forceinline__ int first_row_of_block(int b, int B, int q_len, int k
   return max(0, b * B - (kv_len - q_len));
 }
 
-// A slab the merge may read: its sequence, block and row range agree with
-// the problem, and its hq * row_count state rows lie inside the table.
-__device__ __forceinline__ bool slab_ok(const MergeParams& p, const Slab& sl) {
-  if (sl.seq < 0 || sl.seq >= p.num_seqs || sl.block < 0 || sl.block >= p.max_blocks) return false;
-  const int q_len = p.cu_q[sl.seq + 1] - p.cu_q[sl.seq];
-  const int kv_len = p.cu_k[sl.seq + 1] - p.cu_k[sl.seq];
+// A slab of this launch's sequence range the merge may read: its sequence,
+// block and row range agree with the problem, and its hq * row_count state
+// rows lie inside the table.  (ls: the slab's sequence relative to the range.)
+__device__ __forceinline__ bool slab_ok(const MergeParams& p, const Slab& sl, int ls) {
+  if (ls < 0 || ls >= p.num_seqs || sl.block < 0 || sl.block >= p.max_blocks) return false;
+  const int q_len = p.cu_q[ls + 1] - p.cu_q[ls];
+  const int kv_len = p.cu_k[ls + 1] - p.cu_k[ls];
   return sl.block * p.block < kv_len && sl.row_begin == first_row_of_block(sl.block, p.block, q_len, kv_len) &&
          sl.row_count == q_len - sl.row_begin && sl.offset >= 0 &&
          sl.offset <= p.n_pairs - static_cast<int64_t>(p.hq) * sl.row_count;
 }
 
-// One CTA: index[s][b] = slab id, then check every valid slab owns its slot
-// (a slab that fails slab_ok is reported and never indexed, so its block
-// counts as missing unless another slab supplies it).
+// One CTA: index[s][b] = slab id for the slabs of this launch's sequence
+// range, then check every valid slab owns its slot (a slab that fails
+// slab_ok is reported and never indexed, so its block counts as missing
+// unless another slab supplies it).  Slabs of other ranges of the call are
+// left to those ranges' launches; a sequence id outside the call is bad.
 __global__ void __launch_bounds__(1024) rlk_merge_index_kernel(const __grid_constant__ MergeParams p) {
   const int n_idx = p.num_seqs * p.max_blocks;
   for (int i = threadIdx.x; i < n_idx; i += blockDim.x) p.index[i] = -1;
   __syncthreads();
   for (int64_t sid = threadIdx.x; sid < p.n_slabs; sid += blockDim.x) {
     const Slab sl = p.slabs[sid];
-    if (slab_ok(p, sl)) p.index[sl.seq * p.max_blocks + sl.block] = static_cast<int32_t>(sid);
+    const int ls = sl.seq - p.seq_base;
+    if (sl.seq < 0 || sl.seq >= p.total_seqs) report_error(p.err, kErrBadSlab, 0x501);
+    else if (ls < 0 || ls >= p.num_seqs) continue;
+    else if (slab_ok(p, sl, ls)) p.index[ls * p.max_blocks + sl.block] = static_cast<int32_t>(sid);
     else report_error(p.err, kErrBadSlab, 0x501);
   }
   __syncthreads();
   for (int64_t sid = threadIdx.x; sid < p.n_slabs; sid += blockDim.x) {
     const Slab sl = p.slabs[sid];
-    if (slab_ok(p, sl) && p.index[sl.seq * p.max_blocks + sl.block] != static_cast<int32_t>(sid))
+    const int ls = sl.seq - p.seq_base;
+    if (slab_ok(p, sl, ls) && p.index[ls * p.max_blocks + sl.block] != static_cast<int32_t>(sid))
       report_error(p.err, kErrDuplicateBlock, 0x502);
   }
 }

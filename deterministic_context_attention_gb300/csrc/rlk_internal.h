@@ -8,7 +8,8 @@
 namespace rlk {
 
 constexpr int kHeadDim = 128;           // D, the only head size the kernels take
-constexpr int kMaxSeqs = 128;           // sequences per call (they ride in kernel params)
+constexpr int kMaxSeqs = 128;           // sequences per launch (their tables ride in kernel params)
+constexpr int kMaxSeqsPerCall = 1 << 20;  // sequences per call: larger batches run as 128-sequence ranges
 constexpr int kMaxTilesPerLaunch = 880; // work tiles per launch (kernel param space)
 constexpr int kTileRows = 128;          // MMA M: query rows per tile
 constexpr int kDecodeMaxGroup = 8;     // query heads per KV head the transposed decode kernel takes
@@ -84,6 +85,8 @@ struct Slab {  // mirrors rlk_attn_slab
 struct MergeParams {
   ErrWord* err;
   int32_t num_seqs, hq, block, max_blocks;
+  int32_t seq_base;        // the slabs' sequence ids are seq_base + local index
+  int32_t total_seqs;      // sequences of the whole call (slab ids outside are bad)
   int64_t total_rows;      // query rows over all sequences
   int64_t n_slabs;
   const Slab* slabs;       // device, arrival order

@@ -42,6 +42,12 @@
  *   - Faults detected on the device (a wait that timed out, a bad page id, a
  *     duplicate or missing block in a state table) set the device error word;
  *     read it with rlk_attn_check_device_error().
+ *   - A batch may hold up to 2^20 sequences.  One launch's sequence tables
+ *     ride in kernel parameters and take 128 sequences, so a larger batch
+ *     runs as consecutive ranges of 128 sequences on `stream`, each range a
+ *     complete call on its own rows (every range is validated before the
+ *     first launch).  A sequence's arithmetic does not depend on the other
+ *     sequences of its batch, so the results are those of one launch.
  *   - Causal masking is bottom-right aligned: query row i of a sequence with
  *     q_len queries and kv_len keys sits at key position kv_len - q_len + i
  *     (q_len <= kv_len), so chunked-prefill replay passes the chunk's queries
@@ -74,7 +80,7 @@ typedef enum {
 
 /* Problem description shared by the entry points. */
 typedef struct {
-  int32_t num_seqs;      /* sequences in the batch, 1..128 */
+  int32_t num_seqs;      /* sequences in the batch, 1..1048576 */
   int32_t num_q_heads;   /* Hq */
   int32_t num_kv_heads;  /* Hkv, divides Hq */
   int32_t head_dim;      /* must be 128 */

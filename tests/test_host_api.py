@@ -261,3 +261,36 @@ def test_split_decode_rope_rejects_before_any_launch(lib):
         with pytest.raises(rlk.RlkError) as e:
             call(**kw)
         assert e.value.status == 1
+
+
+def test_large_batch_validates_every_range_before_any_launch(lib):
+    # 300 sequences run as ranges of 128; a context length of 0 in the third
+    # range must fail the whole call in its host checks, before the library
+    # touches the device (the tensor pointers are placeholders never read)
+    p = rlk.make_params(300, 8, 2, 128)
+    ctx = np.full(300, 64, np.int32)
+    ctx[260] = 0
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_decode_paged(p, 16, 16, 16, 8, 16, 16, 4, ctx, 16, None, 16, stream=0)
+    assert e.value.status == 1 and "sequence 4" in rlk.rlk_attn_last_error()  # index 260 is the 5th of range 2
+    cu = synth.cu_seqlens([5] * 300)
+    cuk = cu.copy()
+    cuk[270:] += 3  # sequence 269 has a longer KV side: fine ...
+    cq_bad = cu.copy()
+    cq_bad[281:] += 10  # ... but sequence 280 has q_len 15 > kv_len 5
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.rlk_attn_prefill(p, 16, 16, 16, cq_bad, cu, -1, 16, None, 16, stream=0)
+    assert e.value.status == 1
+
+
+def test_large_batch_plan_and_workspace(lib):
+    # the host-side helpers take the whole batch: the plan's slabs keep the
+    # batch's sequence ids and consecutive pair offsets
+    lens = [3] * 200
+    cu = synth.cu_seqlens(lens)
+    p = rlk.make_params(200, 8, 2, 64)
+    slabs, npairs = rlk.rlk_attn_plan_states(p, cu, cu, -1, 0)
+    assert len(slabs) == 200 and npairs == 200 * 3 * 8
+    assert list(slabs["seq"]) == list(range(200))
+    assert np.all(np.diff(slabs["offset"]) == 24)
+    assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_MERGE, cu, cu) >= 200 * 4
