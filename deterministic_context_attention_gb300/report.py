@@ -44,9 +44,7 @@ def _dlogp(out, vocab=512, seed=7):
     the same numpy arithmetic for every path compared."""
     rows = out.shape[0]
     x = np.ascontiguousarray(out.reshape(rows, -1), dtype=np.float32)
-    rng = np.random.default_rng([seed, x.shape[1], vocab])
-    w = (rng.standard_normal((x.shape[1], vocab)) / np.sqrt(x.shape[1])).astype(np.float32)
-    tok = rng.integers(0, vocab, size=rows)
+    w, tok = synth.lm_head(x.shape[1], rows, vocab, seed)
     logits = x @ w
     m = logits.max(axis=1, keepdims=True)
     lse = m[:, 0] + np.log(np.exp(logits - m).sum(axis=1, dtype=np.float32), dtype=np.float32)

@@ -208,6 +208,17 @@ CFG_DECODE = dict(n=64, ctx_lo=512, ctx_hi=32768, hq=32, hkv=8, d=128, page_size
 CFG_BACKWARD = dict(lens=[4096, 4096], hq=32, hkv=8, d=128, block=128, seed=4)
 
 
+def lm_head(width: int, rows: int, vocab: int = 512, seed: int = 7):
+    """The seeded synthetic lm_head of the dlogp drift class: FP32 weights
+    W [width, vocab] ~ N(0, 1/width) and one selected token per row (uniform
+    over the vocabulary).  Only the draw lives here; the projection and the
+    log-softmax are computed by whoever checks the outputs."""
+    g = np.random.default_rng([seed, width, vocab])
+    w = (g.standard_normal((width, vocab)) / np.sqrt(width)).astype(np.float32)
+    tok = g.integers(0, vocab, size=rows)
+    return w, tok
+
+
 def prefill_flops(cu_q, cu_k, hq, d) -> float:
     """Algorithmic causal flops: 4 * D * Hq * (visible (row, key) pairs)."""
     pairs = 0

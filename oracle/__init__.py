@@ -226,3 +226,21 @@ def rope_f64(x, pos, theta):
     y = np.empty(x.shape, np.float64)
     _check(lib.rlko_rope_f64(t, h, d, float(theta), _ptr(pos), _ptr(x), _ptr(y)), "rlko_rope_f64")
     return y
+
+
+def dlogp_f64(out, w, tok):
+    """Log-probability of the selected token per row under a linear head
+    ("WS2 Attention PR5 Drift Benchmark", the --include-dlogp paragraph: a
+    synthetic FP32 lm_head over the attention output and the selected-token
+    log-probability; "[WS2][Attention] H100 validation and reproduction
+    guide", Status: dlogp max abs 0.0).  FP64 by definition:
+        logit_j = sum_i x_i W_ij            (x: the row's outputs of all heads)
+        dlogp   = logit_tok - log sum_j exp(logit_j)
+    with the sum of exponentials taken relative to the row's largest logit.
+    out: [rows, ...] (flattened per row), w: [width, vocab], tok: [rows]."""
+    rows = out.shape[0]
+    x = np.asarray(out, np.float64).reshape(rows, -1)
+    logits = x @ np.asarray(w, np.float64)
+    m = logits.max(axis=1)
+    lse = m + np.log(np.exp(logits - m[:, None]).sum(axis=1))
+    return logits[np.arange(rows), np.asarray(tok)] - lse
