@@ -108,24 +108,37 @@ def bf16_ulp(x):
 
 def assert_forward_parity(out, outb, lse, ref_out, ref_lse, what=""):
     """FP32 out within TOL_OUT, lse within TOL_LSE, and BF16 out within one
-    BF16 ulp of the oracle rounded to BF16.  The BF16 output is the FP32
-    output rounded once, so where an element is so close to zero that the
-    FP32 tolerance exceeds a BF16 ulp, the BF16 gate reads as the FP32 gate
-    plus half an ulp of that final rounding."""
+    BF16 ulp of the oracle rounded to BF16.
+
+    The BF16 output must be the FP32 output rounded once (round to nearest
+    even), bit for bit: that is the "downcast only at the final write"
+    statement itself.  Given that, BF16 out lands within one BF16 ulp of
+    bf16(oracle) whenever the FP32 error is at most half a BF16 ulp at the
+    oracle's magnitude; only elements whose FP32 error exceeds that (values
+    so close to zero that a BF16 ulp is below the FP32 error) are exempt from
+    the one-ulp gate, and they still pass the FP32 gate and the bitwise
+    rounding check.  Returns (max out error, max lse error, max BF16 ulp
+    distance over the gated elements, number of exempt elements)."""
+    from deterministic_context_attention_gb300.synth import bf16_round
     assert np.isfinite(out).all(), what
     e_out = float(np.abs(out - ref_out).max())
     e_lse = float(np.abs(lse - ref_lse).max())
-    ref_b = ref_out.astype(np.float32)
-    ulp = np.abs(bf16_ordered(outb) - bf16_ordered(ref_b))
-    near_zero_ok = np.abs(outb.astype(np.float64) - ref_out) <= TOL_OUT + 0.5 * bf16_ulp(outb)
-    bad = (ulp > TOL_BF16_ULP) & ~near_zero_ok
     assert e_out <= TOL_OUT, f"{what}: max |out - oracle| = {e_out:.3g}"
     assert e_lse <= TOL_LSE, f"{what}: max |lse - oracle| = {e_lse:.3g}"
+    rounded = bf16_round(np.asarray(out, np.float32))
+    if not np.array_equal(np.asarray(outb, np.float32).view(np.uint32), rounded.view(np.uint32)):
+        n = int(np.sum(np.asarray(outb, np.float32).view(np.uint32) != rounded.view(np.uint32)))
+        raise AssertionError(f"{what}: BF16 out is not bf16_rn(FP32 out) in {n} elements")
+    ref_b = ref_out.astype(np.float32)
+    ulp = np.abs(bf16_ordered(outb) - bf16_ordered(ref_b))
+    exempt = np.abs(out.astype(np.float64) - ref_out) > 0.5 * bf16_ulp(ref_out)
+    bad = (ulp > TOL_BF16_ULP) & ~exempt
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: BF16 out {int(ulp[tuple(i)])} ulp from the oracle at {tuple(i)}: "
                              f"gpu {outb[tuple(i)]!r} oracle {ref_out[tuple(i)]!r}")
-    return e_out, e_lse, int(ulp[~near_zero_ok].max()) if (~near_zero_ok).any() else 0
+    gated = ~exempt
+    return e_out, e_lse, int(ulp[gated].max()) if gated.any() else 0, int(exempt.sum())
 
 
 def assert_bitwise(a, b, what=""):

@@ -41,6 +41,33 @@ def rel_l2(x, ref):
     return float(np.linalg.norm((x - ref).ravel()) / np.linalg.norm(ref.ravel()))
 
 
+TOL_GRAD_ROW = 1e-3
+
+
+def assert_grad_parity(got, ref, name):
+    """The whole-tensor relative L2 gate, and a row-by-row check that no row
+    or block is wrong: for every (row, head) vector, |got - ref|_2 <=
+    TOL_GRAD_ROW * max(|ref|_2, RMS row norm of ref).  A row's own norm is
+    the wrong yardstick on its own: each row of dS sums to zero, so a
+    gradient row can cancel to near zero (a query that sees one key has an
+    exactly zero dQ) while its rounding stays at the scale of its terms; and
+    FP32 rounding spreads unevenly over rows (at 2 x 4096 the largest dK/dV
+    rows carry up to ~1.5e-4 of their norm while the tensor's relative L2 is
+    6e-5).  A wrong row or block shows an error of the order of the row
+    itself, far above this bound."""
+    assert np.isfinite(got).all(), name
+    e = rel_l2(got, ref)
+    assert e <= TOL_GRAD_REL_L2, f"{name}: relative L2 {e:.3g}"
+    g = got.reshape(-1, got.shape[-1]).astype(np.float64)
+    r = ref.reshape(-1, ref.shape[-1]).astype(np.float64)
+    rn = np.linalg.norm(r, axis=1)
+    rms = float(np.sqrt(np.mean(rn ** 2)))
+    ratio = np.linalg.norm(g - r, axis=1) / np.maximum(rn, rms)
+    worst = int(np.argmax(ratio))
+    assert ratio[worst] <= TOL_GRAD_ROW, f"{name}: row {worst} error {ratio[worst]:.3g} of max(row, RMS row) norm"
+    return e, float(ratio[worst])
+
+
 def assert_bitwise3(a, b, what):
     for x, y, name in zip(a, b, ("dq", "dk", "dv")):
         if not np.array_equal(x.view(np.uint32), y.view(np.uint32)):
@@ -59,9 +86,7 @@ def test_backward_parity_small(small):
     dq, dk, dv = forward_and_backward(prob, dout)
     rq, rk, rv = oracle.backward_f64(prob.q, prob.k, prob.v, dout, prob.cu_q, prob.scale)
     for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
-        assert np.isfinite(got).all(), name
-        e = rel_l2(got, ref)
-        assert e <= TOL_GRAD_REL_L2, f"{name}: relative L2 {e:.3g}"
+        assert_grad_parity(got, ref, name)
 
 
 @pytest.mark.parametrize("cp", [2, 4])
@@ -82,16 +107,18 @@ def full():
     return prob, dout, qkv, forward_and_backward(prob, dout, qkv=qkv)
 
 
-def test_backward_fullsize_parity(full):
+@pytest.mark.parametrize("s,g", [(0, 0), (0, 7), (1, 2), (1, 5)])
+def test_backward_fullsize_parity(full, s, g):
+    # four (sequence, KV head) pairs of the 2 x 4096 workload: both
+    # sequences, the first and last KV heads; each pair is its 4 query heads'
+    # dQ and the KV head's dK/dV over all 4096 rows
     prob, dout, _, (dq, dk, dv) = full
-    s, g = 1, 5
     rq, rk, rv = oracle.backward_f64(prob.q, prob.k, prob.v, dout, prob.cu_q, prob.scale, only_seq=s, only_group=g)
     a, b = prob.cu_q[s], prob.cu_q[s + 1]
     heads = slice(g * 4, g * 4 + 4)
     for got, ref, name in ((dq[a:b, heads], rq[a:b, heads], "dq"), (dk[a:b, g], rk[a:b, g], "dk"),
                            (dv[a:b, g], rv[a:b, g], "dv")):
-        e = rel_l2(got, ref)
-        assert e <= TOL_GRAD_REL_L2, f"{name}: relative L2 {e:.3g}"
+        assert_grad_parity(got, ref, f"{name} (seq {s}, KV head {g})")
     assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
 
 
