@@ -10,8 +10,9 @@ inputs resident in HBM; L2 is flushed (a 512 MB write) before every timed
 step and each step is timed with CUDA events on the launch stream.  `value`
 is algorithmic TFLOP/s = 4*D*Hq*sum(visible (row, key) pairs) / time.  `e2e`
 is the same metric through the public API from pinned host buffers
-(host->device copy of q/k/v, the prefill, device->host copy of out_bf16 and
-lse every step) over K pipelined steps: uploads, compute and downloads on
+(host->device copy of q/k/v, the prefill, device->host copy of the same
+outputs as the headline -- out_f32, out_bf16 and lse -- every step) over K
+pipelined steps: uploads, compute and downloads on
 three streams with double-buffered device tensors, as a serving loop would
 run them.  Under torchrun every rank runs the same batch
 on its own GPU (weak scaling, no collective on the data path).
@@ -225,19 +226,22 @@ def run_gpu(args):
     peak = peaks["bf16_tflops"]
 
     # ---- end to end through the public API from pinned host buffers: every
-    # step copies its inputs host -> device, runs the prefill and copies the
-    # BF16 output and lse device -> host.  Steps are pipelined the way a
+    # step copies its inputs host -> device, runs the prefill and copies its
+    # outputs (FP32 and BF16 out and lse, the headline's output set) device ->
+    # host.  Steps are pipelined the way a
     # serving loop double-buffers them: step i+1's upload (one stream) and
     # step i-1's download (another) overlap step i's compute, ordered by
     # events; the timed region spans all K steps, copies included.
     qh = torch.from_numpy(synth.bf16_bits(prob.q).view(np.int16)).pin_memory()
     kh = torch.from_numpy(synth.bf16_bits(prob.k).view(np.int16)).pin_memory()
     vh = torch.from_numpy(synth.bf16_bits(prob.v).view(np.int16)).pin_memory()
+    out_h = [torch.empty((rows, 32, 128), dtype=torch.float32).pin_memory() for _ in range(2)]
     outb_h = [torch.empty((rows, 32, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     lse_h = [torch.empty((rows, 32), dtype=torch.float32).pin_memory() for _ in range(2)]
     qd = [torch.empty_like(qh, device="cuda") for _ in range(2)]
     kd = [torch.empty_like(kh, device="cuda") for _ in range(2)]
     vd = [torch.empty_like(vh, device="cuda") for _ in range(2)]
+    out_d = [torch.empty((rows, 32, 128), dtype=torch.float32, device="cuda") for _ in range(2)]
     outb_d = [torch.empty((rows, 32, 128), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     lse_d = [torch.empty((rows, 32), dtype=torch.float32, device="cuda") for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -262,12 +266,13 @@ def run_gpu(args):
             if i >= 2:
                 stream.wait_event(ev_out[i - 2])  # outputs b were read back
             rlk.rlk_attn_prefill(p, qd[b].view(torch.bfloat16), kd[b].view(torch.bfloat16), vd[b].view(torch.bfloat16),
-                                 prob.cu_q, prob.cu_k, -1, None, outb_d[b], lse_d[b], stream=stream)
+                                 prob.cu_q, prob.cu_k, -1, out_d[b], outb_d[b], lse_d[b], stream=stream)
             e = torch.cuda.Event()
             e.record(stream)
             ev_comp.append(e)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[i])
+                out_h[b].copy_(out_d[b], non_blocking=True)
                 outb_h[b].copy_(outb_d[b], non_blocking=True)
                 lse_h[b].copy_(lse_d[b], non_blocking=True)
                 e = torch.cuda.Event()
@@ -282,7 +287,7 @@ def run_gpu(args):
     e2e_ms = e2e_run(args.steps)
     rlk.rlk_attn_check_device_error(stream)
     h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
-    d2h = outb_h[0].numel() * 2 + lse_h[0].numel() * 4
+    d2h = out_h[0].numel() * 4 + outb_h[0].numel() * 2 + lse_h[0].numel() * 4
 
     extras = {}
     if not args.no_extras and rank == 0:
@@ -299,7 +304,7 @@ def run_gpu(args):
                        "l2": "flushed (512 MB write) before every timed step", "flops_per_step": flops},
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 5),
+                    "ms_per_step": round(e2e_ms, 5), "outputs": "out_f32 + out_bf16 + lse (the headline's set)",
                     "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i"},
             "gpu_launches": args.steps,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
