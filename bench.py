@@ -22,8 +22,9 @@ path (each with its own CUDA-event timing and L2 flush): "merge" (the
 canonical fold of the prefill's CP=1 state table), "states" (the state
 producer), "decode" (64 sequences, contexts U[512, 32768], 16-token pages),
 "decode_long" (4 x 32768 tokens: single pass against the split decode),
-"rope" (the RoPE pass over the prefill's Q and K, also after a flush that
-leaves L2 clean), "backward" (2 x 4096) and "chunked" (2 x 8192 in chunks of
+"rope" (the RoPE pass over the prefill's Q and K in one launch, also after a
+flush that leaves L2 clean), "prefill_rope" (the headline prefill with the
+queries' RoPE inside the kernel), "backward" (2 x 4096) and "chunked" (2 x 8192 in chunks of
 2048); --no-extras skips them.  --profile NAME runs one path a few times,
 untimed, for ncu.
 
@@ -292,6 +293,7 @@ def run_gpu(args):
     extras = {}
     if not args.no_extras and rank == 0:
         extras = measure_extras(torch, rlk, dv, peaks, prob, q, k, v, flush, stream, args)
+        extras["prefill_rope"] = measure_prefill_rope(torch, rlk, peaks, prob, q, k, v, flush, stream, args, ms)
 
     if rank == 0:
         line = {
@@ -451,11 +453,10 @@ def measure_rope(torch, rlk, dv, peaks, flush, stream, args):
     k = torch.randn((t, cfg["hkv"], 128), generator=g, device="cuda").to(torch.bfloat16)
     max_pos = max(cfg["lens"])
     table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
-    pr = rlk.make_params(len(cfg["lens"]))
+    pr = rlk.make_params(len(cfg["lens"]), cfg["hq"], cfg["hkv"])
 
     def step():
-        rlk.rlk_attn_rope(pr, q, q, cfg["hq"], cu, None, table, max_pos, stream=stream)
-        rlk.rlk_attn_rope(pr, k, k, cfg["hkv"], cu, None, table, max_pos, stream=stream)
+        rlk.rlk_attn_rope_qk(pr, q, q, k, k, cu, None, table, max_pos, stream=stream)
     ts = time_steps(torch, step, args.steps, args.warmup, flush, stream)
     # the same after a flush that leaves L2 clean: the 512 MB write leaves up
     # to 129 MB of dirty lines whose write-back a 182 MB pass otherwise pays
@@ -478,11 +479,40 @@ def measure_rope(torch, rlk, dv, peaks, flush, stream, args):
     nbytes = t * (cfg["hq"] + cfg["hkv"]) * 512
     ms, msc = float(np.mean(ts)), float(np.mean(tc))
     gbs, gbsc = nbytes / (ms * 1e-3) / 1e9, nbytes / (msc * 1e-3) / 1e9
-    return {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": nbytes, "launches_per_step": 2,
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": nbytes, "launches_per_step": 1,
             "frac": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
             "clean_l2": {"ms": round(msc, 4), "gbs": round(gbsc, 1), "frac": round(gbsc / peaks["hbm_gbs"], 4),
                          "flush": "512 MB write, then a 256 MB read (L2 left holding clean lines)"},
-            "workload": "RoPE in place on the varlen prefill Q [8897,32,128] and K [8897,8,128] (BF16)"}
+            "workload": "RoPE in place on the varlen prefill Q [8897,32,128] and K [8897,8,128] (BF16), one launch"}
+
+
+def measure_prefill_rope(torch, rlk, peaks, prob, q, k, v, flush, stream, args, plain_ms):
+    """The headline prefill with the queries' RoPE inside the kernel (pre-RoPE
+    q, post-RoPE k): against the plain prefill and against the RoPE pass on
+    the queries followed by the plain prefill."""
+    rows = q.shape[0]
+    max_pos = int(np.diff(prob.cu_k).max())
+    table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
+    p = rlk.make_params(4, 32, 8, 128, 1, rlk.ZIGZAG, prob.scale)
+    out = torch.empty((rows, 32, 128), dtype=torch.float32, device="cuda")
+    outb = torch.empty((rows, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, 32), dtype=torch.float32, device="cuda")
+    qr = torch.empty_like(q)
+    pr = rlk.make_params(4, 32, 8)
+    t_fused = time_steps(torch, lambda: rlk.rlk_attn_prefill_rope(p, q, k, v, prob.cu_q, prob.cu_k, -1, table, max_pos,
+                                                                   out, outb, lse, stream=stream),
+                         args.steps, args.warmup, flush, stream)
+
+    def two_step():
+        rlk.rlk_attn_rope(pr, q, qr, 32, prob.cu_q, None, table, max_pos, stream=stream)
+        rlk.rlk_attn_prefill(p, qr, k, v, prob.cu_q, prob.cu_k, -1, out, outb, lse, stream=stream)
+    t_two = time_steps(torch, two_step, args.steps, args.warmup, flush, stream)
+    rlk.rlk_attn_check_device_error(stream)
+    flops = synth.prefill_flops(prob.cu_q, prob.cu_k, 32, 128)
+    ms, ms2 = float(np.mean(t_fused)), float(np.mean(t_two))
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+            "vs_plain_prefill": round(ms / plain_ms, 4), "rope_pass_then_prefill_ms": round(ms2, 4),
+            "workload": "the headline prefill with pre-RoPE queries rotated inside the kernel (RoPE theta 1e6)"}
 
 
 def measure_decode_long(torch, rlk, dv, peaks, flush, stream, args, n=4, ctx_len=32768, split_k=(4, 8, 19)):

@@ -9,7 +9,7 @@ calls raise.
 Entry points (same names as the C ABI):
     rlk_attn_plan_states, rlk_attn_block_manifest_hash,
     rlk_attn_prefill_states, rlk_attn_merge_states, rlk_attn_merge_states_noalloc,
-    rlk_attn_prefill,
+    rlk_attn_prefill, rlk_attn_prefill_rope,
     rlk_attn_decode_paged, rlk_attn_backward, rlk_attn_workspace_size,
     rlk_attn_check_device_error, rlk_attn_last_error, rlk_attn_core_id
 """
@@ -88,11 +88,13 @@ def load():
             "rlk_attn_merge_states": [PP, P, P, P, i64, P, P, i64, P, P, P, P, sz, P],
             "rlk_attn_merge_states_noalloc": [PP, P, P, P, i64, P, P, i64, P, P, P, P],
             "rlk_attn_prefill": [PP, P, P, P, P, P, i32, P, P, P, P],
+            "rlk_attn_prefill_rope": [PP, P, P, P, P, P, i32, P, i32, P, P, P, P],
             "rlk_attn_decode_paged": [PP, P, P, P, i32, i32, P, i32, P, P, P, P, P],
             "rlk_attn_decode_paged_splitk": [PP, P, P, P, i32, i32, P, i32, P, i32, P, P, P, P, sz, P],
             "rlk_attn_decode_auto_split": [PP, P, i32],
             "rlk_attn_rope_table": [ctypes.c_double, i32, P],
             "rlk_attn_rope": [PP, P, P, i32, P, P, P, i32, P],
+            "rlk_attn_rope_qk": [PP, P, P, P, P, P, P, P, i32, P],
             "rlk_attn_decode_paged_rope": [PP, P, P, P, i32, i32, P, i32, P, P, i32, P, P, P, P],
             "rlk_attn_decode_paged_splitk_rope": [PP, P, P, P, i32, i32, P, i32, P, i32, P, i32, P, P, P, P, sz, P],
             "rlk_attn_backward": [PP, P, P, P, P, P, P, P, i32, P, P, P, P, sz, P],
@@ -234,6 +236,15 @@ def rlk_attn_prefill(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank, out_f
            "rlk_attn_prefill")
 
 
+def rlk_attn_prefill_rope(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank, rope_table, rope_max_pos, out_f32,
+                          out_bf16, lse, stream=None):
+    """rlk_attn_prefill with the pre-RoPE queries rotated inside the kernel."""
+    cq, ck = _i32_host(cu_seqlens_q), _i32_host(cu_seqlens_k)
+    _check(load().rlk_attn_prefill_rope(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
+                                        int(cp_rank), _ptr(rope_table), int(rope_max_pos), _ptr(out_f32),
+                                        _ptr(out_bf16), _ptr(lse), _stream(stream)), "rlk_attn_prefill_rope")
+
+
 def rlk_attn_decode_paged(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
                           out_f32, out_bf16, lse, stream=None):
     sl = _i32_host(seqlens)
@@ -278,6 +289,14 @@ def rlk_attn_rope(params, x, y, num_heads, cu_seqlens, pos_offset, table, max_po
     po = None if pos_offset is None else _i32_host(pos_offset)
     _check(load().rlk_attn_rope(ctypes.byref(params), _ptr(x), _ptr(y), int(num_heads), _ptr(cu), _ptr(po),
                                 _ptr(table), int(max_pos), _stream(stream)), "rlk_attn_rope")
+
+
+def rlk_attn_rope_qk(params, q, q_out, k, k_out, cu_seqlens, pos_offset, table, max_pos, stream=None):
+    """RoPE of the queries and keys of the same tokens in one launch."""
+    cu = _i32_host(cu_seqlens)
+    po = None if pos_offset is None else _i32_host(pos_offset)
+    _check(load().rlk_attn_rope_qk(ctypes.byref(params), _ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), _ptr(cu),
+                                   _ptr(po), _ptr(table), int(max_pos), _stream(stream)), "rlk_attn_rope_qk")
 
 
 def rlk_attn_decode_paged_rope(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,

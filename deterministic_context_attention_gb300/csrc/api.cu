@@ -470,24 +470,38 @@ rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q,
   return ok();
 }
 
-rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const void* k, const void* v,
-                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
-                            float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused prefill, with the query rows rotated by RoPE inside the kernel
+// when rope_table is given (at their absolute positions kv_len - q_len + i).
+rlk_status prefill_impl(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
+                        const float* rope_table, int32_t rope_max_pos, float* out_f32, void* out_bf16, float* lse,
+                        cudaStream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if ((st = check_cu(params, cu_seqlens_q, cu_seqlens_k))) return st;
   if (cp_rank < -1 || cp_rank >= params->cp_size) return fail(RLK_ERR_INVALID_ARGUMENT, "cp_rank %d", cp_rank);
   if (!q || !k || !v) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL tensor");
   if (!out_f32 && !out_bf16) return fail(RLK_ERR_INVALID_ARGUMENT, "out_f32 and out_bf16 are both NULL");
+  if (rope_table) {
+    if (!aligned16(rope_table)) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table must be 16-byte aligned");
+    for (int s = 0; s < params->num_seqs; ++s)
+      if (cu_seqlens_q[s + 1] > cu_seqlens_q[s] && cu_seqlens_k[s + 1] - cu_seqlens_k[s] > rope_max_pos)
+        return fail(RLK_ERR_INVALID_ARGUMENT, "sequence %d: position %d is past the RoPE table (%d positions)", s,
+                    cu_seqlens_k[s + 1] - cu_seqlens_k[s] - 1, rope_max_pos);
+  }
   if (params->num_seqs > rlk::kMaxSeqs)
     return over_ranges(params->num_seqs, [&](int s0, int s1) {
       const rlk_attn_params rp = range_params(params, s0, s1);
       const auto cq = rebase(cu_seqlens_q, s0, s1), ck = rebase(cu_seqlens_k, s0, s1);
       const int64_t tq = cu_seqlens_q[s0], tk = cu_seqlens_k[s0];
       const int64_t oq = tq * params->num_q_heads, ok_ = tk * params->num_kv_heads;
-      return rlk_attn_prefill(&rp, adv(q, oq * 128, 2), adv(k, ok_ * 128, 2), adv(v, ok_ * 128, 2), cq.data(),
-                              ck.data(), cp_rank, adv(out_f32, oq * 128, 4), adv(out_bf16, oq * 128, 2),
-                              adv(lse, oq, 4), stream);
+      return prefill_impl(&rp, adv(q, oq * 128, 2), adv(k, ok_ * 128, 2), adv(v, ok_ * 128, 2), cq.data(),
+                          ck.data(), cp_rank, rope_table, rope_max_pos, adv(out_f32, oq * 128, 4),
+                          adv(out_bf16, oq * 128, 2), adv(lse, oq, 4), stream);
     });
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out_f32 && !aligned16(out_f32)) ||
       (out_bf16 && !aligned16(out_bf16)))
@@ -538,8 +552,29 @@ rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const 
   fp->out_f32 = out_f32;
   fp->out_bf16 = static_cast<uint16_t*>(out_bf16);
   fp->lse = lse;
+  fp->rope_table = rope_table;
   if ((st = launch_fwd_tiles(fp.get(), tiles, params->num_q_heads, mq, mk, mv, dev, stream))) return st;
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
+                            float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream) {
+  return prefill_impl(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank, nullptr, 0, out_f32, out_bf16, lse,
+                      stream);
+}
+
+rlk_status rlk_attn_prefill_rope(const rlk_attn_params* params, const void* q, const void* k, const void* v,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
+                                 const float* rope_table, int32_t rope_max_pos, float* out_f32, void* out_bf16,
+                                 float* lse, rlk_stream_t stream) {
+  if (!rope_table) return fail(RLK_ERR_INVALID_ARGUMENT, "rope table is NULL");
+  return prefill_impl(params, q, k, v, cu_seqlens_q, cu_seqlens_k, cp_rank, rope_table, rope_max_pos, out_f32,
+                      out_bf16, lse, stream);
 }
 
 namespace {
@@ -678,23 +713,33 @@ rlk_status rlk_attn_rope_table(double theta, int32_t max_pos, float* table) {
   return ok();
 }
 
-rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads,
-                         const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table, int32_t max_pos,
-                         rlk_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The RoPE pass over x (num_heads heads) and, when x2 is given, over x2
+// (num_heads2 heads) of the same tokens, in one launch.
+rlk_status rope_impl(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads, const void* x2,
+                     void* y2, int32_t num_heads2, const int32_t* cu_seqlens, const int32_t* pos_offset,
+                     const float* table, int32_t max_pos, cudaStream_t stream) {
   rlk_status st = check_params(params);
   if (st) return st;
   if (!x || !y || !table || !cu_seqlens) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
   if (!aligned16(x) || !aligned16(y) || !aligned16(table))
     return fail(RLK_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
   if (num_heads < 1) return fail(RLK_ERR_INVALID_ARGUMENT, "num_heads %d < 1", num_heads);
+  if (x2 && (!y2 || !aligned16(x2) || !aligned16(y2) || num_heads2 < 1))
+    return fail(RLK_ERR_INVALID_ARGUMENT, "second tensor: NULL, unaligned or no heads");
   if (cu_seqlens[0] != 0) return fail(RLK_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0");
   if (params->num_seqs > rlk::kMaxSeqs)
     return over_ranges(params->num_seqs, [&](int s0, int s1) {
       const rlk_attn_params rp = range_params(params, s0, s1);
       const auto cu = rebase(cu_seqlens, s0, s1);
       const int64_t o = static_cast<int64_t>(cu_seqlens[s0]) * num_heads * 128;
-      return rlk_attn_rope(&rp, adv(x, o, 2), adv(y, o, 2), num_heads, cu.data(),
-                           pos_offset ? pos_offset + s0 : nullptr, table, max_pos, stream);
+      const int64_t o2 = static_cast<int64_t>(cu_seqlens[s0]) * num_heads2 * 128;
+      return rope_impl(&rp, adv(x, o, 2), adv(y, o, 2), num_heads, x2 ? adv(x2, o2, 2) : nullptr,
+                       x2 ? adv(y2, o2, 2) : nullptr, num_heads2, cu.data(), pos_offset ? pos_offset + s0 : nullptr,
+                       table, max_pos, stream);
     });
   for (int s = 0; s < params->num_seqs; ++s) {
     const int64_t len = static_cast<int64_t>(cu_seqlens[s + 1]) - cu_seqlens[s];
@@ -717,12 +762,37 @@ rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, 
   rp->table = table;
   rp->rows = rows;
   rp->heads = num_heads;
+  if (x2) {
+    rp->x2 = static_cast<const uint16_t*>(x2);
+    rp->y2 = static_cast<uint16_t*>(y2);
+    rp->rows2 = static_cast<int64_t>(cu_seqlens[params->num_seqs]) * num_heads2;
+    rp->heads2 = num_heads2;
+  }
   rp->num_seqs = params->num_seqs;
   for (int s = 0; s <= params->num_seqs; ++s) rp->cu[s] = cu_seqlens[s];
   for (int s = 0; s < params->num_seqs; ++s) rp->pos0[s] = pos_offset ? pos_offset[s] : 0;
   cudaError_t e = rlk::launch_rope(*rp, dev->num_sms, stream);
   if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads,
+                         const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table, int32_t max_pos,
+                         rlk_stream_t stream) {
+  return rope_impl(params, x, y, num_heads, nullptr, nullptr, 0, cu_seqlens, pos_offset, table, max_pos, stream);
+}
+
+rlk_status rlk_attn_rope_qk(const rlk_attn_params* params, const void* q, void* q_out, const void* k, void* k_out,
+                            const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table,
+                            int32_t max_pos, rlk_stream_t stream) {
+  if (!params) return fail(RLK_ERR_INVALID_ARGUMENT, "params is NULL");
+  if (!k || !k_out) return fail(RLK_ERR_INVALID_ARGUMENT, "NULL argument");
+  return rope_impl(params, q, q_out, params->num_q_heads, k, k_out, params->num_kv_heads, cu_seqlens, pos_offset,
+                   table, max_pos, stream);
 }
 
 

@@ -73,7 +73,7 @@ struct FwdLayout {
   static constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = kKFull + kSK, kVFull = kKEmpty + kSK,
                        kVEmpty = kVFull + kSV, kSFull = kVEmpty + kSV, kPFull = kSFull + 2, kPVFull = kPFull + 2,
                        kPVEmpty = kPVFull + 2, kStatsFull = kPVEmpty + 2, kXch = kStatsFull + kStatsRing,
-                       kNumBars = kXch + 4;
+                       kQRot = kXch + 4, kNumBars = kQRot + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kStatsOff = (kMiscOff + 16 + 15) / 16 * 16;
   // softmax exchange: the half maxima and half sums of every row, [2][128] each
@@ -235,7 +235,40 @@ __device__ __forceinline__ float half_probs(uint32_t ta, uint32_t (&s)[NC][32], 
   return partial_tree(part);
 }
 
-template <int B, int MODE>
+// RoPE of one quarter of a query row in the shared-memory tile (128-byte
+// swizzle, two 64-column halves of kQHalf bytes): pairs 32h .. 32h + 31 of
+// row r, i.e. 16-byte chunks 4h .. 4h + 3 of the first half and the chunks at
+// the same swizzled offsets of the second half.  trow: the row's position in
+// the table, advanced to cos[32h] (sin follows 64 floats later).  One chunk
+// at a time (the table lines were prefetched into L1), so few registers are
+// live.
+__device__ __forceinline__ void rope_row_quarter(const float* trow, uint8_t* q_tile, int r, int h) {
+  const float4* t4 = reinterpret_cast<const float4*>(trow);
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    const float4 x0 = __ldg(t4 + 2 * cc), x1 = __ldg(t4 + 2 * cc + 1);
+    const float4 y0 = __ldg(t4 + 16 + 2 * cc), y1 = __ldg(t4 + 16 + 2 * cc + 1);
+    const float c[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const float sn[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    const int pj = (4 * h + cc) ^ (r & 7);
+    uint4* pa = reinterpret_cast<uint4*>(q_tile + r * 128 + pj * 16);
+    uint4* pb = reinterpret_cast<uint4*>(q_tile + FwdLayout<128>::kQHalf + r * 128 + pj * 16);
+    uint4 a = *pa, b = *pb;
+    rope_words8(a, b, c, sn);
+    *pa = a;
+    *pb = b;
+  }
+}
+// Bring a quarter row of the table (128 B of cos, 128 B of sin) towards the
+// SM ahead of its use.
+__device__ __forceinline__ void rope_prefetch(const float* trow) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(trow));
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(trow + 64));
+}
+
+// ROPE (fused mode only): the query tile is rotated in shared memory by the
+// softmax warps before the first S of each item (the table in p.rope_table).
+template <int B, int MODE, bool ROPE>
 __global__ void __launch_bounds__(512, 1)
     rlk_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -271,6 +304,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int s = 0; s < SR; ++s) mbar_init(&bars[L::kStatsFull + s], 128);
     for (int s = 0; s < 4; ++s) mbar_init(&bars[L::kXch + s], 64);
+    mbar_init(&bars[L::kQRot], 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -399,7 +433,8 @@ __global__ void __launch_bounds__(512, 1)
         const int item = snake_item(round);
         if (item >= p.num_items) continue;
         const ItemInfo it = item_info<MODE>(p, item);
-        bool ok = mbar_wait(&bars[L::kQFull], q_it & 1, abort, p.err, 0x201);
+        // with RoPE in the prefill the softmax warps hand over the rotated tile
+        bool ok = mbar_wait(&bars[ROPE ? L::kQRot : L::kQFull], q_it & 1, abort, p.err, 0x201);
         if (!__all_sync(0xffffffffu, ok)) break;
         ++q_it;
         const uint32_t kb = k_it, vb = v_it, sb = s_it, pb = pv_it;
@@ -496,7 +531,7 @@ __global__ void __launch_bounds__(512, 1)
     const int quad = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     uint64_t* xbar = &bars[L::kXch + quad];  // the quadrant's two warps meet here
-    uint32_t x_par = 0;
+    uint32_t x_par = 0, q_par = 0;
     float* xmax = reinterpret_cast<float*>(smem + L::kXchOff);  // [2][128]
     float* xsum = xmax + 2 * kTileRows;                          // [2][128]
     uint32_t s_it = 0, st_it = 0;
@@ -510,6 +545,21 @@ __global__ void __launch_bounds__(512, 1)
       const bool warp_rows = __any_sync(0xffffffffu, valid);
       const int pos = (MODE == kModeDecode) ? it.kv_len - 1 : it.kv_len - it.q_len + it.row_begin + r;
       bool fail = false;
+      if (ROPE) {
+        // RoPE of the item's query tile, in place in shared memory, while the
+        // tensor core finishes the previous item: thread (h, r) rotates row
+        // r's pairs 32h .. 32h + 31 -- 16-byte chunks 4h .. 4h + 3 of the
+        // first half, whose partners (element i + 64) sit at the same
+        // swizzled offset of the second half.  The table rows are fetched
+        // before the tile lands.
+        if (valid) rope_prefetch(p.rope_table + static_cast<int64_t>(pos) * kHeadDim + 32 * h);
+        bool w = mbar_wait(&bars[L::kQFull], q_par, abort, p.err, 0x304);
+        q_par ^= 1;
+        if (!__all_sync(0xffffffffu, w)) break;
+        if (valid) rope_row_quarter(p.rope_table + static_cast<int64_t>(pos) * kHeadDim + 32 * h, smem + L::kQOff, r, h);
+        fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+        mbar_arrive(&bars[L::kQRot]);
+      }
       for (int j = 0; j < it.nb; ++j) {
         const int b = it.blk0 + j;
         const uint32_t buf = s_it & 1;
@@ -761,10 +811,10 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ---------------------------------------------------------------- launchers
-template <int B, int MODE>
+template <int B, int MODE, bool ROPE>
 static cudaError_t configure_fwd_t() {
   using L = FwdLayout<B>;
-  auto kern = rlk_fwd_kernel<B, MODE>;
+  auto kern = rlk_fwd_kernel<B, MODE, ROPE>;
   // The warpgroup register split (208 / 128 / 128 / 48) needs the launch to
   // grant 128 registers per thread; with fewer, setmaxnreg.inc would wait
   // forever.
@@ -772,8 +822,8 @@ static cudaError_t configure_fwd_t() {
   cudaError_t e = cudaFuncGetAttributes(&a, kern);
   if (e != cudaSuccess) return e;
   if (a.numRegs < kRegsLaunch) {
-    fprintf(stderr, "rlk_fwd_kernel<%d,%d>: %d registers at launch, the warpgroup split needs %d\n", B, MODE,
-            a.numRegs, kRegsLaunch);
+    fprintf(stderr, "rlk_fwd_kernel<%d,%d,%d>: %d registers at launch, the warpgroup split needs %d\n", B, MODE,
+            ROPE ? 1 : 0, a.numRegs, kRegsLaunch);
     return cudaErrorInvalidConfiguration;
   }
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -781,34 +831,41 @@ static cudaError_t configure_fwd_t() {
 
 cudaError_t configure_fwd_kernels() {
   cudaError_t e;
-  if ((e = configure_fwd_t<128, kModeFused>()) != cudaSuccess) return e;
-  if ((e = configure_fwd_t<128, kModeStates>()) != cudaSuccess) return e;
-  if ((e = configure_fwd_t<128, kModeDecode>()) != cudaSuccess) return e;
-  if ((e = configure_fwd_t<64, kModeFused>()) != cudaSuccess) return e;
-  if ((e = configure_fwd_t<64, kModeStates>()) != cudaSuccess) return e;
-  return configure_fwd_t<64, kModeDecode>();
+  if ((e = configure_fwd_t<128, kModeFused, false>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<128, kModeFused, true>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<128, kModeStates, false>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<128, kModeDecode, false>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<64, kModeFused, false>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<64, kModeFused, true>()) != cudaSuccess) return e;
+  if ((e = configure_fwd_t<64, kModeStates, false>()) != cudaSuccess) return e;
+  return configure_fwd_t<64, kModeDecode, false>();
 }
 
-template <int B, int MODE>
+template <int B, int MODE, bool ROPE>
 static cudaError_t launch_fwd_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t stream) {
-  rlk_fwd_kernel<B, MODE><<<grid, kThreads, FwdLayout<B>::kAlloc, stream>>>(p, tq, tk, tv);
+  rlk_fwd_kernel<B, MODE, ROPE><<<grid, kThreads, FwdLayout<B>::kAlloc, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  const bool rope = p.rope_table != nullptr;
   if (p.block == 128) {
     switch (p.mode) {
-      case kModeFused: return launch_fwd_t<128, kModeFused>(p, tq, tk, tv, grid, stream);
-      case kModeStates: return launch_fwd_t<128, kModeStates>(p, tq, tk, tv, grid, stream);
-      case kModeDecode: return launch_fwd_t<128, kModeDecode>(p, tq, tk, tv, grid, stream);
+      case kModeFused:
+        return rope ? launch_fwd_t<128, kModeFused, true>(p, tq, tk, tv, grid, stream)
+                    : launch_fwd_t<128, kModeFused, false>(p, tq, tk, tv, grid, stream);
+      case kModeStates: return launch_fwd_t<128, kModeStates, false>(p, tq, tk, tv, grid, stream);
+      case kModeDecode: return launch_fwd_t<128, kModeDecode, false>(p, tq, tk, tv, grid, stream);
     }
   } else if (p.block == 64) {
     switch (p.mode) {
-      case kModeFused: return launch_fwd_t<64, kModeFused>(p, tq, tk, tv, grid, stream);
-      case kModeStates: return launch_fwd_t<64, kModeStates>(p, tq, tk, tv, grid, stream);
-      case kModeDecode: return launch_fwd_t<64, kModeDecode>(p, tq, tk, tv, grid, stream);
+      case kModeFused:
+        return rope ? launch_fwd_t<64, kModeFused, true>(p, tq, tk, tv, grid, stream)
+                    : launch_fwd_t<64, kModeFused, false>(p, tq, tk, tv, grid, stream);
+      case kModeStates: return launch_fwd_t<64, kModeStates, false>(p, tq, tk, tv, grid, stream);
+      case kModeDecode: return launch_fwd_t<64, kModeDecode, false>(p, tq, tk, tv, grid, stream);
     }
   }
   return cudaErrorInvalidValue;

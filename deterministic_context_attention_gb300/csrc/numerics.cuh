@@ -158,6 +158,32 @@ __device__ __forceinline__ float fold_elem(float O, float o, float alpha, float 
   return __fmaf_rn(o, beta, __fmul_rn(O, alpha));
 }
 
+// RoPE of one rotate-half pair (x0 = element i, x1 = element i + 64) with
+// the table's FP32 cos / sin of its position and frequency, in the one FP32
+// form every RoPE path of the library uses (the products rounded to FP32 on
+// their own, then one fma each):
+//   y0 = fma(x0, c, -(x1 * s)),  y1 = fma(x1, c, x0 * s)
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0, float& y1) {
+  y0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
+  y1 = __fmaf_rn(x1, c, __fmul_rn(x0, s));
+}
+// Rotate 8 pairs held as packed BF16: a holds elements i..i+7, b elements
+// i+64..i+71; c[e], s[e] belong to pair e.  Results rounded once to BF16.
+__device__ __forceinline__ void rope_words8(uint4& a, uint4& b, const float (&c)[8], const float (&s)[8]) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+  uint32_t ra[4], rb[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float ya0, yb0, ya1, yb1;
+    rope_pair(bf16_lo_as_f32(wa[w]), bf16_lo_as_f32(wb[w]), c[2 * w], s[2 * w], ya0, yb0);
+    rope_pair(bf16_hi_as_f32(wa[w]), bf16_hi_as_f32(wb[w]), c[2 * w + 1], s[2 * w + 1], ya1, yb1);
+    ra[w] = pack_bf16x2(ya0, ya1);
+    rb[w] = pack_bf16x2(yb0, yb1);
+  }
+  a = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+  b = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
   uint32_t w;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(0.0f), "f"(x));

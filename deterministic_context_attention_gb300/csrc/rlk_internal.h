@@ -101,14 +101,18 @@ struct MergeParams {
   int32_t cu_k[kMaxSeqs + 1];
 };
 
-// RoPE pass over packed BF16 rows [T, heads, 128]; row i of sequence s sits
-// at position pos0[s] + i.
+// RoPE pass over packed BF16 rows [T, heads, 128] (and optionally a second
+// tensor [T, heads2, 128] of the same tokens); row i of sequence s sits at
+// position pos0[s] + i.
 struct RopeParams {
   const uint16_t* x;
   uint16_t* y;          // may equal x
+  const uint16_t* x2;   // optional second tensor of the same tokens (K beside Q), or null
+  uint16_t* y2;
   const float* table;   // [positions][cos 64, sin 64]
   int64_t rows;         // T * heads
-  int32_t heads, num_seqs;
+  int64_t rows2;        // T * heads2
+  int32_t heads, heads2, num_seqs, pad0;
   int32_t cu[kMaxSeqs + 1];
   int32_t pos0[kMaxSeqs];
 };

@@ -28,31 +28,12 @@ namespace {
 
 constexpr int kRopeThreads = 256;
 
-__device__ __forceinline__ float bf16_as_f32(uint32_t h) { return __uint_as_float(h << 16); }
-
 // Rotate the 8 pairs held in a (first half) and b (second half).
 __device__ __forceinline__ void rope8(uint4& a, uint4& b, const float4& c0, const float4& c1, const float4& s0,
                                       const float4& s1) {
   const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-  uint32_t ra[4], rb[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    float ya[2], yb[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = 2 * w + h;
-      const float x0 = bf16_as_f32(h ? (wa[w] >> 16) : (wa[w] & 0xFFFFu));
-      const float x1 = bf16_as_f32(h ? (wb[w] >> 16) : (wb[w] & 0xFFFFu));
-      ya[h] = __fmaf_rn(x0, c[e], -__fmul_rn(x1, s[e]));
-      yb[h] = __fmaf_rn(x1, c[e], __fmul_rn(x0, s[e]));
-    }
-    ra[w] = pack_bf16x2(ya[0], ya[1]);
-    rb[w] = pack_bf16x2(yb[0], yb[1]);
-  }
-  a = make_uint4(ra[0], ra[1], ra[2], ra[3]);
-  b = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+  rope_words8(a, b, c, s);
 }
 
 __global__ void __launch_bounds__(kRopeThreads) rlk_rope_kernel(const __grid_constant__ RopeParams p) {
@@ -61,12 +42,16 @@ __global__ void __launch_bounds__(kRopeThreads) rlk_rope_kernel(const __grid_con
   for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) s_cu[i] = p.cu[i];
   for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) s_pos0[i] = p.pos0[i];
   __syncthreads();
-  const int64_t units = p.rows * 8;
+  const int64_t units1 = p.rows * 8, units = units1 + p.rows2 * 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
-    const int64_t row = u >> 3;
-    const int j = static_cast<int>(u & 7);
-    const int tok = static_cast<int>(row / p.heads);
+    // units of the first tensor, then of the second
+    const bool second = u >= units1;
+    const int64_t uu = second ? u - units1 : u;
+    const int heads = second ? p.heads2 : p.heads;
+    const int64_t row = uu >> 3;
+    const int j = static_cast<int>(uu & 7);
+    const int tok = static_cast<int>(row / heads);
     // the sequence holding tok: the last s with cu[s] <= tok (empty
     // sequences share their start with the next one)
     int lo = 0, hi = p.num_seqs - 1;
@@ -76,13 +61,13 @@ __global__ void __launch_bounds__(kRopeThreads) rlk_rope_kernel(const __grid_con
       else hi = mid - 1;
     }
     const int pos = s_pos0[lo] + (tok - s_cu[lo]);
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + row * kHeadDim);
+    const uint4* xr = reinterpret_cast<const uint4*>((second ? p.x2 : p.x) + row * kHeadDim);
     uint4 a = xr[j], b = xr[8 + j];
     const float4* t = reinterpret_cast<const float4*>(p.table + static_cast<int64_t>(pos) * kHeadDim);
     const float4 c0 = __ldg(t + 2 * j), c1 = __ldg(t + 2 * j + 1);
     const float4 s0 = __ldg(t + 16 + 2 * j), s1 = __ldg(t + 16 + 2 * j + 1);
     rope8(a, b, c0, c1, s0, s1);
-    uint4* yr = reinterpret_cast<uint4*>(p.y + row * kHeadDim);
+    uint4* yr = reinterpret_cast<uint4*>((second ? p.y2 : p.y) + row * kHeadDim);
     yr[j] = a;
     yr[8 + j] = b;
   }
@@ -91,7 +76,7 @@ __global__ void __launch_bounds__(kRopeThreads) rlk_rope_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_rope(const RopeParams& p, int num_sms, cudaStream_t stream) {
-  const int64_t units = p.rows * 8;
+  const int64_t units = (p.rows + p.rows2) * 8;
   if (units == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((units + kRopeThreads - 1) / kRopeThreads, static_cast<int64_t>(num_sms) * 16);
   rlk_rope_kernel<<<static_cast<int>(blocks), kRopeThreads, 0, stream>>>(p);

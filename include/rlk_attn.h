@@ -195,6 +195,24 @@ rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const 
                             rlk_stream_t stream);
 
 /*
+ * rlk_attn_prefill with the queries' RoPE applied inside the prefill kernel:
+ * q is the PRE-RoPE query; each query row is rotated at its absolute
+ * position kv_len - q_len + i (the sequence's token index) right after its
+ * tile lands in shared memory, in the FP32 form of rlk_attn_rope, so the
+ * result is bit-identical to rlk_attn_rope on q followed by
+ * rlk_attn_prefill.  k is post-RoPE, as stored in a KV cache.
+ *   rope_table: device FP32 [rope_max_pos][128] from rlk_attn_rope_table;
+ *   every sequence with queries needs kv_len <= rope_max_pos.
+ * Other arguments and outputs as in rlk_attn_prefill.
+ * [P1] Scope: optional RoPE composition before Attention (CP attention still
+ * consumes post-RoPE Q/K); [P3] PR stack: cache/position/RoPE identity.
+ */
+rlk_status rlk_attn_prefill_rope(const rlk_attn_params* params, const void* q, const void* k,
+                                 const void* v, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                 int32_t cp_rank, const float* rope_table, int32_t rope_max_pos,
+                                 float* out_f32, void* out_bf16, float* lse, rlk_stream_t stream);
+
+/*
  * Paged-KV decode: one query token per sequence, at the last position of its
  * context, against keys stored in pages of page_size tokens:
  *   q: device BF16 [num_seqs, Hq, 128]
@@ -249,6 +267,19 @@ rlk_status rlk_attn_rope_table(double theta, int32_t max_pos, float* table);
 rlk_status rlk_attn_rope(const rlk_attn_params* params, const void* x, void* y, int32_t num_heads,
                          const int32_t* cu_seqlens, const int32_t* pos_offset, const float* table,
                          int32_t max_pos, rlk_stream_t stream);
+
+/*
+ * rlk_attn_rope over the queries and keys of the same tokens in one launch:
+ * q [T, Hq, 128] -> q_out and k [T, Hkv, 128] -> k_out (BF16, device; an
+ * output may equal its input), Hq and Hkv from params, every token of
+ * sequence s at position pos_offset[s] + its index (pos_offset HOST or
+ * NULL).  Bit-identical to rlk_attn_rope on q and on k.
+ * [P1] Scope: RoPE composed before Attention; [P3] PR stack:
+ * cache/position/RoPE identity.
+ */
+rlk_status rlk_attn_rope_qk(const rlk_attn_params* params, const void* q, void* q_out, const void* k,
+                            void* k_out, const int32_t* cu_seqlens, const int32_t* pos_offset,
+                            const float* table, int32_t max_pos, rlk_stream_t stream);
 
 /*
  * rlk_attn_decode_paged with the query's RoPE applied inside the decode

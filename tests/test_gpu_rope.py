@@ -1,7 +1,9 @@
-"""GPU parity of RoPE: the streaming pass equals the oracle's canonical FP32
-RoPE bit for bit (BF16 results are byte-exact work), and the decode kernel's
-in-kernel query RoPE equals the pass followed by plain decode, which in turn
-equals the last row of the prefill over rotated inputs ("WS2 Attention PR5
+"""GPU parity of RoPE: the streaming pass (one tensor, or queries and keys in
+one launch) equals the oracle's canonical FP32 RoPE bit for bit (BF16
+results are byte-exact work); the prefill's and the decode kernel's
+in-kernel query RoPE equal the pass followed by the plain kernel, which in
+turn matches the oracle (prefill) and the last row of the prefill over
+rotated inputs (decode) ("WS2 Attention PR5
 Drift Benchmark", Scope: RoPE composed before Attention, Attention consuming
 post-RoPE Q/K; "[WS2][Attention] H100 validation and reproduction guide", PR
 stack: decode KV-cache replay and cache/position/RoPE identity)."""
@@ -153,3 +155,66 @@ def test_rope_cache_position_identity():
                             1.0 / np.sqrt(128), 46)
     d = run_decode_q(dec, q[-1:], rope_max_pos=ctx)
     assert_bitwise(d, (po[-1:], pb[-1:], pl[-1:]), "decode with RoPE vs prefill last row")
+
+
+def _prefill_rope(prob, q_raw, k_rot, cp=1, ranks=None):
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    from tests.gpu_helpers import params_of, to_np
+    qd, kd, vd = dv.bf16_to_device(q_raw), dv.bf16_to_device(k_rot), dv.bf16_to_device(prob.v)
+    max_pos = int(np.diff(prob.cu_k).max())
+    out, outb, lse = empty_outputs(torch, qd.shape[0], prob.hq)
+    p = params_of(prob, cp, 1)
+    for r in (ranks if ranks is not None else [-1]):
+        rlk.rlk_attn_prefill_rope(p, qd, kd, vd, prob.cu_q, prob.cu_k, r, table_dev(max_pos), max_pos, out, outb, lse)
+    rlk.rlk_attn_check_device_error()
+    return to_np(out, outb, lse)
+
+
+@pytest.mark.parametrize("lens,kv_extra,block", [([4096, 3000, 1024, 777], 0, 128), ([300, 1, 129], 37, 64)])
+def test_prefill_with_in_kernel_rope(lens, kv_extra, block):
+    # pre-RoPE queries rotated inside the prefill kernel at positions
+    # kv_len - q_len + i, post-RoPE keys: bit-identical to the RoPE pass on
+    # the queries followed by the plain prefill, and within the gates of the
+    # oracle's attention over the oracle-rotated queries.  The second case is
+    # a chunk of queries over a longer KV cache (positions offset by 37).
+    kv = [n + kv_extra for n in lens]
+    prob = synth.prefill_problem(lens=lens, hq=32, hkv=8, block=block, seed=81, kv_lens=kv)
+    q_raw = synth.normal_bf16(82, synth.T_Q, prob.q.shape)
+    k_rot = oracle.rope_f32(prob.k, positions(prob.cu_k, None), THETA)
+    offs = (np.diff(prob.cu_k) - np.diff(prob.cu_q)).astype(np.int32)
+    max_pos = int(np.diff(prob.cu_k).max())
+    q_rot = gpu_rope(q_raw, prob.cu_q, offs, max_pos)
+    np.testing.assert_array_equal(q_rot, oracle.rope_f32(q_raw, positions(prob.cu_q, offs), THETA))
+    rotated = synth.Prefill(q_rot, k_rot, prob.v, prob.cu_q, prob.cu_k, prob.hq, prob.hkv, prob.d, prob.scale,
+                            prob.block)
+    fused = _prefill_rope(prob, q_raw, k_rot)
+    assert_bitwise(fused, run_fused(rotated), "in-kernel RoPE vs pass + prefill")
+    assert_bitwise(_prefill_rope(prob, q_raw, k_rot, cp=2, ranks=[1, 0]), fused, "in-kernel RoPE, CP 2")
+    rows = np.sort(np.random.default_rng(83).choice(int(prob.cu_q[-1]), 120, replace=False))
+    ref_out, ref_lse = oracle.attention_f64(q_rot, k_rot, prob.v, prob.cu_q, prob.cu_k, prob.scale, rows=rows)
+    assert_forward_parity(*(x[rows] for x in fused), ref_out, ref_lse, "prefill with in-kernel RoPE")
+
+
+def test_rope_qk_single_launch_equals_two_passes():
+    # queries and keys of the same tokens in one launch, bit for bit the two
+    # single-tensor passes (ragged lengths, an empty sequence, offsets)
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    lens = [300, 0, 129, 1, 1000]
+    offs = np.array([0, 7, 100, 4000, 3], np.int32)
+    cu = synth.cu_seqlens(lens)
+    q = dv.bf16_to_device(synth.normal_bf16(91, synth.T_Q, (int(cu[-1]), 32, 128)))
+    k = dv.bf16_to_device(synth.normal_bf16(91, synth.T_K, (int(cu[-1]), 8, 128)))
+    table = table_dev(5001)
+    p = rlk.make_params(len(lens), 32, 8)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    rlk.rlk_attn_rope_qk(p, q, qo, k, ko, cu, offs, table, 5001)
+    q1, k1 = torch.empty_like(q), torch.empty_like(k)
+    rlk.rlk_attn_rope(p, q, q1, 32, cu, offs, table, 5001)
+    rlk.rlk_attn_rope(p, k, k1, 8, cu, offs, table, 5001)
+    rlk.rlk_attn_check_device_error()
+    assert torch.equal(qo.view(torch.int16), q1.view(torch.int16))
+    assert torch.equal(ko.view(torch.int16), k1.view(torch.int16))
