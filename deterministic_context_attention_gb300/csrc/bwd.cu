@@ -261,6 +261,10 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t kIdK = idesc_bf16(128, 64, false, false);   // both operands K-major, N = 64
     constexpr uint32_t kIdMN = idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major
     uint32_t res_it = 0, st_it = 0, s_it = 0, acc_it = 0;
+    // the whole warp walks the K-steps (warp-uniform descriptors) and the
+    // elected lane issues each MMA: a lone lane in a divergent branch issues
+    // them slower than the tensor core runs them
+    const uint32_t leader = elect_one_sync();
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
       const int item = round * g_ + ((round & 1) ? g_ - 1 - c_ : c_);  // snake order over the longest-first list
@@ -273,42 +277,43 @@ __global__ void __launch_bounds__(384, 1)
       ++res_it;
       // S^T|S and dP^T|dP of half c of step t (stream stage of step t)
       auto issue_sdp = [&](uint32_t st_addr, int c) {
-        if (lane == 0) {
-          const uint32_t boff = static_cast<uint32_t>(c) * 64 * 128;  // rows 64c.. of the streamed tiles
+        const uint32_t boff = static_cast<uint32_t>(c) * 64 * 128;  // rows 64c.. of the streamed tiles
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ss(tm_s + 64 * c, kdesc(res_addr, k), kdesc(st_addr + boff, k), kIdK, k > 0);
+        for (int k = 0; k < 8; ++k)
+          if (leader) umma_ss(tm_s + 64 * c, kdesc(res_addr, k), kdesc(st_addr + boff, k), kIdK, k > 0);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 8; ++k)
+          if (leader)
             umma_ss(tm_dp + 64 * c, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile + boff, k), kIdK, k > 0);
-          umma_commit(&bars[L::kSFull + c]);
-        }
+        if (leader) umma_commit(&bars[L::kSFull + c]);
         __syncwarp();
       };
       // K-steps 4c..4c+3 of the accumulators (first: the item's first product)
       auto issue_acc = [&](uint32_t st_addr, int c, bool first) {
-        if (lane == 0) {
-          const int k0 = 4 * c;
-          if (KIND == 0) {
-            // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: N = D, K = query rows)
+        const int k0 = 4 * c;
+        if (KIND == 0) {
+          // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: N = D, K = query rows)
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k)
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader)
               umma_ts(tm_acc0, tm_s + 16 * k, mndesc(st_addr + L::kTile, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc0, tm_s + 16 * k + 8, mndesc(st_addr + L::kTile, k), kIdMN, 1u);
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc0, tm_s + 16 * k + 8, mndesc(st_addr + L::kTile, k), kIdMN, 1u);
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k)
-              umma_ts(tm_acc1, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc1, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
-          } else {
-            // dQ += dS K_j  (B = K_j MN-major: N = D, K = keys)
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
+        } else {
+          // dQ += dS K_j  (B = K_j MN-major: N = D, K = keys)
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k)
-              umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
 #pragma unroll
-            for (int k = k0; k < k0 + 4; ++k) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
-          }
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
         }
         __syncwarp();
       };
@@ -322,12 +327,13 @@ __global__ void __launch_bounds__(384, 1)
         // for the whole backward); the accumulation order is the halves'.
         constexpr uint32_t kIdK128 = idesc_bf16(128, 128, false, false);
         auto issue_sdp128 = [&](uint32_t st_addr) {
-          if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK128, k > 0);
+          for (int k = 0; k < 8; ++k)
+            if (leader) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK128, k > 0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK128, k > 0);
+          for (int k = 0; k < 8; ++k)
+            if (leader) umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK128, k > 0);
+          if (leader) {
             umma_commit(&bars[L::kSFull]);
             umma_commit(&bars[L::kSFull + 1]);
           }
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           issue_acc(stage_addr(cur), 0, t == 0);
           issue_acc(stage_addr(cur), 1, false);
-          if (lane == 0) {
+          if (leader) {
             umma_commit(&bars[L::kStEmpty + cur % L::kStages]);
             if (!more) {
               umma_commit(&bars[L::kAccFull]);
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
           issue_acc(stage_addr(cur), c, t == 0 && c == 0);
-          if (c == 1 && lane == 0) {
+          if (c == 1 && leader) {
             umma_commit(&bars[L::kStEmpty + cur % L::kStages]);  // step t's stage is no longer read
             if (!more) {
               umma_commit(&bars[L::kAccFull]);
