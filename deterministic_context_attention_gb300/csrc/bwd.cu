@@ -25,6 +25,7 @@
 #include <cstdio>
 #include <cstring>
 #include <memory>
+#include <type_traits>
 #include <vector>
 
 #include "../../include/rlk_attn.h"
@@ -159,10 +160,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&bars[L::kSFull + h], 1);
-      mbar_init(&bars[L::kPFull + h], 128);  // the four warps of the half
+      mbar_init(&bars[L::kPFull + h], 256);  // the eight elementwise warps
     }
     mbar_init(&bars[L::kAccFull], 1);
-    mbar_init(&bars[L::kAccEmpty], 128);
+    mbar_init(&bars[L::kAccEmpty], 256);
     *abort = 0;
     fence_mbar_init();
   }
@@ -350,11 +351,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < nsteps; ++t) {
           const uint32_t cur = st_it, nxt = st_it + 1;
           const bool more = t + 1 < nsteps;
+          // the elementwise warps finish column half 0 before half 1
           bool w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
-          w = w && mbar_wait(&bars[L::kPFull + 1], s_it & 1, abort, p.err, 0x614);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
           issue_acc(stage_addr(cur), 0, t == 0);
+          w = mbar_wait(&bars[L::kPFull + 1], s_it & 1, abort, p.err, 0x614);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          tc_fence_after();
           issue_acc(stage_addr(cur), 1, false);
           if (leader) {
             umma_commit(&bars[L::kStEmpty + cur % L::kStages]);
@@ -421,13 +425,15 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ P / dS (+ epilogue)
-    // warps 4-7 take columns 0-63 of each step, warps 0-3 columns 64-127
-    // (P and dS are elementwise given the column or row statistics, so the
-    // halves need no exchange); warps 0-3 also write the item's results.
-    const int half = warp < 4 ? 1 : 0;
-    const int r = tid - (half ? 0 : 128);
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int cbase = 64 * half;  // first column of this half
+    // The tensor core hands over the two column halves of a step one after
+    // the other, and all eight warps work on each half in turn: warp w takes
+    // TMEM lane quadrant w mod 4 and the 32 columns 64 c + 32 (w / 4) .. of
+    // half c.  (Two warps per SMSP on every half: a single warp per SMSP is
+    // latency-bound on the arithmetic.)  The epilogue splits the same way:
+    // warps 0-3 write dV (dQ: columns 0-63), warps 4-7 dK (dQ: 64-127).
+    const int wq = warp & 3, wh = warp >> 2;
+    const int r = wq * 32 + lane;  // tile row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint32_t s_it = 0, acc_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int g_ = static_cast<int>(gridDim.x), c_ = static_cast<int>(blockIdx.x);
@@ -451,126 +457,150 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       const int key_pos = (KIND == 0) ? it.block * 128 + r : 0;
+      // dK/dV: the column statistics (lse, Delta of the step's query rows) of
+      // this warp's columns in both halves, loaded one step ahead
+      float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
+      auto load_stats = [&](int t) {
+        const int i = it.block + t / p.group;
+        const int h = it.head * p.group + t % p.group;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int qp = i * 128 + 64 * c + 32 * wh + lane;
+          const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
+          nl[c] = qp < len ? p.lse_t[idx] : 0.f;
+          nd[c] = qp < len ? p.delta_t[idx] : 0.f;
+        }
+      };
+      if (KIND == 0) load_stats(0);
       bool fail = false;
       for (int t = 0; t < nsteps; ++t) {
-        float* vb = vecs + ((s_it & 1) * 8 + warp) * 128;  // [lse2 64][Delta 64] of this half
+        float* vb = vecs + ((s_it & 1) * 8 + warp) * 128;  // [half][lse2 32, Delta 32] of this warp's columns
         int col0;  // position of column 0 of this step
         if (KIND == 0) {
-          const int i = it.block + t / p.group;
-          const int h = it.head * p.group + t % p.group;
-          col0 = i * 128;
-          // column statistics of this half: each warp stages its own copy
-          // (warp-local sync only)
+          col0 = (it.block + t / p.group) * 128;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = lane + 32 * u;
-            const int qp = col0 + cbase + col;
-            const int64_t idx = static_cast<int64_t>(h) * p.t_pad + tok0 + qp;
-            vb[col] = qp < len ? __fmul_rn(p.lse_t[idx], kLog2e) : 0.f;
-            vb[64 + col] = qp < len ? p.delta_t[idx] : 0.f;
+          for (int c = 0; c < 2; ++c) {  // each warp stages its own copy (warp-local sync only)
+            vb[64 * c + lane] = __fmul_rn(nl[c], kLog2e);
+            vb[64 * c + 32 + lane] = nd[c];
           }
           __syncwarp();
+          if (t + 1 < nsteps) load_stats(t + 1);
         } else {
           col0 = t * 128;
         }
-        bool w = mbar_wait(&bars[L::kSFull + half], s_it & 1, abort, p.err, 0x621);
-        if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-        tc_fence_after();
-        // every element of this warp's half is visible: no per-element mask
-        bool full;
-        if (KIND == 0)
-          full = __all_sync(0xffffffffu, key_pos < len && col0 + cbase + 63 < len && col0 + cbase >= key_pos);
-        else
-          full = __all_sync(0xffffffffu, row_ok && col0 + cbase + 63 <= row_pos);
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
-          const int colc = cbase + 32 * c;
+          bool w = mbar_wait(&bars[L::kSFull + c], s_it & 1, abort, p.err, 0x621);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          tc_fence_after();
+          const int colc = 64 * c + 32 * wh;  // first column of this warp's 32
+          // every element of this warp's columns is visible: no per-element mask
+          bool full;
+          if (KIND == 0)
+            full = __all_sync(0xffffffffu, key_pos < len && col0 + colc + 31 < len && col0 + colc >= key_pos);
+          else
+            full = __all_sync(0xffffffffu, row_ok && col0 + colc + 31 <= row_pos);
           uint32_t sr[32], dr[32];
           tmem_ld32(tm_s + lane_off + colc, sr);
           tmem_ld32(tm_dp + lane_off + colc, dr);
           tmem_ld_wait(sr);
           tmem_ld_wait(dr);
+          const float* vc = vb + 64 * c;
           uint32_t pw[32], dw[32];
+          // the masked form only on tiles that need it: a warp-uniform branch
+          // inside the unrolled loop would cut it into one short block per
+          // pair and expose the exp -> split latency chain of every pair
+          auto arith = [&](auto masked) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float4 l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
-            float4 d4 = make_float4(row_delta, row_delta, row_delta, row_delta);
-            if (KIND == 0) {
-              l4 = *reinterpret_cast<const float4*>(vb + 32 * c + e);
-              d4 = *reinterpret_cast<const float4*>(vb + 64 + 32 * c + e);
-            }
-            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            for (int e = 0; e < 32; e += 4) {
+              float4 l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
+              float4 d4 = make_float4(row_delta, row_delta, row_delta, row_delta);
+              if (KIND == 0) {
+                l4 = *reinterpret_cast<const float4*>(vc + e);
+                d4 = *reinterpret_cast<const float4*>(vc + 32 + e);
+              }
+              const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+              const float da[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              // p = 2^(s scale_log2 - lse log2 e), ds = p (dp - Delta); a masked
-              // element has p = 0, hence ds = 0
-              const float2 x = ffma2(make_float2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2,
-                                     make_float2(-la[u], -la[u + 1]));
-              float2 pp = make_float2(ex2_hw(x.x), ex2_hw(x.y));
-              if (!full) {
-                const int cA = colc + e + u, cB = cA + 1;
-                bool okA, okB;
-                if (KIND == 0) {
-                  okA = key_pos < len && col0 + cA < len && col0 + cA >= key_pos;
-                  okB = key_pos < len && col0 + cB < len && col0 + cB >= key_pos;
-                } else {
-                  okA = row_ok && col0 + cA <= row_pos;
-                  okB = row_ok && col0 + cB <= row_pos;
+              for (int u = 0; u < 4; u += 2) {
+                // p = 2^(s scale_log2 - lse log2 e), ds = p (dp - Delta); a
+                // masked element has p = 0, hence ds = 0
+                const float2 x = ffma2(make_float2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2,
+                                       make_float2(-la[u], -la[u + 1]));
+                float2 pp = make_float2(ex2_hw(x.x), ex2_hw(x.y));
+                if constexpr (decltype(masked)::value) {
+                  const int cA = colc + e + u, cB = cA + 1;
+                  bool okA, okB;
+                  if (KIND == 0) {
+                    okA = key_pos < len && col0 + cA < len && col0 + cA >= key_pos;
+                    okB = key_pos < len && col0 + cB < len && col0 + cB >= key_pos;
+                  } else {
+                    okA = row_ok && col0 + cA <= row_pos;
+                    okB = row_ok && col0 + cB <= row_pos;
+                  }
+                  pp.x = okA ? pp.x : 0.0f;
+                  pp.y = okB ? pp.y : 0.0f;
                 }
-                pp.x = okA ? pp.x : 0.0f;
-                pp.y = okB ? pp.y : 0.0f;
+                const float2 ds = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                                                  make_float2(da[u], da[u + 1])));
+                // a 16-column group of TMEM holds one K-step: its 8 hi words, then its 8 lo words
+                const int slot = ((e + u) >> 4) * 16 + (((e + u) & 15) >> 1);
+                uint32_t hi, lo;
+                if (KIND == 0) {  // dQ reads only dS
+                  split_pair2(pp, hi, lo);
+                  pw[slot] = hi;
+                  pw[slot + 8] = lo;
+                }
+                split_pair2(ds, hi, lo);
+                dw[slot] = hi;
+                dw[slot + 8] = lo;
               }
-              const float2 ds = fmul2(pp, fsub2(make_float2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
-                                                make_float2(da[u], da[u + 1])));
-              const int slot = ((e + u) >> 4) * 16 + (((e + u) & 15) >> 1);
-              uint32_t hi, lo;
-              if (KIND == 0) {  // dQ reads only dS
-                split_pair2(pp, hi, lo);
-                pw[slot] = hi;
-                pw[slot + 8] = lo;
-              }
-              split_pair2(ds, hi, lo);
-              dw[slot] = hi;
-              dw[slot + 8] = lo;
             }
-          }
+          };
+          if (full)
+            arith(std::false_type{});
+          else
+            arith(std::true_type{});
           if (KIND == 0) tmem_st32(tm_s + lane_off + colc, pw);
           tmem_st32(tm_dp + lane_off + colc, dw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[L::kPFull + c]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[L::kPFull + half]);
+        if (fail) break;
         ++s_it;
       }
       if (fail) break;
-      if (!half) continue;
       // ---------------------------------------------------------- epilogue
       bool w = mbar_wait(&bars[L::kAccFull], acc_it & 1, abort, p.err, 0x631);
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
-      const int nacc = (KIND == 0) ? 2 : 1;
-      for (int a = 0; a < nacc; ++a) {
+      {
         float* dst_base;
         bool ok;
         float mul;
+        uint32_t src;
         if (KIND == 0) {
+          // warps 0-3: dV (the raw sum), warps 4-7: dK (times the softmax scale)
           const int kp = it.block * 128 + r;
           ok = kp < len;
           const int64_t row = static_cast<int64_t>(tok0 + kp) * p.hkv + it.head;
-          dst_base = (a == 0 ? p.dv : p.dk) + row * kHeadDim;
-          mul = (a == 0) ? 1.0f : p.scale;
+          dst_base = (wh == 0 ? p.dv : p.dk) + row * kHeadDim;
+          mul = (wh == 0) ? 1.0f : p.scale;
+          src = (wh == 0 ? tm_acc0 : tm_acc1) + lane_off;
         } else {
+          // dQ (times the softmax scale): warps 0-3 columns 0-63, warps 4-7 64-127
           const int qp = it.block + r;
           ok = r < it.rows && qp < len;
           const int64_t row = static_cast<int64_t>(tok0 + qp) * p.hq + it.head;
-          dst_base = p.dq + row * kHeadDim;
+          dst_base = p.dq + row * kHeadDim + 64 * wh;
           mul = p.scale;
+          src = tm_acc0 + lane_off + 64 * wh;
         }
-        const uint32_t src = (a == 0 ? tm_acc0 : tm_acc1) + lane_off;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        const int nchunks = (KIND == 0) ? 4 : 2;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
           uint32_t x[32];
           tmem_ld32(src + 32 * c, x);
           tmem_ld_wait(x);
@@ -578,7 +608,6 @@ __global__ void __launch_bounds__(384, 1)
             float4* dst = reinterpret_cast<float4*>(dst_base + 32 * c);
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-              // dV is the raw sum; dK and dQ take the softmax scale here
               float v0 = __uint_as_float(x[e]), v1 = __uint_as_float(x[e + 1]);
               float v2 = __uint_as_float(x[e + 2]), v3 = __uint_as_float(x[e + 3]);
               if (mul != 1.0f) {
@@ -597,7 +626,6 @@ __global__ void __launch_bounds__(384, 1)
       ++acc_it;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
