@@ -29,6 +29,8 @@ cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t st
 cudaError_t launch_rope(const RopeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t stream);
+cudaError_t launch_decode_cooperative(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, int grid, cudaStream_t stream);
 rlk_status run_backward(const rlk_attn_params* prm, const void* q, const void* k, const void* v,
                         const float* out_f32, const void* dout, const float* lse,
                         const int32_t* cu, int32_t cp_rank, float* dq, float* dk, float* dv,
@@ -807,12 +809,30 @@ namespace {
 // to the smaller k (less state traffic).
 constexpr double kSplitItemStartup = 1.0;  // blocks' worth of start-up per item
 constexpr double kSplitFoldPerBlock = 0.08;  // fold chain step / KV block step
-int choose_split(const int32_t* seqlens, int num_seqs, int hkv, int B, int num_sms) {
+// The fold on chip: split_k producer items per (sequence, KV head) pair and
+// fold CTAs (one warp per (sequence, query head), 15 a CTA) in one
+// cooperative launch, the folds following their producers, so every CTA must
+// be resident at once: one CTA per SM.
+constexpr int kFoldChainsPerCta = 15;
+int fold_ctas(int num_seqs, int hq) { return (num_seqs * hq + kFoldChainsPerCta - 1) / kFoldChainsPerCta; }
+bool fold_on_chip(int num_seqs, int hkv, int hq, int k, int num_sms) {
+  const int64_t items = static_cast<int64_t>(num_seqs) * hkv * k;
+  return k >= 2 && items + fold_ctas(num_seqs, hq) <= num_sms && items <= rlk::kMaxTilesPerLaunch;
+}
+
+int choose_split(const int32_t* seqlens, int num_seqs, int hkv, int hq, int B, int num_sms) {
   std::vector<int> nbs(num_seqs);
   int nb_max = 0;
   for (int s = 0; s < num_seqs; ++s) {
     nbs[s] = (seqlens[s] + B - 1) / B;
     nb_max = std::max(nb_max, nbs[s]);
+  }
+  // few pairs: spread each over as many SMs as there are to share, with the
+  // fold on chip (hidden behind the producers, so no fold term to weigh)
+  {
+    const int free_sms = num_sms - fold_ctas(num_seqs, hq);
+    const int k = std::min({std::max(free_sms, 0) / std::max(num_seqs * hkv, 1), nb_max, 64});
+    if (fold_on_chip(num_seqs, hkv, hq, k, num_sms)) return k;
   }
   int best_k = 1;
   double best = 0.0;
@@ -851,7 +871,7 @@ int32_t rlk_attn_decode_auto_split(const rlk_attn_params* params, const int32_t*
   const int B = params->kv_block_size;
   for (int s = 0; s < params->num_seqs; ++s)
     if (seqlens[s] < 1) return -1;
-  return choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, num_sms);
+  return choose_split(seqlens, params->num_seqs, params->num_kv_heads, params->num_q_heads, B, num_sms);
 }
 
 namespace {
@@ -909,7 +929,7 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev))) return st;
   if (split_k == 0) {
-    split_k = choose_split(seqlens, params->num_seqs, params->num_kv_heads, B, dev->num_sms);
+    split_k = choose_split(seqlens, params->num_seqs, params->num_kv_heads, params->num_q_heads, B, dev->num_sms);
     // one range per sequence is the single-pass decode, which needs no state table
     if (split_k == 1)
       return decode_paged_impl(params, q, k_pool, v_pool, n_pages, page_size, page_table, max_pages, seqlens,
@@ -919,28 +939,53 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   std::vector<int32_t> block_base(params->num_seqs + 1, 0);
   for (int s = 0; s < params->num_seqs; ++s) block_base[s + 1] = block_base[s] + (seqlens[s] + B - 1) / B;
   const int64_t pairs = static_cast<int64_t>(block_base[params->num_seqs]) * params->num_q_heads;
+  bool on_chip = fold_on_chip(params->num_seqs, params->num_kv_heads, params->num_q_heads, split_k, dev->num_sms);
   std::vector<std::pair<int, rlk::FwdTile>> costed;
-  for (int s = 0; s < params->num_seqs; ++s) {
-    const int nb = (seqlens[s] + B - 1) / B;
-    for (int g = 0; g < params->num_kv_heads; ++g)
-      for (int r = 0; r < split_k; ++r) {
-        const int b0 = static_cast<int>(static_cast<int64_t>(r) * nb / split_k);
-        const int b1 = static_cast<int>(static_cast<int64_t>(r + 1) * nb / split_k);
-        if (b1 <= b0) continue;
-        rlk::FwdTile t;
-        std::memset(&t, 0, sizeof(t));
-        t.seq = s;
-        t.row_begin = g;
-        t.row_count = group;
-        t.block = b0;
-        t.slab_row_count = b1 - b0;
-        costed.push_back({b1 - b0, t});
-      }
+  if (on_chip) {
+    // item r of a pair takes its blocks r, r + k, r + 2k, ...: the pair's
+    // blocks are produced in ascending order across its k CTAs, and the fold
+    // warps of item 0 follow them
+    for (int s = 0; s < params->num_seqs; ++s) {
+      const int nb = (seqlens[s] + B - 1) / B;
+      for (int g = 0; g < params->num_kv_heads; ++g)
+        for (int r = 0; r < split_k && r < nb; ++r) {
+          rlk::FwdTile t;
+          std::memset(&t, 0, sizeof(t));
+          t.seq = s;
+          t.row_begin = g;
+          t.row_count = group;
+          t.block = r;
+          t.slab_row_count = (nb - r + split_k - 1) / split_k;
+          costed.push_back({t.slab_row_count, t});
+        }
+    }
   }
-  std::stable_sort(costed.begin(), costed.end(),
-                   [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
-                     return a.first > b.first;
-                   });
+  // contiguous ranges (the second kernel folds), longest first
+  auto contiguous_items = [&]() {
+    costed.clear();
+    for (int s = 0; s < params->num_seqs; ++s) {
+      const int nb = (seqlens[s] + B - 1) / B;
+      for (int g = 0; g < params->num_kv_heads; ++g)
+        for (int r = 0; r < split_k; ++r) {
+          const int b0 = static_cast<int>(static_cast<int64_t>(r) * nb / split_k);
+          const int b1 = static_cast<int>(static_cast<int64_t>(r + 1) * nb / split_k);
+          if (b1 <= b0) continue;
+          rlk::FwdTile t;
+          std::memset(&t, 0, sizeof(t));
+          t.seq = s;
+          t.row_begin = g;
+          t.row_count = group;
+          t.block = b0;
+          t.slab_row_count = b1 - b0;
+          costed.push_back({b1 - b0, t});
+        }
+    }
+    std::stable_sort(costed.begin(), costed.end(),
+                     [](const std::pair<int, rlk::FwdTile>& a, const std::pair<int, rlk::FwdTile>& b) {
+                       return a.first > b.first;
+                     });
+  };
+  if (!on_chip) contiguous_items();
   CUtensorMap mq, mk, mv;
   // one query head per TMA box: the kernel places each head in its own operand row
   if ((st = make_map(&mq, q, params->num_q_heads, params->num_seqs, 1, 1))) return st;
@@ -961,6 +1006,32 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   fp->max_pages = max_pages;
   fp->page_size = page_size;
   fp->n_pages = n_pages;
+  if (on_chip) {
+    // the fold warps take a state as landed once it differs from the fill
+    const size_t state_bytes = static_cast<size_t>(pairs) * (rlk::kHeadDim + 1) * 4;
+    fp->split_stride = split_k;
+    fp->fold_seqs = params->num_seqs;
+    fp->out_f32 = out_f32;
+    fp->out_bf16 = static_cast<uint16_t*>(out_bf16);
+    fp->lse = lse;
+    for (size_t i = 0; i < costed.size(); ++i) fp->tiles[i] = costed[i].second;
+    fp->num_tiles = static_cast<int32_t>(costed.size());
+    fp->num_items = fp->num_tiles;
+    static_assert(rlk::kUnwritten == 0xFFFFFFFFu, "the table fill is all-ones bytes");
+    cudaError_t e = cudaMemsetAsync(workspace, 0xFF, state_bytes, stream);
+    const int grid = fp->num_items + fold_ctas(params->num_seqs, params->num_q_heads);
+    if (e == cudaSuccess) e = rlk::launch_decode_cooperative(*fp, mq, mk, mv, grid, stream);
+    if (e == cudaSuccess) return ok();
+    if (e != cudaErrorCooperativeLaunchTooLarge)
+      return fail(RLK_ERR_CUDA, "split decode launch: %s", cudaGetErrorString(e));
+    // fewer SMs free than the device has (shared or partitioned): the same
+    // split in contiguous ranges, folded by the second kernel
+    (void)cudaGetLastError();
+    on_chip = false;
+    fp->split_stride = 0;
+    fp->fold_seqs = 0;
+    contiguous_items();
+  }
   for (size_t t0 = 0; t0 < costed.size(); t0 += rlk::kMaxTilesPerLaunch) {
     const size_t n = std::min(costed.size() - t0, static_cast<size_t>(rlk::kMaxTilesPerLaunch));
     for (size_t i = 0; i < n; ++i) fp->tiles[i] = costed[t0 + i].second;

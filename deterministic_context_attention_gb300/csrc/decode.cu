@@ -26,6 +26,9 @@
 //   warp  12    TMA producer of the group's query rows and the K pages
 //   warp  13    TMA producer of the V pages
 //   warp  14    TMEM allocator and MMA issuer
+// Split decode with the fold on chip adds CTAs past the work items, on SMs
+// the producers leave free, whose warps fold one (sequence, KV head, query
+// head) each as the producers write the block states.
 // TMEM (128 columns): S^T ring [0,64), O^T ring [64,128), 16 columns a slot.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -78,6 +81,7 @@ struct DecLayout {
   static constexpr int kAlloc = kTotal + 1024;
 };
 static_assert(DecLayout::kAlloc <= 232448, "decode shared memory");
+static_assert(DecLayout::kPageWin == 1 << 9, "the producers index the page window with shifts by 9");
 static_assert(DecLayout::kKOff % 1024 == 0 && DecLayout::kVOff % 1024 == 0 && DecLayout::kPOff % 1024 == 0,
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 
@@ -98,12 +102,14 @@ __device__ __forceinline__ int dec_snake_item(int round) {
 __device__ __forceinline__ float bf16_bits_as_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
 // One item: the query heads of KV head g of sequence seq against the global
-// blocks [b0, b0 + nb).  Plain decode: all of the sequence's blocks, folded on
-// chip.  Split decode (state_o set): a fixed range of them, whose block states
-// are written to the state table at pair (cu_q[seq] + b) * hq + head for the
-// merge to fold.
+// blocks b0, b0 + stride, ... (nb of them).  Plain decode: all of the
+// sequence's blocks (stride 1), folded on chip.  Split decode (state_o set):
+// a fixed range of them (stride 1), or with the fold on chip the blocks
+// b = r (mod split_stride) of item r; their block states are written to the
+// state table at pair (cu_q[seq] + b) * hq + head, for the merge kernel or
+// the fold CTAs to fold.
 struct DecItem {
-  int seq, g, kv_len, b0, nb;
+  int seq, g, kv_len, b0, nb, stride;
 };
 __device__ __forceinline__ DecItem dec_item(const FwdParams& p, int item) {
   const FwdTile& t = p.tiles[item];
@@ -111,9 +117,13 @@ __device__ __forceinline__ DecItem dec_item(const FwdParams& p, int item) {
   d.seq = t.seq;
   d.g = t.row_begin;
   d.kv_len = p.cu_k[t.seq];
+  d.stride = 1;
   if (p.state_o) {
     d.b0 = t.block;
     d.nb = t.slab_row_count;
+    if (p.split_stride > 0) {
+      d.stride = p.split_stride;
+    }
   } else {
     d.b0 = 0;
     d.nb = (d.kv_len + DecLayout::B - 1) / DecLayout::B;
@@ -128,9 +138,113 @@ __device__ __forceinline__ float warp_max(float v) {
   return m;
 }
 
+// Split decode with the fold on chip, the fold side: one warp folds query
+// head q of the pair (seq, g) over the pair's block states in ascending block
+// order as the producer CTAs write them -- the fold the correction role
+// applies in the single pass, operation for operation, so the result is the
+// same bit for bit.  Lane l folds head dimensions 4 l .. 4 l + 3 and every
+// lane runs the head's lse chain (the same inputs, so no lane waits on
+// another).
+//
+// C blocks at a time, the next chunk's reads in flight while the current one
+// folds.  The table holds the all-ones NaN until a state lands (arithmetic
+// never produces that pattern, and a 32-bit store lands whole, so a value
+// that differs from it is the final one).  Reads are weak first (they overlap
+// one another); values still unwritten, or stale, are read again with strong
+// (device-scope relaxed) loads, which the memory model guarantees to see
+// other SMs' stores eventually (a thread's strong loads complete one after
+// another).  Returns false on a timeout (reported) or an abort.
+__device__ __noinline__ bool fold_chain_on_chip(const FwdParams& p, int seq, int g, int q, int lane,
+                                                volatile int* abort) {
+  constexpr int C = 8;
+  const int G = p.group;
+  const int nbp = (p.cu_k[seq] + DecLayout::B - 1) / DecLayout::B;
+  const int64_t base = p.cu_q[seq];
+  // lane i: the lse of block c0 + i; every lane: dimensions 4 lane .. of the
+  // chunk's blocks (past the chunk: its last block, a valid value)
+  auto lse_src = [&](int c0, int nc) { return p.state_lse + (base + c0 + min(lane, nc - 1)) * p.hq + g * G + q; };
+  auto o_src = [&](int c0, int nc, int i) {
+    return p.state_o + ((base + c0 + min(i, nc - 1)) * p.hq + g * G + q) * kHeadDim + 4 * lane;
+  };
+  auto issue = [&](int c0, float& lsl, float4 (&v)[C]) {
+    const int nc = min(C, nbp - c0);
+    lsl = ld_l2_weak(lse_src(c0, nc));
+#pragma unroll
+    for (int i = 0; i < C; ++i) v[i] = ld_l2_weak4(o_src(c0, nc, i));
+  };
+  auto unwritten4 = [](const float4& a) {
+    return __float_as_uint(a.x) == kUnwritten || __float_as_uint(a.y) == kUnwritten ||
+           __float_as_uint(a.z) == kUnwritten || __float_as_uint(a.w) == kUnwritten;
+  };
+  // until every value of the chunk has landed: strong re-reads of what is missing
+  auto settle = [&](int c0, float& lsl, float4 (&v)[C]) -> bool {
+    const int nc = min(C, nbp - c0);
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      uint32_t miss = static_cast<uint32_t>(__float_as_uint(lsl) == kUnwritten);
+#pragma unroll
+      for (int i = 0; i < C; ++i) miss |= static_cast<uint32_t>(unwritten4(v[i]));
+      if (__all_sync(0xffffffffu, miss == 0)) return true;
+      const bool late = __shfl_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitTimeoutNs, 0);
+      if (late || *abort) {
+        if (late && lane == 0) {
+          *abort = 1;
+          report_error(p.err, kErrDeviceTimeout, 0x901);
+        }
+        return false;
+      }
+      if (__float_as_uint(lsl) == kUnwritten) lsl = ld_l2_poll(lse_src(c0, nc));
+#pragma unroll
+      for (int i = 0; i < C; ++i)
+        if (unwritten4(v[i])) v[i] = ld_l2_poll4(o_src(c0, nc, i));
+    }
+  };
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Lrun = -INFINITY;
+  float lsl, lsn = 0.f;
+  float4 v[C], vn[C];
+  issue(0, lsl, v);
+  for (int c0 = 0; c0 < nbp; c0 += C) {
+    const int nc = min(C, nbp - c0);
+    if (!settle(c0, lsl, v)) return false;
+    if (c0 + C < nbp) issue(c0 + C, lsn, vn);  // lands while this chunk folds
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      if (i < nc) {
+        const float lb = __shfl_sync(0xffffffffu, lsl, i);
+        if (c0 + i == 0) {
+          O = v[i];
+          Lrun = lb;
+        } else {
+          float Lp, al, be;
+          fold_coeffs(Lrun, lb, Lp, al, be);
+          O.x = __fmaf_rn(v[i].x, be, __fmul_rn(O.x, al));
+          O.y = __fmaf_rn(v[i].y, be, __fmul_rn(O.y, al));
+          O.z = __fmaf_rn(v[i].z, be, __fmul_rn(O.z, al));
+          O.w = __fmaf_rn(v[i].w, be, __fmul_rn(O.w, al));
+          Lrun = Lp;
+        }
+      }
+    }
+    lsl = lsn;
+#pragma unroll
+    for (int i = 0; i < C; ++i) v[i] = vn[i];
+  }
+  const int64_t row = static_cast<int64_t>(seq) * p.hq + g * G + q;
+  if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + row * kHeadDim + 4 * lane) = O;
+  if (p.out_bf16) {
+    const uint32_t w0 = pack_bf16x2(O.x, O.y), w1 = pack_bf16x2(O.z, O.w);
+    *reinterpret_cast<uint2*>(p.out_bf16 + row * kHeadDim + 4 * lane) = make_uint2(w0, w1);
+  }
+  if (lane == 0 && p.lse) p.lse[row] = Lrun;
+  return true;
+}
+
 // MG: the group's query heads rounded up to 1, 2, 4 or 8 (heads at or past
 // the group size are skipped at run time).
-template <int MG>
+// FOLD: the instance the split decode with the fold on chip launches (its
+// CTAs past the items fold); the others never carry the fold code.
+template <int MG, bool FOLD>
 __global__ void __launch_bounds__(kDThreads, 1)
     rlk_decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -201,7 +315,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
   uint8_t* v_base = smem + L::kVOff;
   uint8_t* p_base = smem + L::kPOff;
 
-  if (warp == 12 || warp == 13) {
+  if (FOLD && static_cast<int>(blockIdx.x) >= p.num_items) {
+    // ------------------------------------------------------------ fold CTA
+    // split decode with the fold on chip: the CTAs past the items, on SMs
+    // the producers leave free, fold one (sequence, KV head, query head)
+    // chain a warp, in (sequence, KV head, query head) order
+    const int chain = (static_cast<int>(blockIdx.x) - p.num_items) * (kDThreads / 32) + warp;
+    const int per_seq = p.hkv * G;
+    if (p.split_stride > 0 && chain < p.fold_seqs * per_seq) {
+      const int seq = chain / per_seq, g = (chain % per_seq) / G, q = chain % G;
+      fold_chain_on_chip(p, seq, g, q, lane, abort);
+    }
+  } else if (warp == 12 || warp == 13) {
     // ------------------------------------------------------------ producers
     // warp 12 loads the query rows and K, warp 13 V, so neither ring waits
     // on the other's free slots
@@ -240,21 +365,24 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const int seq_pages = (kv_len + ps - 1) / ps;
       const int32_t* prow = p.page_table + static_cast<int64_t>(seq) * p.max_pages;
       int cached = -1;  // a new sequence's page ids
+      const int lg = 31 - __clz(B / ps);  // log2 of the pages per block
       bool fail = false;
       for (int j = 0; j < nb; ++j) {
-        const int b = di.b0 + j;  // global block
+        const int b = di.b0 + j * di.stride;  // global block
         const uint32_t stage = it_n % S;
         bool ok = mbar_wait(empty_b + stage, ((it_n / S) & 1) ^ 1, abort, p.err, is_v ? 0x503 : 0x502);
         if (!__all_sync(0xffffffffu, ok)) { fail = true; break; }
         uint8_t* dst = ring + stage * L::kKVBytes;
         const int n_tok = min(B, kv_len - b * B);
         const int n_pg = (n_tok + ps - 1) / ps;
-        const int pg0 = b * (B / ps);  // B / ps divides the window
-        const int win = pg0 / L::kPageWin;
+        // the window holds the pages of 2^(9 - lg) consecutive blocks of the
+        // item (a block's 2^lg pages: page_size is a power of two dividing B)
+        const int win = j >> (9 - lg);
         if (cached != win) {
           for (int i = lane; i < L::kPageWin; i += 32) {
-            const int gp = win * L::kPageWin + i;
-            wc[i] = gp < seq_pages ? prow[gp] : -1;
+            const int jj = (win << (9 - lg)) + (i >> lg);  // block of the item
+            const int gp = ((di.b0 + jj * di.stride) << lg) + (i & ((1 << lg) - 1));
+            wc[i] = (jj < nb && gp < seq_pages) ? prow[gp] : -1;
           }
           __syncwarp();
           cached = win;
@@ -262,7 +390,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(full_b + stage, n_pg * ps * 256);
         __syncwarp();
         if (lane < n_pg) {
-          int32_t pe = wc[(pg0 + lane) % L::kPageWin];
+          int32_t pe = wc[((j & ((1 << (9 - lg)) - 1)) << lg) + lane];
           if (pe < 0 || pe >= p.n_pages) {
             report_error(p.err, kErrBadPage, 0x504);
             pe = p.n_pages;  // out of range: the copy reads the zero fill
@@ -333,7 +461,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         uint8_t* vd = v_base + vstage * L::kKVBytes;
         // V rows past the context may hold stale or non-finite data; P is
         // exactly 0 there, so zero them (0 * NaN = NaN)
-        const int valid = min(B, kv_len - (di.b0 + j) * B);
+        const int valid = min(B, kv_len - (di.b0 + j * di.stride) * B);
         if (valid < B) {
           const int nrow = B - valid;
           for (int i = lane; i < nrow * 16; i += 32) {
@@ -401,7 +529,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         tmem_ld_wait(raw);
         tc_fence_before();
         mbar_arrive(&bars[L::kSEmpty + slot]);
-        const bool vis = (di.b0 + j) * B + t < kv_len;
+        const bool vis = (di.b0 + j * di.stride) * B + t < kv_len;
         const int rb = static_cast<int>(sy_it & 1);
         const uint32_t sy_par = (sy_it >> 1) & 1;
         // block maximum of every query head over the visible keys (exact)
@@ -549,7 +677,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
         mbar_arrive(&bars[L::kOEmpty + oslot]);
         // o_b = PV * (1/l); O = fma(o_b, beta, O * alpha), or (split) the
         // block state written out
-        const int64_t pair_b = static_cast<int64_t>(p.cu_q[seq] + di.b0 + j) * p.hq + g * G;
+        const int64_t blk = p.cu_q[seq] + di.b0 + j * di.stride;  // state-table block
+        const int64_t pair_b = blk * p.hq + g * G;
 #pragma unroll
         for (int q = 0; q < MG; ++q) {
           const float rq = __shfl_sync(0xffffffffu, rc, q);
@@ -601,8 +730,20 @@ __global__ void __launch_bounds__(kDThreads, 1)
 template <int MG>
 cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, cudaStream_t stream) {
-  rlk_decode_kernel<MG><<<grid, kDThreads, DecLayout::kAlloc, stream>>>(p, tq, tk, tv);
+  rlk_decode_kernel<MG, false><<<grid, kDThreads, DecLayout::kAlloc, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
+}
+
+// The split decode with the fold on chip: its fold warps wait for states
+// that other CTAs of the launch publish, so every CTA must be resident at
+// once -- a cooperative launch guarantees it (or fails).
+template <int MG>
+cudaError_t launch_decode_coop_t(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  void* args[] = {const_cast<FwdParams*>(&p), const_cast<CUtensorMap*>(&tq), const_cast<CUtensorMap*>(&tk),
+                  const_cast<CUtensorMap*>(&tv)};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&rlk_decode_kernel<MG, true>), dim3(grid),
+                                     dim3(kDThreads), args, DecLayout::kAlloc, stream);
 }
 
 // Split decode, second step: the canonical fold of one (sequence, query head)
@@ -714,16 +855,21 @@ bool decode_transposed_supported(const FwdParams& p) {
          DecLayout::kPageWin % (DecLayout::B / p.page_size) == 0;
 }
 
+template <int MG>
+cudaError_t configure_decode_mg() {
+  cudaError_t e = cudaFuncSetAttribute(rlk_decode_kernel<MG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DecLayout::kAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(rlk_decode_kernel<MG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecLayout::kAlloc);
+}
+
 cudaError_t configure_decode_kernels() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
-    return e;
-  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
-    return e;
-  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
-    return e;
-  if ((e = cudaFuncSetAttribute(rlk_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout::kAlloc)))
-    return e;
+  if ((e = configure_decode_mg<1>())) return e;
+  if ((e = configure_decode_mg<2>())) return e;
+  if ((e = configure_decode_mg<4>())) return e;
+  if ((e = configure_decode_mg<8>())) return e;
   return cudaFuncSetAttribute(rlk_decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDmSmem);
 }
 
@@ -744,6 +890,14 @@ cudaError_t launch_decode_merge(const FwdParams& p, int num_sms, cudaStream_t st
   const int64_t blocks = std::min<int64_t>(std::max<int64_t>(pairs, 1), static_cast<int64_t>(num_sms) * 3);
   rlk_decode_merge_kernel<<<static_cast<int>(blocks), kDmThreads, kDmSmem, stream>>>(f);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_cooperative(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, int grid, cudaStream_t stream) {
+  if (p.group <= 1) return launch_decode_coop_t<1>(p, tq, tk, tv, grid, stream);
+  if (p.group <= 2) return launch_decode_coop_t<2>(p, tq, tk, tv, grid, stream);
+  if (p.group <= 4) return launch_decode_coop_t<4>(p, tq, tk, tv, grid, stream);
+  return launch_decode_coop_t<8>(p, tq, tk, tv, grid, stream);
 }
 
 cudaError_t launch_decode(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

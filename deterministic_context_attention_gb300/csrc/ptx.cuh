@@ -359,4 +359,33 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// A load for polling values other CTAs of the same launch are writing: a
+// strong (relaxed, device-scope) load, so the memory model guarantees it
+// eventually observes another SM's store (a weak load may keep returning a
+// stale copy), issued every time it is reached.
+__device__ __forceinline__ float ld_l2_poll(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+// The weak forms: L2 (never L1, which other SMs' stores do not update), and
+// overlapping one another; a value they return is current or older.
+__device__ __forceinline__ float ld_l2_weak(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_l2_weak4(const float* p) {  // p 16-byte aligned
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_l2_poll4(const float* p) {  // p 16-byte aligned
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
 }  // namespace rlk

@@ -15,6 +15,7 @@ constexpr int kTileRows = 128;          // MMA M: query rows per tile
 constexpr int kDecodeMaxGroup = 8;     // query heads per KV head the transposed decode kernel takes
 constexpr int64_t kNoAllocIndexEntries = 65536;  // no-alloc merge scratch: (sequence, block) index entries
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded mbarrier waits: 1 s
+constexpr uint32_t kUnwritten = 0xFFFFFFFFu;  // state-table fill of the on-chip fold (a NaN arithmetic never makes)
 
 // device error word bits
 constexpr unsigned kErrDeviceTimeout = 1u;
@@ -64,7 +65,13 @@ struct FwdParams {
   float* state_lse;
   // decode
   const int32_t* page_table;
-  int32_t max_pages, page_size, n_pages, pad0;
+  int32_t max_pages, page_size, n_pages;
+  // split decode with the fold on chip: item r of a (sequence, KV head) takes
+  // the blocks b = r, r + split_stride, ... (0: contiguous ranges, or the
+  // whole sequence); the CTAs past the items fold the states of fold_seqs
+  // sequences as the producers write them into the table, which holds
+  // kUnwritten before
+  int32_t split_stride, fold_seqs;
   // transposed decode: RoPE table [positions][cos 64, sin 64] (FP32); when
   // set, the query rows are rotated at position kv_len - 1 after they land
   const float* rope_table;

@@ -302,23 +302,32 @@ rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void*
                                       float* lse, rlk_stream_t stream);
 
 /*
- * Paged-KV decode with each sequence's KV blocks split into split_k fixed,
- * contiguous ranges of global blocks (range r: blocks floor(r*nb/k) up to
- * floor((r+1)*nb/k), nb = the sequence's blocks) that different SMs process:
- * every range writes the block states (o_b, lse_b) of its blocks to a state
- * table in the workspace, and a second kernel folds each (sequence, query
- * head) in ascending block order with the canonical fold.  The arithmetic is
- * the single-pass decode's step for step, so the result equals
- * rlk_attn_decode_paged (and the last row of the equivalent prefill) bit for
- * bit whatever split_k; it spreads few long sequences over all SMs.
+ * Paged-KV decode with each (sequence, KV head)'s KV blocks split over
+ * split_k fixed work items that different SMs process.  Every item writes
+ * the block states (o_b, lse_b) of its blocks to a state table in the
+ * workspace, and each (sequence, query head) is folded in ascending block
+ * order with the canonical fold.  Two schedules, with the same bits:
+ *   - when the num_seqs * num_kv_heads * split_k items and the fold CTAs
+ *     (one warp per (sequence, query head), 15 a CTA) fit on the device at
+ *     once (one CTA per SM), item r takes the blocks b = r (mod split_k) and
+ *     the whole call is one cooperative launch whose fold CTAs, on SMs the
+ *     items leave free, fold the states as the items write them (the fold
+ *     hides behind the producers);
+ *   - otherwise item r takes the contiguous blocks floor(r*nb/k) up to
+ *     floor((r+1)*nb/k) (nb = the sequence's blocks) and a second kernel
+ *     folds the table.
+ * The arithmetic is the single-pass decode's step for step, so the result
+ * equals rlk_attn_decode_paged (and the last row of the equivalent prefill)
+ * bit for bit whatever split_k; it spreads few long sequences over all SMs.
  *   Arguments as rlk_attn_decode_paged, plus
- *   split_k: 1 .. 64 ranges per (sequence, KV head), or 0 to let the
- *     library pick k from the context lengths and the SM count (a model of
- *     the busiest SM's blocks plus the fold; k = 1 runs the single-pass
- *     decode) -- the result is the same for every k;
+ *   split_k: 1 .. 64 items per (sequence, KV head), or 0 to let the library
+ *     pick k from the context lengths and the SM count (few pairs: the
+ *     largest k whose items fit on the device at once, with the fold on
+ *     chip; otherwise a model of the busiest SM's blocks plus the fold; k = 1
+ *     runs the single-pass decode) -- the result is the same for every k;
  *   workspace: device, >= rlk_attn_workspace_size(params,
- *     RLK_OP_DECODE_SPLIT, NULL, seqlens) bytes (the state table:
- *     516 bytes per (sequence, block, query head)).
+ *     RLK_OP_DECODE_SPLIT, NULL, seqlens) bytes (the state table: 516 bytes
+ *     per (sequence, block, query head)).
  * Needs kv_block_size 128 and at most 8 query heads per KV head
  * (RLK_ERR_UNSUPPORTED otherwise).
  * [P3] PR stack: decode KV-cache replay; Status: fixed global_block_index

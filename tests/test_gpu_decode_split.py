@@ -54,3 +54,15 @@ def test_split_decode_parity(dec):
 def test_split_decode_group_sizes(hq, hkv):
     d = synth.paged_decode_problem(ctx=[5, 300, 1500], hq=hq, hkv=hkv, seed=52)
     assert_bitwise(run_split(d, 5), run_decode(d), f"hq{hq}/hkv{hkv}")
+
+
+def test_split_decode_fold_on_chip_long():
+    # 4 x 32768 tokens (the long-context split workload): 32 (sequence, KV
+    # head) pairs, so k = 4 and the library's own choice run as one
+    # cooperative launch with the fold on chip, k = 8 as contiguous ranges
+    # and the fold kernel; every call, repeated, equals the single pass bit
+    # for bit
+    d = synth.paged_decode_problem(ctx=[32768] * 4, seed=53)
+    ref = run_decode(d)
+    for k in (4, 0, 4, 8):
+        assert_bitwise(run_split(d, k), ref, f"4 x 32768, split_k {k}")
