@@ -1022,10 +1022,11 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
     const int grid = fp->num_items + fold_ctas(params->num_seqs, params->num_q_heads);
     if (e == cudaSuccess) e = rlk::launch_decode_cooperative(*fp, mq, mk, mv, grid, stream);
     if (e == cudaSuccess) return ok();
-    if (e != cudaErrorCooperativeLaunchTooLarge)
+    if (e != cudaErrorCooperativeLaunchTooLarge && e != cudaErrorNotSupported)
       return fail(RLK_ERR_CUDA, "split decode launch: %s", cudaGetErrorString(e));
-    // fewer SMs free than the device has (shared or partitioned): the same
-    // split in contiguous ranges, folded by the second kernel
+    // fewer SMs free than the device has (shared or partitioned), or no
+    // cooperative launches: the same split in contiguous ranges, folded by
+    // the second kernel
     (void)cudaGetLastError();
     on_chip = false;
     fp->split_stride = 0;

@@ -189,13 +189,15 @@ def test_decode_auto_split_choice(lib):
     # host-only policy query: few long sequences spread over the SMs, a batch
     # that already fills them stays single-pass
     p4 = rlk.make_params(4)  # Hq 32 / Hkv 8: 32 (sequence, KV head) pairs
-    k = rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 152)
-    assert 4 <= k <= 27  # 32k items stay within one launch's 880-entry item list
+    # few pairs: the largest k whose items and fold CTAs (one warp per
+    # (sequence, query head), 15 a CTA) are resident at once, one per SM:
+    # 32 pairs x 4 + ceil(128 / 15) = 137 <= 152, 32 x 5 + 9 > 152
+    assert rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 152) == 4
     assert rlk.rlk_attn_decode_auto_split(p4, [128] * 4, 152) == 1  # one block each: nothing to split
     p64 = rlk.make_params(64)
     assert rlk.rlk_attn_decode_auto_split(p64, [32768] * 64, 152) == 1  # 512 pairs already cover 152 SMs
     p1 = rlk.make_params(1)
-    assert rlk.rlk_attn_decode_auto_split(p1, [131072], 152) > 8  # one very long sequence
+    assert rlk.rlk_attn_decode_auto_split(p1, [131072], 152) == 18  # 8 pairs x 18 + 3 fold CTAs = 147
     assert rlk.rlk_attn_decode_auto_split(p1, [131072], 1) == 1  # a single SM gains nothing from splitting
     assert rlk.rlk_attn_decode_auto_split(p4, [32768, 0, 5, 5], 152) == -1
     assert rlk.rlk_attn_decode_auto_split(p4, [32768] * 4, 0) == -1
