@@ -66,3 +66,11 @@ def test_split_decode_fold_on_chip_long():
     ref = run_decode(d)
     for k in (4, 0, 4, 8):
         assert_bitwise(run_split(d, k), ref, f"4 x 32768, split_k {k}")
+
+
+@pytest.mark.parametrize("hq,hkv,k", [(24, 8, 3), (40, 8, 2), (8, 8, 7)])
+def test_split_decode_fold_on_chip_group_shapes(hq, hkv, k):
+    # the on-chip fold with groups of 3, 5 and 1 query heads per KV head,
+    # partial last blocks and a one-block sequence (fewer items than k)
+    d = synth.paged_decode_problem(ctx=[1, 200, 1999, 4097], hq=hq, hkv=hkv, seed=54)
+    assert_bitwise(run_split(d, k), run_decode(d), f"hq{hq}/hkv{hkv} k {k}")
