@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     constexpr uint32_t kIdS = idesc_bf16(128, kDN, false, false);  // A = K (K-major), B = Q (K-major)
     constexpr uint32_t kIdO = idesc_bf16(128, kDN, true, false);   // A = V^T (dims contiguous), B = P^T
     const Desc qd = make_desc(smem_u32(q_tile), 16, 1024);
+    const uint32_t leader = elect_one_sync();
     uint32_t k_it = 0, v_it = 0, s_it = 0, o_it = 0, q_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
@@ -428,18 +429,24 @@ __global__ void __launch_bounds__(kDThreads, 1)
         w = w && mbar_wait(&bars[L::kSEmpty + slot], ((si / SS) & 1) ^ 1, abort, p.err, 0x603);
         if (!__all_sync(0xffffffffu, w)) return false;
         tc_fence_after();
-        if (lane == 0) {
+        {
+          // the whole warp walks the K-steps (warp-uniform descriptors) and
+          // the elected lane issues: a lone lane in a divergent branch issues
+          // these small MMAs far slower than the tensor core runs them
           const Desc kd = make_desc(smem_u32(k_base + stage * L::kKVBytes), 16, 1024);
           const uint32_t d = tm_s + slot * 16;
           // K-steps over head dimensions: 0-3 in the first 64-dim half, 4-7 in the second
-          mma_ss<0>(d, kd, 0, qd, 0, kIdS);
+          if (leader) mma_ss<0>(d, kd, 0, qd, 0, kIdS);
 #pragma unroll
           for (int s = 1; s < kHeadDim / 16; ++s)
-            mma_ss<1>(d, kd, (s >> 2) * (L::kKVHalf >> 4) + (s & 3) * 2, qd, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2,
-                      kIdS);
-          umma_commit(&bars[L::kSFull + slot]);
-          umma_commit(&bars[L::kKEmpty + stage]);
-          if (j + 1 == nb) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
+            if (leader)
+              mma_ss<1>(d, kd, (s >> 2) * (L::kKVHalf >> 4) + (s & 3) * 2, qd,
+                        (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdS);
+          if (leader) {
+            umma_commit(&bars[L::kSFull + slot]);
+            umma_commit(&bars[L::kKEmpty + stage]);
+            if (j + 1 == nb) umma_commit(&bars[L::kQEmpty]);  // Q no longer read
+          }
         }
         __syncwarp();
         return true;
@@ -474,23 +481,25 @@ __global__ void __launch_bounds__(kDThreads, 1)
           __syncwarp();
         }
         tc_fence_after();
-        if (lane == 0) {
+        {
           // O^T = V^T P_hi^T + V^T P_lo^T: K-step s covers keys 16s..16s+15
           // (V rows: 2048 B a step; P^T columns: 32 B a step within a half)
           const Desc vdd = make_desc(smem_u32(vd), L::kKVHalf, 1024);
           const Desc ph = make_desc(smem_u32(p_base + pslot * 2 * L::kTBytes), 16, 1024);
           const Desc pl = make_desc(smem_u32(p_base + pslot * 2 * L::kTBytes + L::kTBytes), 16, 1024);
           const uint32_t d = tm_o + oslot * 16;
-          mma_ss<0>(d, vdd, 0, ph, 0, kIdO);
+          if (leader) mma_ss<0>(d, vdd, 0, ph, 0, kIdO);
 #pragma unroll
           for (int s = 1; s < B / 16; ++s)
-            mma_ss<1>(d, vdd, s * 128, ph, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
+            if (leader) mma_ss<1>(d, vdd, s * 128, ph, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
 #pragma unroll
           for (int s = 0; s < B / 16; ++s)
-            mma_ss<1>(d, vdd, s * 128, pl, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
-          umma_commit(&bars[L::kOFull + oslot]);
-          umma_commit(&bars[L::kVEmpty + vstage]);
-          umma_commit(&bars[L::kPEmpty + pslot]);
+            if (leader) mma_ss<1>(d, vdd, s * 128, pl, (s >> 2) * (L::kTHalf >> 4) + (s & 3) * 2, kIdO);
+          if (leader) {
+            umma_commit(&bars[L::kOFull + oslot]);
+            umma_commit(&bars[L::kVEmpty + vstage]);
+            umma_commit(&bars[L::kPEmpty + pslot]);
+          }
         }
         __syncwarp();
       }
