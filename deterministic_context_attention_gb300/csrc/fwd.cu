@@ -136,7 +136,8 @@ __device__ __forceinline__ ItemInfo item_info(const FwdParams& p, int item) {
 
 // Item of this CTA in round k of the static schedule: CTAs take one item per
 // round from the longest-first list, in ascending CTA order on even rounds
-// and descending on odd ones, which evens out the per-CTA work.
+// and descending on odd ones, which evens out the per-CTA work.  A CTA's item
+// index grows with the round, so its loop ends at the first round without one.
 __device__ __forceinline__ int snake_item(int round) {
   const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   return round * g + ((round & 1) ? g - 1 - c : c);
@@ -429,10 +430,13 @@ __global__ void __launch_bounds__(512, 1)
       const Desc qd0 = make_desc(q_addr, 16, 1024);
       const uint32_t leader = elect_one_sync();
       uint32_t k_it = 0, v_it = 0, s_it = 0, pv_it = 0, q_it = 0;
-      for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
-        const int item = snake_item(round);
-        if (item >= p.num_items) continue;
-        const ItemInfo it = item_info<MODE>(p, item);
+      // the next item's descriptor (two levels of dependent global loads,
+      // ~700 cycles) is read while the current item runs, not between the
+      // last PV and the next item's first S
+      ItemInfo nxt;
+      if (snake_item(0) < p.num_items) nxt = item_info<MODE>(p, snake_item(0));
+      for (int round = 0; snake_item(round) < p.num_items; ++round) {
+        const ItemInfo it = nxt;
         // with RoPE in the prefill the softmax warps hand over the rotated tile
         bool ok = mbar_wait(&bars[ROPE ? L::kQRot : L::kQFull], q_it & 1, abort, p.err, 0x201);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -463,6 +467,7 @@ __global__ void __launch_bounds__(512, 1)
           return true;
         };
         if (!issue_s(0)) break;
+        if (snake_item(round + 1) < p.num_items) nxt = item_info<MODE>(p, snake_item(round + 1));
         bool fail = false;
         for (int j = 0; j < it.nb; ++j) {
           if (j + 1 < it.nb) {
@@ -615,10 +620,13 @@ __global__ void __launch_bounds__(512, 1)
     float O[kHeadDim];
 #pragma unroll
     for (int e = 0; e < kHeadDim; ++e) O[e] = 0.0f;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
-      const int item = snake_item(round);
-      if (item >= p.num_items) continue;
-      const ItemInfo it = item_info<MODE>(p, item);
+    // the next item's descriptor is read ahead: the epilogue already puts
+    // these warps behind the PV products at an item start
+    ItemInfo nxt;
+    if (snake_item(0) < p.num_items) nxt = item_info<MODE>(p, snake_item(0));
+    for (int round = 0; snake_item(round) < p.num_items; ++round) {
+      const ItemInfo it = nxt;
+      if (snake_item(round + 1) < p.num_items) nxt = item_info<MODE>(p, snake_item(round + 1));
       const bool valid = row_of_lane<MODE>(r) < it.row_count;
       const bool warp_rows = __any_sync(0xffffffffu, valid);
       float Lrun = -INFINITY;
