@@ -6,12 +6,15 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <memory>
 #include <mutex>
+#include <random>
 #include <string>
 #include <type_traits>
 #include <vector>
@@ -813,6 +816,29 @@ constexpr double kSplitFoldPerBlock = 0.08;  // fold chain step / KV block step
 // fold CTAs (one warp per (sequence, query head), 15 a CTA) in one
 // cooperative launch, the folds following their producers, so every CTA must
 // be resident at once: one CTA per SM.
+// split decode workspace: the state table (o_b then lse_b of every pair),
+// rounded to 256 bytes, then one 8-byte fill flag per (sequence, KV head,
+// item) for the on-chip fold
+size_t split_table_bytes(int64_t pairs) { return static_cast<size_t>((pairs * (rlk::kHeadDim + 1) * 4 + 255) / 256 * 256); }
+size_t split_flag_bytes(int num_seqs, int hkv) {
+  return static_cast<size_t>(num_seqs) * hkv * rlk::kMaxSplitK * sizeof(uint64_t);
+}
+
+// A value no earlier call of this process has used (an odd step walks all
+// 2^64 values before repeating), from a random start, so that a flag an
+// earlier call or another process left in a workspace does not hold it.
+uint64_t next_fill_nonce() {
+  static std::atomic<uint64_t> next{[] {
+    std::random_device rd;
+    return (static_cast<uint64_t>(rd()) << 32) ^ rd() ^
+           static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+  }()};
+  for (;;) {
+    const uint64_t v = next.fetch_add(0x9E3779B97F4A7C15ull);
+    if (v != 0 && v != ~0ull) return v;  // not the values a zero or all-ones fill leaves
+  }
+}
+
 constexpr int kFoldChainsPerCta = 15;
 int fold_ctas(int num_seqs, int hq) { return (num_seqs * hq + kFoldChainsPerCta - 1) / kFoldChainsPerCta; }
 bool fold_on_chip(int num_seqs, int hkv, int hq, int k, int num_sms) {
@@ -1007,8 +1033,20 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
   fp->page_size = page_size;
   fp->n_pages = n_pages;
   if (on_chip) {
-    // the fold warps take a state as landed once it differs from the fill
+    // the fold warps take a state as landed once it differs from the fill;
+    // each item fills its own slots and publishes a flag, except inside a
+    // graph capture, where a replay would find the flags of the previous
+    // replay already set: there a fill of the table precedes the launch
     const size_t state_bytes = static_cast<size_t>(pairs) * (rlk::kHeadDim + 1) * 4;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+      (void)cudaGetLastError();
+      cap = cudaStreamCaptureStatusActive;  // unknown: take the form that is safe in both
+    }
+    const bool self_fill = cap == cudaStreamCaptureStatusNone;
+    fp->fill_flag = self_fill ? reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + split_table_bytes(pairs))
+                              : nullptr;
+    fp->fill_nonce = self_fill ? next_fill_nonce() : 0;
     fp->split_stride = split_k;
     fp->fold_seqs = params->num_seqs;
     fp->out_f32 = out_f32;
@@ -1018,7 +1056,7 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
     fp->num_tiles = static_cast<int32_t>(costed.size());
     fp->num_items = fp->num_tiles;
     static_assert(rlk::kUnwritten == 0xFFFFFFFFu, "the table fill is all-ones bytes");
-    cudaError_t e = cudaMemsetAsync(workspace, 0xFF, state_bytes, stream);
+    cudaError_t e = self_fill ? cudaSuccess : cudaMemsetAsync(workspace, 0xFF, state_bytes, stream);
     const int grid = fp->num_items + fold_ctas(params->num_seqs, params->num_q_heads);
     if (e == cudaSuccess) e = rlk::launch_decode_cooperative(*fp, mq, mk, mv, grid, stream);
     if (e == cudaSuccess) return ok();
@@ -1031,6 +1069,7 @@ rlk_status decode_splitk_impl(const rlk_attn_params* params, const void* q, cons
     on_chip = false;
     fp->split_stride = 0;
     fp->fold_seqs = 0;
+    fp->fill_flag = nullptr;
     contiguous_items();
   }
   for (size_t t0 = 0; t0 < costed.size(); t0 += rlk::kMaxTilesPerLaunch) {
@@ -1086,7 +1125,7 @@ size_t rlk_attn_workspace_size(const rlk_attn_params* params, int32_t op, const 
       blocks += (cu_seqlens_k[s] + params->kv_block_size - 1) / params->kv_block_size;
     }
     const int64_t pairs = blocks * params->num_q_heads;
-    return static_cast<size_t>((pairs * (rlk::kHeadDim + 1) * 4 + 255) / 256 * 256);
+    return split_table_bytes(pairs) + split_flag_bytes(params->num_seqs, params->num_kv_heads);
   }
   if (op == RLK_OP_MERGE) {
     if (check_cu(params, cu_seqlens_q, cu_seqlens_k) != RLK_OK) return 0;

@@ -73,7 +73,8 @@ struct DecLayout {
                        kPFull = kSEmpty + kSS, kPEmpty = kPFull + kPS, kOFull = kPEmpty + kPS,
                        kOEmpty = kOFull + kOS, kStatsFull = kOEmpty + kOS, kSyncMax = kStatsFull + kSR,
                        kSyncPart = kSyncMax + 4, kQRope = kSyncPart + 4,  // sync: [group][parity]
-                       kNumBars = kQRope + 1;
+                       kFillDone = kQRope + 1,  // split decode: the correction warps' table fill
+                       kNumBars = kFillDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kPageWin = 512;                     // page ids cached per window (one per producer)
   static constexpr int kPageOff = (kMiscOff + 16 + 15) / 16 * 16;
@@ -153,7 +154,10 @@ __device__ __forceinline__ float warp_max(float v) {
 // one another); values still unwritten, or stale, are read again with strong
 // (device-scope relaxed) loads, which the memory model guarantees to see
 // other SMs' stores eventually (a thread's strong loads complete one after
-// another).  Returns false on a timeout (reported) or an abort.
+// another).  When the producers fill the table themselves (fill_flag set),
+// the chain first waits until every item of the pair has published its
+// flag: before that, an item's slots may still hold an earlier call's
+// states.  Returns false on a timeout (reported) or an abort.
 __device__ __noinline__ bool fold_chain_on_chip(const FwdParams& p, int seq, int g, int q, int lane,
                                                 volatile int* abort) {
   constexpr int C = 8;
@@ -199,6 +203,27 @@ __device__ __noinline__ bool fold_chain_on_chip(const FwdParams& p, int seq, int
         if (unwritten4(v[i])) v[i] = ld_l2_poll4(o_src(c0, nc, i));
     }
   };
+  if (p.fill_flag) {
+    // lane r (and r + 32): item r's flag; the warp barrier then orders every
+    // lane's table reads after the acquiring loads
+    const int nr = min(p.split_stride, nbp);
+    const uint64_t* flag = p.fill_flag + (static_cast<int64_t>(seq) * p.hkv + g) * kMaxSplitK;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      bool filled = true;
+      for (int r = lane; r < nr; r += 32) filled = ld_acquire_u64(flag + r) == p.fill_nonce && filled;
+      if (__all_sync(0xffffffffu, filled)) break;
+      const bool late = __shfl_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitTimeoutNs, 0);
+      if (late || *abort) {
+        if (late && lane == 0) {
+          *abort = 1;
+          report_error(p.err, kErrDeviceTimeout, 0x903);
+        }
+        return false;
+      }
+    }
+    __syncwarp();
+  }
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   float Lrun = -INFINITY;
   float lsl, lsn = 0.f;
@@ -297,6 +322,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(&bars[L::kSyncPart + s], 128);
     }
     mbar_init(&bars[L::kQRope], 128);
+    mbar_init(&bars[L::kFillDone], 128);
     *abort = 0;
     fence_mbar_init();
   }
@@ -615,7 +641,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     // ------------------------------------------------------------ correction / epilogue
     const int d = tid;  // head dimension lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t o_it = 0, rq_it = 0;
+    uint32_t o_it = 0, rq_it = 0, fill_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
@@ -660,6 +686,33 @@ __global__ void __launch_bounds__(kDThreads, 1)
         fence_proxy_async_smem();  // the tensor core reads the rows through the async proxy
         mbar_arrive(&bars[L::kQRope]);
       }
+      if (FOLD && split && p.fill_flag) {
+        // the item's slots of the state table hold kUnwritten before any of
+        // its states can land (the fold takes any other value as landed);
+        // the flag, set once the first block's state is written (the fill's
+        // stores have long drained by then), tells the fold warps.  After the
+        // query rotation, which the first S waits for.
+        const int64_t blk0 = p.cu_q[seq] + di.b0;
+        const int per = G * (kHeadDim / 4);  // float4s of one block's states
+        const float u = __uint_as_float(kUnwritten);
+        const float4 u4 = make_float4(u, u, u, u);
+        for (int i = tid; i < nb * per; i += 128) {
+          const int j = i / per;
+          reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G) *
+                                                    kHeadDim)[i - j * per] = u4;
+        }
+        for (int i = tid; i < nb * G; i += 128) {
+          const int j = i / G;
+          p.state_lse[(blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G + (i - j * G)] = u;
+        }
+        // another warp's thread writes a slot's state: the barrier (release
+        // on arrival, acquire on completion) orders every fill store before
+        // every state store
+        mbar_arrive(&bars[L::kFillDone]);
+        const bool ok = mbar_wait(&bars[L::kFillDone], fill_it & 1, abort, p.err, 0x804);
+        ++fill_it;
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
       float O[MG];
 #pragma unroll
       for (int q = 0; q < MG; ++q) O[q] = 0.0f;
@@ -701,6 +754,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         if (split) {
           if (warp == 0 && lane < G) p.state_lse[pair_b + lane] = lb;
+          if (FOLD && p.fill_flag && j == 0) {
+            // the fill barrier and the releasing store order the four warps'
+            // fill stores before the flag
+            if (tid == 0)
+              st_release_u64(p.fill_flag + (static_cast<int64_t>(seq) * p.hkv + g) * kMaxSplitK + di.b0,
+                             p.fill_nonce);
+          }
         } else if (lane < G) {
           Lrun = (j == 0) ? lb : Lp;
         }

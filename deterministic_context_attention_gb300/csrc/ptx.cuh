@@ -368,6 +368,16 @@ __device__ __forceinline__ float ld_l2_poll(const float* p) {
   asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
+// Release / acquire at device scope, for a flag that orders a CTA's earlier
+// stores before another CTA's later loads.
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 // The weak forms: L2 (never L1, which other SMs' stores do not update), and
 // overlapping one another; a value they return is current or older.
 __device__ __forceinline__ float ld_l2_weak(const float* p) {

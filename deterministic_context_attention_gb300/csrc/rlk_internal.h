@@ -16,6 +16,7 @@ constexpr int kDecodeMaxGroup = 8;     // query heads per KV head the transposed
 constexpr int64_t kNoAllocIndexEntries = 65536;  // no-alloc merge scratch: (sequence, block) index entries
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded mbarrier waits: 1 s
 constexpr uint32_t kUnwritten = 0xFFFFFFFFu;  // state-table fill of the on-chip fold (a NaN arithmetic never makes)
+constexpr int kMaxSplitK = 64;  // split decode: items per (sequence, KV head)
 
 // device error word bits
 constexpr unsigned kErrDeviceTimeout = 1u;
@@ -69,9 +70,13 @@ struct FwdParams {
   // split decode with the fold on chip: item r of a (sequence, KV head) takes
   // the blocks b = r, r + split_stride, ... (0: contiguous ranges, or the
   // whole sequence); the CTAs past the items fold the states of fold_seqs
-  // sequences as the producers write them into the table, which holds
-  // kUnwritten before
+  // sequences as the producers write them into the table.  Each item first
+  // fills its own slots with kUnwritten and then stores fill_nonce (a value
+  // new to every call) to fill_flag[(seq * hkv + g) * kMaxSplitK + r]; the
+  // fold reads an item's slots once its flag holds the nonce
   int32_t split_stride, fold_seqs;
+  uint64_t* fill_flag;
+  uint64_t fill_nonce;
   // transposed decode: RoPE table [positions][cos 64, sin 64] (FP32); when
   // set, the query rows are rotated at position kv_len - 1 after they land
   const float* rope_table;

@@ -312,7 +312,10 @@ rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void*
  *     once (one CTA per SM), item r takes the blocks b = r (mod split_k) and
  *     the whole call is one cooperative launch whose fold CTAs, on SMs the
  *     items leave free, fold the states as the items write them (the fold
- *     hides behind the producers);
+ *     hides behind the producers).  Each item first marks its table slots
+ *     unwritten and then sets its flag in the workspace to a value new to
+ *     the call; inside a CUDA graph capture a fill of the table precedes
+ *     the launch instead (a replay repeats the launch's arguments);
  *   - otherwise item r takes the contiguous blocks floor(r*nb/k) up to
  *     floor((r+1)*nb/k) (nb = the sequence's blocks) and a second kernel
  *     folds the table.
@@ -327,7 +330,9 @@ rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void*
  *     runs the single-pass decode) -- the result is the same for every k;
  *   workspace: device, >= rlk_attn_workspace_size(params,
  *     RLK_OP_DECODE_SPLIT, NULL, seqlens) bytes (the state table: 516 bytes
- *     per (sequence, block, query head)).
+ *     per (sequence, block, query head), rounded up to 256, then 512 bytes
+ *     of item flags per (sequence, KV head)); its contents need no
+ *     initialisation, and calls on one workspace must not overlap.
  * Needs kv_block_size 128 and at most 8 query heads per KV head
  * (RLK_ERR_UNSUPPORTED otherwise).
  * [P3] PR stack: decode KV-cache replay; Status: fixed global_block_index

@@ -179,9 +179,10 @@ def test_split_decode_rejects_before_any_launch(lib):
 
 def test_split_decode_workspace_size(lib):
     p = rlk.make_params(2)  # Hq 32
-    # 300 and 129 tokens: 3 + 2 blocks of 128; 516 bytes per (block, query head), rounded up to 256
+    # 300 and 129 tokens: 3 + 2 blocks of 128; 516 bytes per (block, query
+    # head), rounded up to 256, then 64 8-byte fill flags per (sequence, KV head)
     got = rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 129])
-    assert got == (5 * 32 * 129 * 4 + 255) // 256 * 256
+    assert got == (5 * 32 * 129 * 4 + 255) // 256 * 256 + 2 * 8 * 64 * 8
     assert rlk.rlk_attn_workspace_size(p, rlk.RLK_OP_DECODE_SPLIT, None, [300, 0]) == 0
 
 
