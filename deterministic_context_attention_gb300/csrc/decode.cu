@@ -405,11 +405,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // item (a block's 2^lg pages: page_size is a power of two dividing B)
         const int win = j >> (9 - lg);
         if (cached != win) {
-          for (int i = lane; i < L::kPageWin; i += 32) {
+          // the lane's 16 loads all in flight before the first store (one
+          // after another they took ~10 us, the whole start of a long item)
+          int32_t pg[L::kPageWin / 32];
+#pragma unroll
+          for (int t = 0; t < L::kPageWin / 32; ++t) {
+            const int i = lane + 32 * t;
             const int jj = (win << (9 - lg)) + (i >> lg);  // block of the item
             const int gp = ((di.b0 + jj * di.stride) << lg) + (i & ((1 << lg) - 1));
-            wc[i] = (jj < nb && gp < seq_pages) ? prow[gp] : -1;
+            pg[t] = (jj < nb && gp < seq_pages) ? __ldg(prow + gp) : -1;
           }
+#pragma unroll
+          for (int t = 0; t < L::kPageWin / 32; ++t) wc[lane + 32 * t] = pg[t];
           __syncwarp();
           cached = win;
         }

@@ -366,9 +366,18 @@ __global__ void __launch_bounds__(512, 1)
           if ((wbuf ? cached_win1 : cached_win0) != win) {
             const int seq_pages = (it.kv_len + ps - 1) / ps;
             const int32_t* row = p.page_table + static_cast<int64_t>(it.seq) * p.max_pages;
-            for (int i = lane; i < L::kPageWin; i += 32) {
-              const int gp = win * L::kPageWin + i;
-              wc[i] = gp < seq_pages ? row[gp] : -1;
+            // four loads of the lane in flight at a time (one after another
+            // they serialise on the memory latency)
+#pragma unroll
+            for (int t0 = 0; t0 < L::kPageWin / 32; t0 += 4) {
+              int32_t pg[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int gp = win * L::kPageWin + lane + 32 * (t0 + t);
+                pg[t] = gp < seq_pages ? __ldg(row + gp) : -1;
+              }
+#pragma unroll
+              for (int t = 0; t < 4; ++t) wc[lane + 32 * (t0 + t)] = pg[t];
             }
             __syncwarp();
             if (wbuf) cached_win1 = win; else cached_win0 = win;
