@@ -138,11 +138,13 @@ EncodeTiledFn encode_fn() {
 
 // BF16 tensor [d2][d1][128] as a 3-D map (innermost first), 128-byte swizzle,
 // box {64, box1, box2}.
-rlk_status make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint32_t box1, uint32_t box2) {
+// Rows of 128 BF16 elements, head_bytes apart (256: packed [T, H, 128]).
+rlk_status make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint32_t box1, uint32_t box2,
+                    uint64_t head_bytes = 256) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {128, d1, d2};
-  cuuint64_t strides[2] = {256, 256 * d1};
+  cuuint64_t strides[2] = {head_bytes, head_bytes * d1};
   cuuint32_t box[3] = {64, box1, box2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -479,8 +481,10 @@ rlk_status rlk_attn_prefill_states(const rlk_attn_params* params, const void* q,
 
 namespace {
 
-// The fused prefill, with the query rows rotated by RoPE inside the kernel
-// when rope_table is given (at their absolute positions kv_len - q_len + i).
+// The fused prefill, with the query rows rotated by RoPE when rope_table is
+// given (at their absolute positions kv_len - q_len + i): by a pass into the
+// output buffer for whole sequences, inside the kernel for one CP rank's
+// rows (the buffer's other rows belong to the other ranks' calls).
 rlk_status prefill_impl(const rlk_attn_params* params, const void* q, const void* k, const void* v,
                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t cp_rank,
                         const float* rope_table, int32_t rope_max_pos, float* out_f32, void* out_bf16, float* lse,
@@ -548,7 +552,35 @@ rlk_status prefill_impl(const rlk_attn_params* params, const void* q, const void
   for (auto& c : costed) tiles.push_back(c.second);
   const int tq = cu_seqlens_q[params->num_seqs], tk = cu_seqlens_k[params->num_seqs];
   CUtensorMap mq, mk, mv;
-  if ((st = make_map(&mq, q, params->num_q_heads, tq, 1, rlk::kTileRows))) return st;
+  if (rope_table && cp_rank < 0) {
+    // whole sequences: one pass rotates the queries into the output buffer
+    // and the plain fused kernel reads them from there.  Row (token, head)
+    // goes to that row's own output slot, which only the item of that token
+    // tile and head reads (at its start) and writes (at its end), so no item
+    // reads a slot another has overwritten.  The rotation is the canonical
+    // one the kernel would apply, so the bits are the same; the pass streams
+    // at HBM rate and takes the rotation off the items' critical path.
+    uint16_t* rq = out_bf16 ? static_cast<uint16_t*>(out_bf16) : reinterpret_cast<uint16_t*>(out_f32);
+    const int ystride = out_bf16 ? rlk::kHeadDim : 2 * rlk::kHeadDim;  // BF16 elements per (token, head) slot
+    auto rp = std::make_unique<rlk::RopeParams>();
+    std::memset(rp.get(), 0, sizeof(*rp));
+    rp->x = static_cast<const uint16_t*>(q);
+    rp->y = rq;
+    rp->y_stride = ystride;
+    rp->table = rope_table;
+    rp->rows = static_cast<int64_t>(tq) * params->num_q_heads;
+    rp->heads = params->num_q_heads;
+    rp->num_seqs = params->num_seqs;
+    for (int s = 0; s <= params->num_seqs; ++s) rp->cu[s] = cu_seqlens_q[s];
+    for (int s = 0; s < params->num_seqs; ++s)
+      rp->pos0[s] = (cu_seqlens_k[s + 1] - cu_seqlens_k[s]) - (cu_seqlens_q[s + 1] - cu_seqlens_q[s]);
+    cudaError_t e = rlk::launch_rope(*rp, dev->num_sms, stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
+    if ((st = make_map(&mq, rq, params->num_q_heads, tq, 1, rlk::kTileRows, 2ull * ystride))) return st;
+    rope_table = nullptr;
+  } else if ((st = make_map(&mq, q, params->num_q_heads, tq, 1, rlk::kTileRows))) {
+    return st;
+  }
   if ((st = make_map(&mk, k, params->num_kv_heads, tk, 1, B))) return st;
   if ((st = make_map(&mv, v, params->num_kv_heads, tk, 1, B))) return st;
   auto fp = std::make_unique<rlk::FwdParams>();
@@ -812,14 +844,13 @@ namespace {
 // to the smaller k (less state traffic).
 constexpr double kSplitItemStartup = 1.0;  // blocks' worth of start-up per item
 constexpr double kSplitFoldPerBlock = 0.08;  // fold chain step / KV block step
-// The fold on chip: split_k producer items per (sequence, KV head) pair and
-// fold CTAs (one warp per (sequence, query head), 15 a CTA) in one
-// cooperative launch, the folds following their producers, so every CTA must
-// be resident at once: one CTA per SM.
+
 // split decode workspace: the state table (o_b then lse_b of every pair),
 // rounded to 256 bytes, then one 8-byte fill flag per (sequence, KV head,
 // item) for the on-chip fold
-size_t split_table_bytes(int64_t pairs) { return static_cast<size_t>((pairs * (rlk::kHeadDim + 1) * 4 + 255) / 256 * 256); }
+size_t split_table_bytes(int64_t pairs) {
+  return static_cast<size_t>((pairs * (rlk::kHeadDim + 1) * 4 + 255) / 256 * 256);
+}
 size_t split_flag_bytes(int num_seqs, int hkv) {
   return static_cast<size_t>(num_seqs) * hkv * rlk::kMaxSplitK * sizeof(uint64_t);
 }
@@ -839,6 +870,10 @@ uint64_t next_fill_nonce() {
   }
 }
 
+// The fold on chip: split_k producer items per (sequence, KV head) pair and
+// fold CTAs (one warp per (sequence, query head), 15 a CTA) in one
+// cooperative launch, the folds following their producers, so every CTA must
+// be resident at once: one CTA per SM.
 constexpr int kFoldChainsPerCta = 15;
 int fold_ctas(int num_seqs, int hq) { return (num_seqs * hq + kFoldChainsPerCta - 1) / kFoldChainsPerCta; }
 bool fold_on_chip(int num_seqs, int hkv, int hq, int k, int num_sms) {

@@ -124,7 +124,8 @@ struct RopeParams {
   const float* table;   // [positions][cos 64, sin 64]
   int64_t rows;         // T * heads
   int64_t rows2;        // T * heads2
-  int32_t heads, heads2, num_seqs, pad0;
+  int32_t heads, heads2, num_seqs;
+  int32_t y_stride;     // elements from one (token, head) row of y to the next (0: 128)
   int32_t cu[kMaxSeqs + 1];
   int32_t pos0[kMaxSeqs];
 };

@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kRopeThreads) rlk_rope_kernel(const __grid_con
     const float4 c0 = __ldg(t + 2 * j), c1 = __ldg(t + 2 * j + 1);
     const float4 s0 = __ldg(t + 16 + 2 * j), s1 = __ldg(t + 16 + 2 * j + 1);
     rope8(a, b, c0, c1, s0, s1);
-    uint4* yr = reinterpret_cast<uint4*>((second ? p.y2 : p.y) + row * kHeadDim);
+    const int64_t ys = (second || p.y_stride == 0) ? kHeadDim : p.y_stride;
+    uint4* yr = reinterpret_cast<uint4*>((second ? p.y2 : p.y) + row * ys);
     yr[j] = a;
     yr[8 + j] = b;
   }

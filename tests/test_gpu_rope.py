@@ -197,6 +197,35 @@ def test_prefill_with_in_kernel_rope(lens, kv_extra, block):
     assert_forward_parity(*(x[rows] for x in fused), ref_out, ref_lse, "prefill with in-kernel RoPE")
 
 
+@pytest.mark.parametrize("keep", ["f32", "bf16"])
+def test_prefill_rope_single_output(keep):
+    # whole sequences rotate their queries through the output buffer they
+    # are given: with only the FP32 or only the BF16 output, the result is
+    # the two-output call's, bit for bit
+    lens = [700, 129, 1]
+    prob = synth.prefill_problem(lens=lens, hq=32, hkv=8, block=128, seed=84, kv_lens=[n + 5 for n in lens])
+    q_raw = synth.normal_bf16(85, synth.T_Q, prob.q.shape)
+    k_rot = oracle.rope_f32(prob.k, positions(prob.cu_k, None), THETA)
+    ref_out, ref_outb, ref_lse = _prefill_rope(prob, q_raw, k_rot)
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    from tests.gpu_helpers import params_of
+    qd, kd, vd = dv.bf16_to_device(q_raw), dv.bf16_to_device(k_rot), dv.bf16_to_device(prob.v)
+    max_pos = int(np.diff(prob.cu_k).max())
+    out, outb, lse = empty_outputs(torch, qd.shape[0], prob.hq)
+    rlk.rlk_attn_prefill_rope(params_of(prob, 1, 1), qd, kd, vd, prob.cu_q, prob.cu_k, -1, table_dev(max_pos), max_pos,
+                              out if keep == "f32" else None, outb if keep == "bf16" else None, lse)
+    rlk.rlk_attn_check_device_error()
+    np.testing.assert_array_equal(lse.cpu().numpy(), ref_lse)
+    if keep == "f32":
+        np.testing.assert_array_equal(out.cpu().numpy(), ref_out)
+    else:
+        np.testing.assert_array_equal(outb.float().cpu().numpy(), ref_outb)
+    # the queries themselves are not modified
+    np.testing.assert_array_equal(qd.cpu().view(torch.int16).numpy().view(np.uint16), synth.bf16_bits(q_raw))
+
+
 def test_rope_qk_single_launch_equals_two_passes():
     # queries and keys of the same tokens in one launch, bit for bit the two
     # single-tensor passes (ragged lengths, an empty sequence, offsets)
