@@ -195,12 +195,17 @@ rlk_status rlk_attn_prefill(const rlk_attn_params* params, const void* q, const 
                             rlk_stream_t stream);
 
 /*
- * rlk_attn_prefill with the queries' RoPE applied inside the prefill kernel:
- * q is the PRE-RoPE query; each query row is rotated at its absolute
- * position kv_len - q_len + i (the sequence's token index) right after its
- * tile lands in shared memory, in the FP32 form of rlk_attn_rope, so the
- * result is bit-identical to rlk_attn_rope on q followed by
- * rlk_attn_prefill.  k is post-RoPE, as stored in a KV cache.
+ * rlk_attn_prefill with the queries' RoPE applied by the call: q is the
+ * PRE-RoPE query (left unchanged); each query row is rotated at its absolute
+ * position kv_len - q_len + i (the sequence's token index) in the FP32 form
+ * of rlk_attn_rope, so the result is bit-identical to rlk_attn_rope on q
+ * followed by rlk_attn_prefill.  k is post-RoPE, as stored in a KV cache.
+ * With cp_rank -1 one pass writes the rotated rows into the output buffer
+ * (out_bf16 if given, else the first half of each out_f32 row), each row into
+ * its own (token, head) slot, and the prefill reads them from there before it
+ * overwrites the slot with the result; with cp_rank >= 0 the kernel rotates
+ * each tile in shared memory after it lands (the other rows of the buffer
+ * belong to the other ranks' calls).  The outputs must not overlap q, k or v.
  *   rope_table: device FP32 [rope_max_pos][128] from rlk_attn_rope_table;
  *   every sequence with queries needs kv_len <= rope_max_pos.
  * Other arguments and outputs as in rlk_attn_prefill.
