@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(384, 1)
         // rate costs more than their overlap gains (measured 1.6 % slower
         // for the whole backward); the accumulation order is the halves'.
         constexpr uint32_t kIdK128 = idesc_bf16(128, 128, false, false);
-        auto issue_sdp128 = [&](uint32_t st_addr) {
+        auto issue_sdp128 = [&](uint32_t st_addr, bool last) {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             if (leader) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK128, k > 0);
@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(384, 1)
           if (leader) {
             umma_commit(&bars[L::kSFull]);
             umma_commit(&bars[L::kSFull + 1]);
+            if (last) umma_commit(&bars[L::kResEmpty]);  // the item's last S/dP: the resident pair is free
           }
           __syncwarp();
         };
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(384, 1)
           bool w = mbar_wait(&bars[L::kStFull + st_it % L::kStages], (st_it / L::kStages) & 1, abort, p.err, 0x613);
           if (!__all_sync(0xffffffffu, w)) break;
           tc_fence_after();
-          issue_sdp128(stage_addr(st_it));
+          issue_sdp128(stage_addr(st_it), nsteps == 1);
         }
         ok = mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -362,17 +363,14 @@ __global__ void __launch_bounds__(384, 1)
           issue_acc(stage_addr(cur), 1, false);
           if (leader) {
             umma_commit(&bars[L::kStEmpty + cur % L::kStages]);
-            if (!more) {
-              umma_commit(&bars[L::kAccFull]);
-              umma_commit(&bars[L::kResEmpty]);
-            }
+            if (!more) umma_commit(&bars[L::kAccFull]);
           }
           __syncwarp();
           if (more) {
             w = mbar_wait(&bars[L::kStFull + nxt % L::kStages], (nxt / L::kStages) & 1, abort, p.err, 0x615);
             if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
             tc_fence_after();
-            issue_sdp128(stage_addr(nxt));
+            issue_sdp128(stage_addr(nxt), t + 2 == nsteps);
           }
           ++s_it;
           ++st_it;
@@ -387,6 +385,10 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         issue_sdp(stage_addr(st_it), 0);
         issue_sdp(stage_addr(st_it), 1);
+        if (nsteps == 1) {
+          if (leader) umma_commit(&bars[L::kResEmpty]);  // the item's last S/dP: the resident pair is free
+          __syncwarp();
+        }
       }
       // the accumulators are free once the previous item's epilogue read them
       ok = mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
@@ -401,10 +403,7 @@ __global__ void __launch_bounds__(384, 1)
           issue_acc(stage_addr(cur), c, t == 0 && c == 0);
           if (c == 1 && leader) {
             umma_commit(&bars[L::kStEmpty + cur % L::kStages]);  // step t's stage is no longer read
-            if (!more) {
-              umma_commit(&bars[L::kAccFull]);
-              umma_commit(&bars[L::kResEmpty]);
-            }
+            if (!more) umma_commit(&bars[L::kAccFull]);
           }
           __syncwarp();
           if (more) {
@@ -414,6 +413,10 @@ __global__ void __launch_bounds__(384, 1)
               tc_fence_after();
             }
             issue_sdp(stage_addr(nxt), c);
+            if (c == 1 && t + 2 == nsteps) {
+              if (leader) umma_commit(&bars[L::kResEmpty]);  // the item's last S/dP: the resident pair is free
+              __syncwarp();
+            }
           }
         }
         if (fail) break;
