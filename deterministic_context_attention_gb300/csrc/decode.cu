@@ -73,7 +73,7 @@ struct DecLayout {
                        kPFull = kSEmpty + kSS, kPEmpty = kPFull + kPS, kOFull = kPEmpty + kPS,
                        kOEmpty = kOFull + kOS, kStatsFull = kOEmpty + kOS, kSyncMax = kStatsFull + kSR,
                        kSyncPart = kSyncMax + 4, kQRope = kSyncPart + 4,  // sync: [group][parity]
-                       kFillDone = kQRope + 1,  // split decode: the correction warps' table fill
+                       kFillDone = kQRope + 1,  // split decode: the table fill (correction + softmax warps)
                        kNumBars = kFillDone + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort (i32)
   static constexpr int kPageWin = 512;                     // page ids cached per window (one per producer)
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(&bars[L::kSyncPart + s], 128);
     }
     mbar_init(&bars[L::kQRope], 128);
-    mbar_init(&bars[L::kFillDone], 128);
+    mbar_init(&bars[L::kFillDone], 384);
     *abort = 0;
     fence_mbar_init();
   }
@@ -559,6 +559,26 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (item >= p.num_items) continue;
       const DecItem di = dec_item(p, item);
       const int kv_len = di.kv_len, nb = di.nb;
+      if (FOLD && p.state_o && p.fill_flag) {
+        // their share of the item's table fill (threads 128-383; the
+        // correction warps take 0-127), released to the correction warps,
+        // which wait for both shares before their first state store (one
+        // item per CTA here, so a phase of the fill barrier is one item)
+        const int64_t blk0 = p.cu_q[di.seq] + di.b0;
+        const int per = G * (kHeadDim / 4);
+        const float u = __uint_as_float(kUnwritten);
+        const float4 u4 = make_float4(u, u, u, u);
+        for (int i = tid; i < nb * per; i += 384) {
+          const int jj = i / per;
+          reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(jj) * di.stride) * p.hq + di.g * G) *
+                                                    kHeadDim)[i - jj * per] = u4;
+        }
+        for (int i = tid; i < nb * G; i += 384) {
+          const int jj = i / G;
+          p.state_lse[(blk0 + static_cast<int64_t>(jj) * di.stride) * p.hq + di.g * G + (i - jj * G)] = u;
+        }
+        mbar_arrive(&bars[L::kFillDone]);
+      }
       bool fail = false;
       for (int j = 0; j < nb; ++j, ++s_it) {
         if (static_cast<int>(s_it & 1) != grp) continue;  // the other group's block
@@ -696,6 +716,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (FOLD && split && p.fill_flag) {
         // the item's slots of the state table hold kUnwritten before any of
         // its states can land (the fold takes any other value as landed);
+        // the softmax warps fill a share (threads 128-383) at their item start;
         // the flag, set once the first block's state is written (the fill's
         // stores have long drained by then), tells the fold warps.  After the
         // query rotation, which the first S waits for.
@@ -703,12 +724,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const int per = G * (kHeadDim / 4);  // float4s of one block's states
         const float u = __uint_as_float(kUnwritten);
         const float4 u4 = make_float4(u, u, u, u);
-        for (int i = tid; i < nb * per; i += 128) {
+        for (int i = tid; i < nb * per; i += 384) {
           const int j = i / per;
           reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G) *
                                                     kHeadDim)[i - j * per] = u4;
         }
-        for (int i = tid; i < nb * G; i += 128) {
+        for (int i = tid; i < nb * G; i += 384) {
           const int j = i / G;
           p.state_lse[(blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G + (i - j * G)] = u;
         }
