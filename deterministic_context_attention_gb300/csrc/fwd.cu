@@ -488,9 +488,11 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t sidx = sb + j, buf = sidx & 1;
           const uint32_t vi = vb + j, vstage = vi % SV;
           const uint32_t pvi = pb + j, pvbuf = pvi & 1;
-          bool w = mbar_wait(&bars[L::kPFull + buf], (sidx >> 1) & 1, abort, p.err, 0x203);
-          w = w && mbar_wait(&bars[L::kVFull + vstage], (vi / SV) & 1, abort, p.err, 0x204);
+          // V_j and the PV buffer are normally ready: their checks come before
+          // the wait for P_j, so only that wait's wake-up follows the softmax
+          bool w = mbar_wait(&bars[L::kVFull + vstage], (vi / SV) & 1, abort, p.err, 0x204);
           w = w && mbar_wait(&bars[L::kPVEmpty + pvbuf], ((pvi >> 1) & 1) ^ 1, abort, p.err, 0x205);
+          w = w && mbar_wait(&bars[L::kPFull + buf], (sidx >> 1) & 1, abort, p.err, 0x203);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           uint8_t* vd = v_base + vstage * L::kKVBytes;
           // V rows past the valid keys of a partial block may hold stale or
