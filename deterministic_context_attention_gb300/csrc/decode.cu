@@ -132,6 +132,27 @@ __device__ __forceinline__ DecItem dec_item(const FwdParams& p, int item) {
   return d;
 }
 
+// Split decode with the fold on chip: thread t of the 384 correction and
+// softmax threads writes its share of the item's state-table slots with
+// kUnwritten (o_b as 16-byte pieces, then lse_b) before any of the item's
+// states can land.
+constexpr int kFillThreads = 384;
+__device__ __forceinline__ void fill_item_slots(const FwdParams& p, const DecItem& di, int G, int t) {
+  const int64_t blk0 = p.cu_q[di.seq] + di.b0;
+  const int per = G * (kHeadDim / 4);  // 16-byte pieces of one block's states
+  const float u = __uint_as_float(kUnwritten);
+  const float4 u4 = make_float4(u, u, u, u);
+  for (int i = t; i < di.nb * per; i += kFillThreads) {
+    const int j = i / per;
+    reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + di.g * G) *
+                                              kHeadDim)[i - j * per] = u4;
+  }
+  for (int i = t; i < di.nb * G; i += kFillThreads) {
+    const int j = i / G;
+    p.state_lse[(blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + di.g * G + (i - j * G)] = u;
+  }
+}
+
 // Row maximum of the 32 lanes of a warp (exact; every lane receives it).
 __device__ __forceinline__ float warp_max(float v) {
   float m;
@@ -322,7 +343,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(&bars[L::kSyncPart + s], 128);
     }
     mbar_init(&bars[L::kQRope], 128);
-    mbar_init(&bars[L::kFillDone], 384);
+    mbar_init(&bars[L::kFillDone], kFillThreads);
     *abort = 0;
     fence_mbar_init();
   }
@@ -564,19 +585,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // correction warps take 0-127), released to the correction warps,
         // which wait for both shares before their first state store (one
         // item per CTA here, so a phase of the fill barrier is one item)
-        const int64_t blk0 = p.cu_q[di.seq] + di.b0;
-        const int per = G * (kHeadDim / 4);
-        const float u = __uint_as_float(kUnwritten);
-        const float4 u4 = make_float4(u, u, u, u);
-        for (int i = tid; i < nb * per; i += 384) {
-          const int jj = i / per;
-          reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(jj) * di.stride) * p.hq + di.g * G) *
-                                                    kHeadDim)[i - jj * per] = u4;
-        }
-        for (int i = tid; i < nb * G; i += 384) {
-          const int jj = i / G;
-          p.state_lse[(blk0 + static_cast<int64_t>(jj) * di.stride) * p.hq + di.g * G + (i - jj * G)] = u;
-        }
+        fill_item_slots(p, di, G, tid);
         mbar_arrive(&bars[L::kFillDone]);
       }
       bool fail = false;
@@ -720,19 +729,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // the flag, set once the first block's state is written (the fill's
         // stores have long drained by then), tells the fold warps.  After the
         // query rotation, which the first S waits for.
-        const int64_t blk0 = p.cu_q[seq] + di.b0;
-        const int per = G * (kHeadDim / 4);  // float4s of one block's states
-        const float u = __uint_as_float(kUnwritten);
-        const float4 u4 = make_float4(u, u, u, u);
-        for (int i = tid; i < nb * per; i += 384) {
-          const int j = i / per;
-          reinterpret_cast<float4*>(p.state_o + ((blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G) *
-                                                    kHeadDim)[i - j * per] = u4;
-        }
-        for (int i = tid; i < nb * G; i += 384) {
-          const int j = i / G;
-          p.state_lse[(blk0 + static_cast<int64_t>(j) * di.stride) * p.hq + g * G + (i - j * G)] = u;
-        }
+        fill_item_slots(p, di, G, tid);
         // another warp's thread writes a slot's state: the barrier (release
         // on arrival, acquire on completion) orders every fill store before
         // every state store
