@@ -871,10 +871,10 @@ uint64_t next_fill_nonce() {
 }
 
 // The fold on chip: split_k producer items per (sequence, KV head) pair and
-// fold CTAs (one warp per (sequence, query head), 15 a CTA) in one
+// fold CTAs (one warp per (sequence, query head), 16 a CTA) in one
 // cooperative launch, the folds following their producers, so every CTA must
 // be resident at once: one CTA per SM.
-constexpr int kFoldChainsPerCta = 15;
+constexpr int kFoldChainsPerCta = 16;
 int fold_ctas(int num_seqs, int hq) { return (num_seqs * hq + kFoldChainsPerCta - 1) / kFoldChainsPerCta; }
 bool fold_on_chip(int num_seqs, int hkv, int hq, int k, int num_sms) {
   const int64_t items = static_cast<int64_t>(num_seqs) * hkv * k;

@@ -18,14 +18,16 @@
 // for a product and for its transposed formulation, so a decode row equals
 // the prefill's last row of the same sequence bit for bit.
 //
-// Warp roles (480 threads):
+// Warp roles (512 threads):
 //   warps 0-3   correction / epilogue: thread d owns TMEM lane d (head
 //               dimension d) and keeps the running O of every query head
 //   warps 4-7   softmax of the even blocks, warps 8-11 of the odd blocks:
 //               thread t owns TMEM lane t (key t of the block)
 //   warp  12    TMA producer of the group's query rows and the K pages
 //   warp  13    TMA producer of the V pages
-//   warp  14    TMEM allocator and MMA issuer
+//   warp  14    TMEM allocator and issuer of the S^T products
+//   warp  15    issuer of the O^T (PV) products (two issuers: these small
+//               MMAs are issue-bound, 7 % on a few long sequences)
 // Split decode with the fold on chip adds CTAs past the work items, on SMs
 // the producers leave free, whose warps fold one (sequence, KV head, query
 // head) each as the producers write the block states.
@@ -43,7 +45,7 @@
 namespace rlk {
 namespace {
 
-constexpr int kDThreads = 480;
+constexpr int kDThreads = 512;
 constexpr int kDN = 16;  // MMA N: the group's query heads, padded with zero rows
 
 struct DecLayout {
@@ -459,12 +461,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
       if (fail || *abort) break;
     }
   } else if (warp == 14) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     constexpr uint32_t kIdS = idesc_bf16(128, kDN, false, false);  // A = K (K-major), B = Q (K-major)
-    constexpr uint32_t kIdO = idesc_bf16(128, kDN, true, false);   // A = V^T (dims contiguous), B = P^T
     const Desc qd = make_desc(smem_u32(q_tile), 16, 1024);
     const uint32_t leader = elect_one_sync();
-    uint32_t k_it = 0, v_it = 0, s_it = 0, o_it = 0, q_it = 0;
+    uint32_t k_it = 0, s_it = 0, q_it = 0;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
       const int item = dec_snake_item(round);
       if (item >= p.num_items) continue;
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       bool ok = mbar_wait(&bars[p.rope_table ? L::kQRope : L::kQFull], q_it & 1, abort, p.err, 0x601);
       if (!__all_sync(0xffffffffu, ok)) break;
       ++q_it;
-      const uint32_t kb = k_it, vb = v_it, sb = s_it, ob = o_it;
+      const uint32_t kb = k_it, sb = s_it;
       // S^T_j = K_j Q^T into S^T slot (sb + j) mod SS
       auto issue_s = [&](int j) -> bool {
         const uint32_t ki = kb + j, stage = ki % SK;
@@ -505,14 +506,27 @@ __global__ void __launch_bounds__(kDThreads, 1)
         __syncwarp();
         return true;
       };
-      // S runs up to three blocks ahead of O (the S^T ring has four slots)
-      const int ahead = min(nb, 3);
+      // S runs as far ahead as the S^T ring allows; warp 15 issues the PV products
       bool fail = false;
-      for (int j = 0; j < ahead && !fail; ++j)
+      for (int j = 0; j < nb && !fail; ++j)
         if (!issue_s(j)) fail = true;
       if (fail) break;
+      k_it += nb;
+      s_it += nb;
+    }
+  } else if (warp == 15) {
+    // ------------------------------------------------------------ PV issuer
+    constexpr uint32_t kIdO = idesc_bf16(128, kDN, true, false);   // A = V^T (dims contiguous), B = P^T
+    const uint32_t leader = elect_one_sync();
+    uint32_t v_it = 0, o_it = 0;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_items; ++round) {
+      const int item = dec_snake_item(round);
+      if (item >= p.num_items) continue;
+      const DecItem di = dec_item(p, item);
+      const int kv_len = di.kv_len, nb = di.nb;
+      const uint32_t vb = v_it, ob = o_it;
+      bool fail = false;
       for (int j = 0; j < nb; ++j) {
-        if (j + 3 < nb && !issue_s(j + 3)) { fail = true; break; }
         const uint32_t vi = vb + j, vstage = vi % SV;
         const uint32_t oi = ob + j, oslot = oi % OS, pslot = oi % PS;
         bool w = mbar_wait(&bars[L::kPFull + pslot], (oi / PS) & 1, abort, p.err, 0x604);
@@ -558,9 +572,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         __syncwarp();
       }
       if (fail) break;
-      k_it += nb;
       v_it += nb;
-      s_it += nb;
       o_it += nb;
     }
   } else if (warp >= 4) {

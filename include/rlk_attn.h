@@ -313,7 +313,7 @@ rlk_status rlk_attn_decode_paged_rope(const rlk_attn_params* params, const void*
  * workspace, and each (sequence, query head) is folded in ascending block
  * order with the canonical fold.  Two schedules, with the same bits:
  *   - when the num_seqs * num_kv_heads * split_k items and the fold CTAs
- *     (one warp per (sequence, query head), 15 a CTA) fit on the device at
+ *     (one warp per (sequence, query head), 16 a CTA) fit on the device at
  *     once (one CTA per SM), item r takes the blocks b = r (mod split_k) and
  *     the whole call is one cooperative launch whose fold CTAs, on SMs the
  *     items leave free, fold the states as the items write them (the fold
