@@ -247,3 +247,43 @@ def test_rope_qk_single_launch_equals_two_passes():
     rlk.rlk_attn_check_device_error()
     assert torch.equal(qo.view(torch.int16), q1.view(torch.int16))
     assert torch.equal(ko.view(torch.int16), k1.view(torch.int16))
+
+
+def test_prefill_rope_graph_replay():
+    # the RoPE pass into the output buffer and the prefill after it, captured
+    # in one CUDA graph: replays with new queries copied in equal the eager
+    # call on those queries bit for bit
+    torch = torch_cuda()
+    rlk = lib()
+    from deterministic_context_attention_gb300 import device as dv
+    from tests.gpu_helpers import params_of
+    lens = [1000, 300, 129]
+    prob = synth.prefill_problem(lens=lens, hq=32, hkv=8, block=128, seed=86, kv_lens=[n + 3 for n in lens])
+    k_rot = oracle.rope_f32(prob.k, positions(prob.cu_k, None), THETA)
+    qs = [synth.normal_bf16(87 + i, synth.T_Q, prob.q.shape) for i in range(2)]
+    refs = [_prefill_rope(prob, q_raw, k_rot) for q_raw in qs]
+    max_pos = int(np.diff(prob.cu_k).max())
+    table = table_dev(max_pos)
+    qd, kd, vd = dv.bf16_to_device(qs[0]), dv.bf16_to_device(k_rot), dv.bf16_to_device(prob.v)
+    out, outb, lse = empty_outputs(torch, qd.shape[0], prob.hq)
+    p = params_of(prob, 1, 1)
+
+    def call():
+        rlk.rlk_attn_prefill_rope(p, qd, kd, vd, prob.cu_q, prob.cu_k, -1, table, max_pos, out, outb, lse)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for i in (1, 0, 1):
+        qd.copy_(dv.bf16_to_device(qs[i]))
+        graph.replay()
+        torch.cuda.synchronize()
+        rlk.rlk_attn_check_device_error()
+        assert_bitwise((out.cpu().numpy(), outb.float().cpu().numpy(), lse.cpu().numpy()), refs[i],
+                       f"graph replay with queries {i}")
