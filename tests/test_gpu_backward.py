@@ -89,6 +89,20 @@ def test_backward_parity_small(small):
         assert_grad_parity(got, ref, name)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2), (12, 4)])
+def test_backward_parity_group_sizes(hq, hkv):
+    # groups of 1, 8 and 3 query heads per KV head: with one head per group a
+    # dK/dV item's last KV block has a single step (its resident pair is
+    # released right after that step's S/dP); lengths across block edges and
+    # a one-token sequence
+    prob = synth.prefill_problem(lens=[257, 128, 1, 700], hq=hq, hkv=hkv, block=128, seed=15)
+    dout = synth.normal_bf16(15, synth.T_DOUT, prob.q.shape)
+    dq, dk, dv = forward_and_backward(prob, dout)
+    rq, rk, rv = oracle.backward_f64(prob.q, prob.k, prob.v, dout, prob.cu_q, prob.scale)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        assert_grad_parity(got, ref, f"hq{hq}/hkv{hkv} {name}")
+
+
 @pytest.mark.parametrize("cp", [2, 4])
 def test_backward_cp_and_repeat_bitwise(small, cp):
     prob, dout = small
