@@ -90,6 +90,19 @@ def test_medium_block64_parity():
                    (out, outb, lse), "block 64 states+merge")
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2), (12, 4)])
+def test_group_sizes_parity(hq, hkv):
+    # groups of 1, 8 and 3 query heads per KV head (the items are (tile,
+    # query head) pairs and K/V is read per KV head): oracle parity, and the
+    # states + merge path equal bit for bit
+    prob = synth.prefill_problem(lens=[257, 128, 1, 700], hq=hq, hkv=hkv, block=128, seed=16)
+    out, outb, lse = run_fused(prob)
+    ref_out, ref_lse = oracle_full(prob)
+    assert_forward_parity(out, outb, lse, ref_out, ref_lse, f"hq{hq}/hkv{hkv}")
+    assert_bitwise(run_states_merge(prob, cp=2, layout=1, rank_order=[1, 0], shuffle_seed=2),
+                   (out, outb, lse), f"hq{hq}/hkv{hkv} states+merge")
+
+
 def test_batch_order_invariance(medium):
     base = run_fused(medium)
     order = [3, 0, 4, 2, 1]
