@@ -487,9 +487,11 @@ def measure_rope(torch, rlk, dv, peaks, flush, stream, args):
 
 
 def measure_prefill_rope(torch, rlk, peaks, prob, q, k, v, flush, stream, args, plain_ms):
-    """The headline prefill with the queries' RoPE inside the kernel (pre-RoPE
-    q, post-RoPE k): against the plain prefill and against the RoPE pass on
-    the queries followed by the plain prefill."""
+    """The headline prefill with the queries' RoPE applied by the call
+    (pre-RoPE q, post-RoPE k; whole sequences, so one pass rotates the
+    queries into the output buffer and the fused kernel reads them there):
+    against the plain prefill and against a RoPE pass into a separate
+    buffer followed by the plain prefill."""
     rows = q.shape[0]
     max_pos = int(np.diff(prob.cu_k).max())
     table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
@@ -512,7 +514,7 @@ def measure_prefill_rope(torch, rlk, peaks, prob, q, k, v, flush, stream, args, 
     ms, ms2 = float(np.mean(t_fused)), float(np.mean(t_two))
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
             "vs_plain_prefill": round(ms / plain_ms, 4), "rope_pass_then_prefill_ms": round(ms2, 4),
-            "workload": "the headline prefill with pre-RoPE queries rotated inside the kernel (RoPE theta 1e6)"}
+            "workload": "the headline prefill with pre-RoPE queries, rotated by the call into the output buffer (RoPE theta 1e6)"}
 
 
 def measure_decode_long(torch, rlk, dv, peaks, flush, stream, args, n=4, ctx_len=32768, split_k=(4, 8, 19)):
