@@ -673,7 +673,7 @@ def run_profile(args):
     stream = torch.cuda.current_stream()
     n = args.profile_iters
     if args.profile == "rope":
-        # RoPE in place on the varlen prefill workload's Q and K
+        # RoPE in place on the varlen prefill workload's Q and K, one launch
         cfg = synth.CFG_PREFILL
         cu = synth.cu_seqlens(cfg["lens"])
         t = int(cu[-1])
@@ -681,10 +681,9 @@ def run_profile(args):
         k = dv.bf16_to_device(synth.normal_bf16(cfg["seed"], synth.T_K, (t, cfg["hkv"], 128)))
         max_pos = max(cfg["lens"])
         table = torch.from_numpy(rlk.rlk_attn_rope_table(1.0e6, max_pos)).cuda()
-        pr = rlk.make_params(len(cfg["lens"]))
+        pr = rlk.make_params(len(cfg["lens"]), cfg["hq"], cfg["hkv"])
         for _ in range(n):
-            rlk.rlk_attn_rope(pr, q, q, cfg["hq"], cu, None, table, max_pos, stream=stream)
-            rlk.rlk_attn_rope(pr, k, k, cfg["hkv"], cu, None, table, max_pos, stream=stream)
+            rlk.rlk_attn_rope_qk(pr, q, q, k, k, cu, None, table, max_pos, stream=stream)
     elif args.profile == "decode-long":
         # few long sequences: 4 x 32768 tokens, split decode with split_k 4
         g = torch.Generator(device="cuda")
