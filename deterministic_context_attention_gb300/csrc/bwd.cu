@@ -107,23 +107,33 @@ __global__ void __launch_bounds__(256) rlk_bwd_prep_kernel(const __grid_constant
 }
 
 // ------------------------------------------------------------------ shared layout
-struct BwdLayout {
+template <int KIND>
+struct BwdLayoutT {
   static constexpr int kTile = 128 * kHeadDim * 2;  // one 128 x 128 BF16 tile (two 64-column halves)
   static constexpr int kHalf = 128 * 128;
   static constexpr int kResOff = 0;                 // resident pair (K_j,V_j) or (Q_i,dO_i)
-  static constexpr int kStreamOff = 2 * kTile;      // 2 stages x streamed pair
-  static constexpr int kStages = 2;
-  // per-warp copies of a step's column statistics: [buf 2][warp 8][lse2, Delta][64] floats
-  static constexpr int kVecOff = kStreamOff + kStages * 2 * kTile;
-  static constexpr int kBarOff = kVecOff + 2 * 8 * 2 * 64 * 4;
-  // barriers
-  // S/dP and P/dS barriers come in pairs: one per 64-column half of a step
-  static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 4, kSFull = 6, kPFull = 8,
-                       kAccFull = 10, kAccEmpty = 11, kNumBars = 12;
+  static constexpr int kStreamOff = 2 * kTile;
+  // dK/dV: two stages of the streamed pair (Q_i, dO_i).  dQ: K_j in a ring of
+  // three slots (read by S and by the accumulation) and V_j in a ring of two
+  // (read by dP only): step t + 1's K loads into the slot of step t - 2 while
+  // the accumulations of steps t - 1 and t may still read theirs, so the load
+  // is not between step t's accumulation and step t + 1's S/dP.
+  static constexpr int kStages = 2, kKSlots = 3, kVSlots = 2;
+  static constexpr int kVOff = kStreamOff + kKSlots * kTile;  // dQ
+  static constexpr int kStreamBytes = KIND == 0 ? kStages * 2 * kTile : (kKSlots + kVSlots) * kTile;
+  // per-warp copies of a step's column statistics (dK/dV): [buf 2][warp 8][lse2, Delta][64] floats
+  static constexpr int kVecOff = kStreamOff + kStreamBytes;
+  static constexpr int kVecBytes = KIND == 0 ? 2 * 8 * 2 * 64 * 4 : 0;
+  static constexpr int kBarOff = kVecOff + kVecBytes;
+  // barriers; S/dP and P/dS barriers come in pairs, one per 64-column half of a step
+  static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 5, kVEmpty = 8, kSFull = 10, kPFull = 12,
+                       kAccFull = 14, kAccEmpty = 15, kSDPRead = 16, kNumBars = 17;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kTotal = kMiscOff + 16;
   static constexpr int kAlloc = kTotal + 1024;
 };
+using BwdLayout = BwdLayoutT<0>;
+static_assert(BwdLayoutT<1>::kAlloc <= 227 * 1024, "dQ shared memory");
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int k) {  // K-major operand, K-step k (16 elements)
   return sdesc_sw128(tile + (k >> 2) * BwdLayout::kHalf + (k & 3) * 32, 16, 1024);
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(384, 1)
     rlk_bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_do) {
-  using L = BwdLayout;
+  using L = BwdLayoutT<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -154,16 +164,18 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0) {
     mbar_init(&bars[L::kResFull], 1);
     mbar_init(&bars[L::kResEmpty], 1);
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < L::kKSlots; ++s) {  // dK/dV uses the first kStages of them
       mbar_init(&bars[L::kStFull + s], 1);
       mbar_init(&bars[L::kStEmpty + s], 1);
     }
+    for (int s = 0; s < L::kVSlots; ++s) mbar_init(&bars[L::kVEmpty + s], 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(&bars[L::kSFull + h], 1);
       mbar_init(&bars[L::kPFull + h], 256);  // the eight elementwise warps
     }
     mbar_init(&bars[L::kAccFull], 1);
     mbar_init(&bars[L::kAccEmpty], 256);
+    mbar_init(&bars[L::kSDPRead], 256);  // dQ: the eight elementwise warps have read S and dP
     *abort = 0;
     fence_mbar_init();
   }
@@ -176,6 +188,10 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem, tm_dp = tmem + 128, tm_acc0 = tmem + 256, tm_acc1 = tmem + 384;
+  // dQ: S (then dS over it) and dP rotate through three 128-column areas
+  // (the fourth holds the accumulator): step s puts S in area s mod 3 and
+  // dP in area (s + 1) mod 3
+  auto dq_area = [&](uint32_t i) { return tmem + (i == 2 ? 384u : 128u * i); };
   const uint32_t res_addr = smem_u32(smem + L::kResOff);
   uint8_t* st_base = smem + L::kStreamOff;
 
@@ -223,6 +239,28 @@ __global__ void __launch_bounds__(384, 1)
       }
       ++res_it;
       for (int t = 0; t < nsteps; ++t) {
+        if (KIND == 1) {
+          // K_j into slot t mod 3 (free once the accumulation of the step
+          // three back is done), V_j into slot t mod 2 (free once the dP of
+          // the step two back is done); both land on the K slot's barrier
+          const uint32_t ks = st_it % L::kKSlots, vs = st_it % L::kVSlots;
+          ok = mbar_wait(&bars[L::kStEmpty + ks], ((st_it / L::kKSlots) & 1) ^ 1, abort, p.err, 0x602);
+          ok = ok && mbar_wait(&bars[L::kVEmpty + vs], ((st_it / L::kVSlots) & 1) ^ 1, abort, p.err, 0x607);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          if (lane == 0) {
+            uint8_t* dk = st_base + ks * L::kTile;
+            uint8_t* dvs = smem + L::kVOff + vs * L::kTile;
+            const int g = it.head / p.group;
+            const int r = tok0 + t * 128;
+            mbar_arrive_expect_tx(&bars[L::kStFull + ks], 2 * L::kTile);
+            tma_load_3d(dk, &tm_k, &bars[L::kStFull + ks], 0, g, r);
+            tma_load_3d(dk + L::kHalf, &tm_k, &bars[L::kStFull + ks], 64, g, r);
+            tma_load_3d(dvs, &tm_v, &bars[L::kStFull + ks], 0, g, r);
+            tma_load_3d(dvs + L::kHalf, &tm_v, &bars[L::kStFull + ks], 64, g, r);
+          }
+          ++st_it;
+          continue;
+        }
         const uint32_t stage = st_it % L::kStages;
         ok = mbar_wait(&bars[L::kStEmpty + stage], ((st_it / L::kStages) & 1) ^ 1, abort, p.err, 0x602);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -289,7 +327,7 @@ __global__ void __launch_bounds__(384, 1)
         if (leader) umma_commit(&bars[L::kSFull + c]);
         __syncwarp();
       };
-      // K-steps 4c..4c+3 of the accumulators (first: the item's first product)
+      // dK/dV: K-steps 4c..4c+3 of the accumulators (first: the item's first product)
       auto issue_acc = [&](uint32_t st_addr, int c, bool first) {
         const int k0 = 4 * c;
         if (KIND == 0) {
@@ -307,71 +345,88 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int k = k0; k < k0 + 4; ++k)
             if (leader) umma_ts(tm_acc1, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
-        } else {
-          // dQ += dS K_j  (B = K_j MN-major: N = D, K = keys)
-#pragma unroll
-          for (int k = k0; k < k0 + 4; ++k)
-            if (leader) umma_ts(tm_acc0, tm_dp + 16 * k, mndesc(st_addr, k), kIdMN, (first && k == k0) ? 0u : 1u);
-#pragma unroll
-          for (int k = k0; k < k0 + 4; ++k)
-            if (leader) umma_ts(tm_acc0, tm_dp + 16 * k + 8, mndesc(st_addr, k), kIdMN, 1u);
         }
         __syncwarp();
       };
       auto stage_addr = [&](uint32_t si) { return smem_u32(st_base + (si % L::kStages) * 2 * L::kTile); };
       bool fail = false;
       if constexpr (KIND == 1) {
-        // dQ: one N = 128 S/dP per step and the accumulation after both
-        // halves' elementwise steps.  Its single accumulator makes S/dP the
-        // larger part of its tensor work, so the N = 64 halves' lower MMA
-        // rate costs more than their overlap gains (measured 1.6 % slower
-        // for the whole backward); the accumulation order is the halves'.
+        // dQ: one N = 128 S/dP per step.  Its single accumulator makes S/dP
+        // the larger part of its tensor work, so N = 64 halves' lower MMA
+        // rate would cost more than their overlap gains (measured 1.6 %
+        // slower for the whole backward).  With the accumulator in 128 of
+        // the 512 TMEM columns, S/dS and dP rotate through the other three
+        // areas, so step t + 1's S/dP is issued as soon as the elementwise
+        // warps have read step t's S and dP (halfway through their step), in
+        // tensor order between the two halves of step t's accumulation:
+        //   acc_0(t) S/dP(t+1) acc_1(t) | acc_0(t+1) S/dP(t+2) acc_1(t+1) | ...
         constexpr uint32_t kIdK128 = idesc_bf16(128, 128, false, false);
-        auto issue_sdp128 = [&](uint32_t st_addr, bool last) {
+        auto k_slot = [&](uint32_t si) { return smem_u32(st_base + (si % L::kKSlots) * L::kTile); };
+        auto v_slot = [&](uint32_t si) { return smem_u32(smem + L::kVOff + (si % L::kVSlots) * L::kTile); };
+        auto issue_sdp128 = [&](uint32_t si, bool last, uint32_t s) {
+          const uint32_t ts = dq_area(s % 3), tdp = dq_area((s + 1) % 3);
+          const uint32_t ka = k_slot(si), va = v_slot(si);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (leader) umma_ss(tm_s, kdesc(res_addr, k), kdesc(st_addr, k), kIdK128, k > 0);
+            if (leader) umma_ss(ts, kdesc(res_addr, k), kdesc(ka, k), kIdK128, k > 0);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (leader) umma_ss(tm_dp, kdesc(res_addr + L::kTile, k), kdesc(st_addr + L::kTile, k), kIdK128, k > 0);
+            if (leader) umma_ss(tdp, kdesc(res_addr + L::kTile, k), kdesc(va, k), kIdK128, k > 0);
           if (leader) {
             umma_commit(&bars[L::kSFull]);
             umma_commit(&bars[L::kSFull + 1]);
+            umma_commit(&bars[L::kVEmpty + si % L::kVSlots]);  // V_j is read by dP only
             if (last) umma_commit(&bars[L::kResEmpty]);  // the item's last S/dP: the resident pair is free
           }
           __syncwarp();
         };
+        // dQ += dS K_j over K-steps 4c..4c+3, with dS in area tds and K_j at ka
+        auto issue_acc_dq = [&](uint32_t ka, int c, bool first, uint32_t tds) {
+          const int k0 = 4 * c;
+#pragma unroll
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc0, tds + 16 * k, mndesc(ka, k), kIdMN, (first && k == k0) ? 0u : 1u);
+#pragma unroll
+          for (int k = k0; k < k0 + 4; ++k)
+            if (leader) umma_ts(tm_acc0, tds + 16 * k + 8, mndesc(ka, k), kIdMN, 1u);
+          __syncwarp();
+        };
         {
-          bool w = mbar_wait(&bars[L::kStFull + st_it % L::kStages], (st_it / L::kStages) & 1, abort, p.err, 0x613);
+          bool w = mbar_wait(&bars[L::kStFull + st_it % L::kKSlots], (st_it / L::kKSlots) & 1, abort, p.err, 0x613);
           if (!__all_sync(0xffffffffu, w)) break;
           tc_fence_after();
-          issue_sdp128(stage_addr(st_it), nsteps == 1);
+          issue_sdp128(st_it, nsteps == 1, s_it);
         }
         ok = mbar_wait(&bars[L::kAccEmpty], (acc_it & 1) ^ 1, abort, p.err, 0x612);
         if (!__all_sync(0xffffffffu, ok)) break;
         for (int t = 0; t < nsteps; ++t) {
           const uint32_t cur = st_it, nxt = st_it + 1;
           const bool more = t + 1 < nsteps;
-          // the elementwise warps finish column half 0 before half 1
+          const uint32_t tds = dq_area(s_it % 3);
           bool w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
-          issue_acc(stage_addr(cur), 0, t == 0);
+          issue_acc_dq(k_slot(cur), 0, t == 0, tds);
+          // this step's S and dP have been read: the next step's S/dP goes
+          // into the areas of this step's dP and of the previous step's dS
+          // (read by accumulations issued before it)
+          w = mbar_wait(&bars[L::kSDPRead], s_it & 1, abort, p.err, 0x616);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          if (more) {
+            w = mbar_wait(&bars[L::kStFull + nxt % L::kKSlots], (nxt / L::kKSlots) & 1, abort, p.err, 0x615);
+            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+            tc_fence_after();
+            issue_sdp128(nxt, t + 2 == nsteps, s_it + 1);
+          }
           w = mbar_wait(&bars[L::kPFull + 1], s_it & 1, abort, p.err, 0x614);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
-          issue_acc(stage_addr(cur), 1, false);
+          issue_acc_dq(k_slot(cur), 1, false, tds);
           if (leader) {
-            umma_commit(&bars[L::kStEmpty + cur % L::kStages]);
+            umma_commit(&bars[L::kStEmpty + cur % L::kKSlots]);  // K_j no longer read
             if (!more) umma_commit(&bars[L::kAccFull]);
           }
           __syncwarp();
-          if (more) {
-            w = mbar_wait(&bars[L::kStFull + nxt % L::kStages], (nxt / L::kStages) & 1, abort, p.err, 0x615);
-            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-            tc_fence_after();
-            issue_sdp128(stage_addr(nxt), t + 2 == nsteps);
-          }
           ++s_it;
           ++st_it;
         }
@@ -492,6 +547,9 @@ __global__ void __launch_bounds__(384, 1)
           col0 = t * 128;
         }
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        const uint32_t ts_e = (KIND == 0) ? tm_s : dq_area(s_it % 3);
+        const uint32_t tdp_e = (KIND == 0) ? tm_dp : dq_area((s_it + 1) % 3);
+        const uint32_t tds_e = (KIND == 0) ? tm_dp : ts_e;  // dQ writes dS over S
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           bool w = mbar_wait(&bars[L::kSFull + c], s_it & 1, abort, p.err, 0x621);
@@ -505,10 +563,15 @@ __global__ void __launch_bounds__(384, 1)
           else
             full = __all_sync(0xffffffffu, row_ok && col0 + colc + 31 <= row_pos);
           uint32_t sr[32], dr[32];
-          tmem_ld32(tm_s + lane_off + colc, sr);
-          tmem_ld32(tm_dp + lane_off + colc, dr);
+          tmem_ld32(ts_e + lane_off + colc, sr);
+          tmem_ld32(tdp_e + lane_off + colc, dr);
           tmem_ld_wait(sr);
           tmem_ld_wait(dr);
+          if (KIND == 1 && c == 1) {
+            // both halves of S and dP read: the MMA warp may reuse their areas
+            tc_fence_before();
+            mbar_arrive(&bars[L::kSDPRead]);
+          }
           const float* vc = vb + 64 * c;
           uint32_t pw[32], dw[32];
           // the masked form only on tiles that need it: a warp-uniform branch
@@ -566,7 +629,7 @@ __global__ void __launch_bounds__(384, 1)
           else
             arith(std::true_type{});
           if (KIND == 0) tmem_st32(tm_s + lane_off + colc, pw);
-          tmem_st32(tm_dp + lane_off + colc, dw);
+          tmem_st32(tds_e + lane_off + colc, dw);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&bars[L::kPFull + c]);
@@ -703,7 +766,7 @@ cudaError_t launch_bwd(BwdParams* bp, const std::vector<BwdItem>& tiles, int hea
     std::copy(tiles.begin() + i0, tiles.begin() + i0 + n, bp->items);
     bp->num_items = static_cast<int32_t>(n) * heads;
     const int grid = std::min(bp->num_items, num_sms);
-    kern<<<grid, 384, BwdLayout::kAlloc, stream>>>(*bp, mq, mk, mv, mdo);
+    kern<<<grid, 384, BwdLayoutT<KIND>::kAlloc, stream>>>(*bp, mq, mk, mv, mdo);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -716,9 +779,9 @@ static_assert(sizeof(BwdParams) + 4 * sizeof(CUtensorMap) + 256 <= 32764, "backw
 
 cudaError_t configure_bwd_kernels() {
   cudaError_t e = cudaFuncSetAttribute(rlk_bwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BwdLayout::kAlloc);
+                                       BwdLayoutT<0>::kAlloc);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(rlk_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kAlloc);
+  return cudaFuncSetAttribute(rlk_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayoutT<1>::kAlloc);
 }
 
 size_t backward_workspace_bytes(const rlk_attn_params* prm, const int32_t* cu) {
