@@ -126,8 +126,9 @@ struct BwdLayoutT {
   static constexpr int kVecBytes = KIND == 0 ? 2 * 8 * 2 * 64 * 4 : 0;
   static constexpr int kBarOff = kVecOff + kVecBytes;
   // barriers; S/dP and P/dS barriers come in pairs, one per 64-column half of a step
+  // (dQ's P/dS pair is double-buffered by step parity: kPFull + 2 (s & 1) + c)
   static constexpr int kResFull = 0, kResEmpty = 1, kStFull = 2, kStEmpty = 5, kVEmpty = 8, kSFull = 10, kPFull = 12,
-                       kAccFull = 14, kAccEmpty = 15, kSDPRead = 16, kNumBars = 17;
+                       kAccFull = 16, kAccEmpty = 17, kSDPRead = 18, kNumBars = 19;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kTotal = kMiscOff + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -169,13 +170,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars[L::kStEmpty + s], 1);
     }
     for (int s = 0; s < L::kVSlots; ++s) mbar_init(&bars[L::kVEmpty + s], 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&bars[L::kSFull + h], 1);
-      mbar_init(&bars[L::kPFull + h], 256);  // the eight elementwise warps
-    }
+    for (int h = 0; h < 2; ++h) mbar_init(&bars[L::kSFull + h], 1);
+    for (int h = 0; h < 4; ++h) mbar_init(&bars[L::kPFull + h], 256);  // the eight elementwise warps
     mbar_init(&bars[L::kAccFull], 1);
     mbar_init(&bars[L::kAccEmpty], 256);
-    mbar_init(&bars[L::kSDPRead], 256);  // dQ: the eight elementwise warps have read S and dP
+    mbar_init(&bars[L::kSDPRead], 256);  // dQ: the eight elementwise warps have read dP
     *abort = 0;
     fence_mbar_init();
   }
@@ -356,10 +355,12 @@ __global__ void __launch_bounds__(384, 1)
         // rate would cost more than their overlap gains (measured 1.6 %
         // slower for the whole backward).  With the accumulator in 128 of
         // the 512 TMEM columns, S/dS and dP rotate through the other three
-        // areas, so step t + 1's S/dP is issued as soon as the elementwise
-        // warps have read step t's S and dP (halfway through their step), in
-        // tensor order between the two halves of step t's accumulation:
-        //   acc_0(t) S/dP(t+1) acc_1(t) | acc_0(t+1) S/dP(t+2) acc_1(t+1) | ...
+        // areas; step t + 1's S/dP overwrites only step t's dP and step
+        // t - 1's dS, so it is issued as soon as the elementwise warps have
+        // read step t's dP (their first act), ahead of step t's accumulation:
+        //   S/dP(t+1) acc_0(t) acc_1(t) | S/dP(t+2) acc_0(t+1) acc_1(t+1) | ...
+        // The elementwise warps can then run one step ahead of the waits on
+        // their P/dS barriers, which are therefore kept per step parity.
         constexpr uint32_t kIdK128 = idesc_bf16(128, 128, false, false);
         auto k_slot = [&](uint32_t si) { return smem_u32(st_base + (si % L::kKSlots) * L::kTile); };
         auto v_slot = [&](uint32_t si) { return smem_u32(smem + L::kVOff + (si % L::kVSlots) * L::kTile); };
@@ -403,14 +404,11 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t cur = st_it, nxt = st_it + 1;
           const bool more = t + 1 < nsteps;
           const uint32_t tds = dq_area(s_it % 3);
-          bool w = mbar_wait(&bars[L::kPFull], s_it & 1, abort, p.err, 0x614);
-          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-          tc_fence_after();
-          issue_acc_dq(k_slot(cur), 0, t == 0, tds);
-          // this step's S and dP have been read: the next step's S/dP goes
-          // into the areas of this step's dP and of the previous step's dS
-          // (read by accumulations issued before it)
-          w = mbar_wait(&bars[L::kSDPRead], s_it & 1, abort, p.err, 0x616);
+          const uint32_t pf = L::kPFull + 2 * (s_it & 1), pph = (s_it >> 1) & 1;
+          // this step's dP has been read: the next step's S/dP goes into its
+          // area and into that of the previous step's dS (read by
+          // accumulations issued before it), ahead of this step's accumulation
+          bool w = mbar_wait(&bars[L::kSDPRead], s_it & 1, abort, p.err, 0x616);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           if (more) {
             w = mbar_wait(&bars[L::kStFull + nxt % L::kKSlots], (nxt / L::kKSlots) & 1, abort, p.err, 0x615);
@@ -418,7 +416,11 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             issue_sdp128(nxt, t + 2 == nsteps, s_it + 1);
           }
-          w = mbar_wait(&bars[L::kPFull + 1], s_it & 1, abort, p.err, 0x614);
+          w = mbar_wait(&bars[pf], pph, abort, p.err, 0x614);
+          if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+          tc_fence_after();
+          issue_acc_dq(k_slot(cur), 0, t == 0, tds);
+          w = mbar_wait(&bars[pf + 1], pph, abort, p.err, 0x614);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
           issue_acc_dq(k_slot(cur), 1, false, tds);
@@ -550,11 +552,29 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t ts_e = (KIND == 0) ? tm_s : dq_area(s_it % 3);
         const uint32_t tdp_e = (KIND == 0) ? tm_dp : dq_area((s_it + 1) % 3);
         const uint32_t tds_e = (KIND == 0) ? tm_dp : ts_e;  // dQ writes dS over S
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          bool w = mbar_wait(&bars[L::kSFull + c], s_it & 1, abort, p.err, 0x621);
+        // dQ: both halves of S/dP complete together; dP of both is read
+        // first, so the MMA warp can issue the next step's S/dP over it
+        // while this step's P and dS are formed
+        uint32_t dq_dp0[32], dq_dp1[32];
+        if constexpr (KIND == 1) {
+          bool w = mbar_wait(&bars[L::kSFull], s_it & 1, abort, p.err, 0x621);
+          w = w && mbar_wait(&bars[L::kSFull + 1], s_it & 1, abort, p.err, 0x621);
           if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
           tc_fence_after();
+          tmem_ld32(tdp_e + lane_off + 32 * wh, dq_dp0);
+          tmem_ld32(tdp_e + lane_off + 64 + 32 * wh, dq_dp1);
+          tmem_ld_wait(dq_dp0);
+          tmem_ld_wait(dq_dp1);
+          tc_fence_before();
+          mbar_arrive(&bars[L::kSDPRead]);
+        }
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          if (KIND == 0) {
+            bool w = mbar_wait(&bars[L::kSFull + c], s_it & 1, abort, p.err, 0x621);
+            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
+            tc_fence_after();
+          }
           const int colc = 64 * c + 32 * wh;  // first column of this warp's 32
           // every element of this warp's columns is visible: no per-element mask
           bool full;
@@ -564,13 +584,13 @@ __global__ void __launch_bounds__(384, 1)
             full = __all_sync(0xffffffffu, row_ok && col0 + colc + 31 <= row_pos);
           uint32_t sr[32], dr[32];
           tmem_ld32(ts_e + lane_off + colc, sr);
-          tmem_ld32(tdp_e + lane_off + colc, dr);
+          if (KIND == 0) tmem_ld32(tdp_e + lane_off + colc, dr);
           tmem_ld_wait(sr);
-          tmem_ld_wait(dr);
-          if (KIND == 1 && c == 1) {
-            // both halves of S and dP read: the MMA warp may reuse their areas
-            tc_fence_before();
-            mbar_arrive(&bars[L::kSDPRead]);
+          if (KIND == 0) {
+            tmem_ld_wait(dr);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dr[e] = c ? dq_dp1[e] : dq_dp0[e];
           }
           const float* vc = vb + 64 * c;
           uint32_t pw[32], dw[32];
@@ -632,7 +652,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(tds_e + lane_off + colc, dw);
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&bars[L::kPFull + c]);
+          mbar_arrive(&bars[L::kPFull + (KIND == 1 ? 2 * (s_it & 1) : 0) + c]);
         }
         if (fail) break;
         ++s_it;
