@@ -115,9 +115,9 @@ struct BwdLayoutT {
   static constexpr int kStreamOff = 2 * kTile;
   // dK/dV: two stages of the streamed pair (Q_i, dO_i).  dQ: K_j in a ring of
   // three slots (read by S and by the accumulation) and V_j in a ring of two
-  // (read by dP only): step t + 1's K loads into the slot of step t - 2 while
-  // the accumulations of steps t - 1 and t may still read theirs, so the load
-  // is not between step t's accumulation and step t + 1's S/dP.
+  // (read by dP only): step t + 1's K loads into the slot of step t - 2,
+  // released by that step's accumulation, while steps t - 1 and t may still
+  // read theirs, so the load waits for no accumulation of the last two steps.
   static constexpr int kStages = 2, kKSlots = 3, kVSlots = 2;
   static constexpr int kVOff = kStreamOff + kKSlots * kTile;  // dQ
   static constexpr int kStreamBytes = KIND == 0 ? kStages * 2 * kTile : (kKSlots + kVSlots) * kTile;
